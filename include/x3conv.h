@@ -1,0 +1,185 @@
+/*
+ * x3conv.h - C ABI of the GB300 (sm_103a) 3x3 / causal 3x3x3 convolution library.
+ *
+ * The operation (what every entry point below computes):
+ *
+ *   2D, stride s in {1,2}, pad 1 (musetalk-bench patches/taesd_conv.cuh.new, header comment and
+ *   taesd_conv3x3_impl):
+ *     y[n,co,oh,ow] = R( act( b[co] + sum_{ci,kh,kw} w[co,ci,kh,kw] * x[n,ci,s*oh+kh-1,s*ow+kw-1] ) )
+ *     with x = 0 outside the image, H_out = (H-1)/s + 1, W_out = (W-1)/s + 1.
+ *
+ *   3D causal, stride 1 (FastVideo fastvideo-kernel/wan22_vae_decode/solution/head.cu, header
+ *   comment and head_stencil_kernel; the decoder's causal convolutions with two carried frames):
+ *     xt = [carry[0], carry[1], x[0], ..., x[D-1]]   (carry absent = two zero frames)
+ *     y[n,co,t,h,w] = R( act( b[co] + sum_{ci,kt,kh,kw} w[co,ci,kt,kh,kw] * xt[n,ci,t+kt,h+kh-1,w+kw-1] ) )
+ *     for t in [0, D), spatial zero padding, no temporal padding besides the carry.
+ *
+ *   All products are accumulated in one fp32 accumulator per output, which starts at the bias;
+ *   act is none, ReLU, or clamp to [-1,1]; R is one round-to-nearest-even to the storage type
+ *   (f16 or bf16) at the store. Inputs, weights and biases are stored in the same 16-bit type.
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers are plain CUDA device (or managed) addresses owned by the caller. The
+ *     library never allocates, frees or retains device memory, except for one internal 4-byte
+ *     device status word per device.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All work is enqueued on it;
+ *     nothing synchronises. Pointers must stay valid until the enqueued work has finished.
+ *   - Functions return x3_status. On failure nothing was enqueued (for X3_ERR_INVALID and
+ *     X3_ERR_UNSUPPORTED) and conv_last_error() describes the problem. The library never aborts
+ *     the process and never traps on the device.
+ *   - Every device-side wait in the library's kernels is bounded. A wait that runs out records
+ *     X3_ERR_TIMEOUT in the device status word (read with conv_device_status) and the kernel
+ *     returns early, leaving the context usable.
+ */
+#ifndef X3CONV_H
+#define X3CONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* x3_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    X3_OK = 0,
+    X3_ERR_INVALID = 1,     /* bad argument: shape, pointer, alignment or combination */
+    X3_ERR_UNSUPPORTED = 2, /* valid, but no kernel in this build handles it (caller falls back) */
+    X3_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    X3_ERR_OOM = 4,         /* a caller-provided buffer is too small */
+    X3_ERR_TIMEOUT = 5      /* a bounded device wait ran out (see conv_device_status) */
+} x3_status;
+
+typedef enum {
+    X3_NCHW = 0,   /* 2D: [N][C][H][W] */
+    X3_NHWC = 1,   /* 2D: [N][H][W][C] */
+    X3_NCDHW = 2,  /* 3D: [N][C][D][H][W] */
+    X3_NDHWC = 3   /* 3D: [N][D][H][W][C] (channels-last) */
+} x3_layout;
+
+typedef enum { X3_F16 = 0, X3_BF16 = 1 } x3_dtype;
+
+typedef enum { X3_ACT_NONE = 0, X3_ACT_RELU = 1, X3_ACT_CLAMP1 = 2 } x3_act;
+
+typedef enum {
+    X3_KERNEL_AUTO = 0,   /* pick the fastest kernel that handles the descriptor */
+    X3_KERNEL_IGEMM = 1,  /* tcgen05/TMEM implicit GEMM (fails with X3_ERR_UNSUPPORTED if it can't) */
+    X3_KERNEL_DIRECT = 2  /* plain SIMT direct convolution; handles every valid descriptor */
+} x3_kernel;
+
+/* Descriptor of one convolution layer. */
+typedef struct {
+    int dims;          /* 2 or 3 */
+    int N;             /* batch, >= 1 */
+    int C_in, C_out;   /* >= 1 each; C_out == 12 when unpatchify2x2 is set */
+    int D;             /* 3D: output frames per call (input has D frames plus 2 carried); 2D: 1 */
+    int H, W;          /* input height and width, >= 1 */
+    int stride;        /* 1 or 2 (2D); 1 (3D) */
+    x3_layout layout;  /* input and output layout: X3_NCHW/X3_NHWC for 2D, X3_NCDHW/X3_NDHWC for 3D */
+    x3_dtype dtype;    /* storage type of x, carry, weights, bias and y */
+    x3_act act;        /* epilogue activation */
+    int has_bias;      /* 1: bias pointer required; 0: no bias */
+    int unpatchify2x2; /* head only (C_out == 12): write y as RGB at twice the resolution, channel
+                          c = rgb*4 + dy*2 + dx going to pixel (2h+dy, 2w+dx); the output is then
+                          [N][D][2H][2W][3] for X3_NDHWC and [N][3][D][2H][2W] for X3_NCDHW
+                          (2D: [N][2H][2W][3] / [N][3][2H][2W]) */
+    x3_kernel kernel;  /* kernel choice (X3_KERNEL_AUTO normally) */
+} x3_conv_desc;
+
+typedef struct x3_conv_plan x3_conv_plan; /* opaque; host memory only */
+
+/*
+ * Validate a descriptor and build a plan (tiling, kernel choice, launch shapes).
+ * Host only: launches nothing and touches no device memory. The caller owns *plan and releases
+ * it with conv_plan_destroy. Errors: X3_ERR_INVALID (bad descriptor or NULL pointer),
+ * X3_ERR_UNSUPPORTED (a forced kernel that can't handle it).
+ */
+x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan);
+
+/* Release a plan (NULL is ignored). */
+void conv_plan_destroy(x3_conv_plan* plan);
+
+/* Name of the kernel the plan runs ("igemm_tcgen05", "direct_simt"), for logs and tests. */
+const char* conv_plan_kernel_name(const x3_conv_plan* plan);
+
+/*
+ * Write a one-line JSON description of the plan (kernel, tiling, pipeline depths, shared memory,
+ * grid) into buf (at most len bytes including the terminating NUL). Returns the length the full
+ * description needs (excluding the NUL), like snprintf.
+ */
+int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len);
+
+/* Number of kernel launches one conv_forward with this plan enqueues. */
+int conv_plan_launches(const x3_conv_plan* plan);
+
+/* Bytes of the packed-weight buffer conv_pack_weights fills for this plan. */
+size_t conv_packed_weight_bytes(const x3_conv_plan* plan);
+
+/*
+ * Repack canonical weights w[C_out][C_in][(3)][3][3] (PyTorch's Conv2d/Conv3d layout, storage
+ * dtype) into the plan's kernel layout in w_packed (conv_packed_weight_bytes bytes, 256-byte
+ * aligned, caller-owned). Done once per set of weights; conv_forward then reads only w_packed.
+ * Errors: X3_ERR_INVALID (NULL or misaligned pointer), X3_ERR_CUDA.
+ */
+x3_status conv_pack_weights(const x3_conv_plan* plan, const void* w, void* w_packed,
+                            x3_stream_t stream);
+
+/*
+ * One convolution: y = conv(x [, carry]) with the fused bias / activation / rounding epilogue.
+ *   x:        input, layout and dtype of the plan; 16-byte aligned.
+ *   carry:    3D only: the two frames that precede x in time, same layout as x with 2 frames
+ *             ([N][2][H][W][C] or [N][C][2][H][W]); NULL = two zero frames. Ignored in 2D.
+ *   w_packed: from conv_pack_weights with the same plan.
+ *   bias:     C_out values (storage dtype) when has_bias, else ignored.
+ *   y:        output (D frames); must not overlap x, carry or w_packed; 16-byte aligned.
+ * Errors: X3_ERR_INVALID (NULL or misaligned pointer), X3_ERR_CUDA (launch failure).
+ */
+x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carry,
+                       const void* w_packed, const void* bias, void* y, x3_stream_t stream);
+
+/*
+ * Workspace bytes conv_stack_forward needs for these layers: two ping-pong buffers, each the size
+ * of the largest intermediate activation (every intermediate is dead as soon as the next layer
+ * has read it). Returns 0 for an invalid stack.
+ */
+size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers);
+
+/*
+ * Run n_layers chained layers: layer i reads layer i-1's output (layer 0 reads x), the last layer
+ * writes y. Consecutive plans must agree: C_out[i] == C_in[i+1], output size of i == input size of
+ * i+1, same dims, N, D, layout and dtype, and no unpatchify except on the last layer.
+ *   carries:     3D only; carries[i] is layer i's two-frame history buffer (layout of its input,
+ *                2 frames). It is read as the frames preceding this pass (as zeros when
+ *                carry_valid is 0) and then overwritten with the last two frames of the layer's
+ *                input sequence [history, input], i.e. the history of the next pass. NULL
+ *                (the array or an entry) = zero history and no carry written.
+ *   carry_valid: 0 on the first pass of a sequence, 1 afterwards.
+ *   w_packed[i], bias[i]: as for conv_forward with plans[i].
+ *   workspace:   >= conv_stack_workspace_bytes(plans, n_layers) bytes, 256-byte aligned.
+ * Errors: X3_ERR_INVALID (mismatched layers, NULL pointers), X3_ERR_OOM (workspace too small),
+ * X3_ERR_CUDA.
+ */
+x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, const void* x,
+                             void* const* carries, int carry_valid, const void* const* w_packed,
+                             const void* const* bias, void* y, void* workspace,
+                             size_t workspace_bytes, x3_stream_t stream);
+
+/*
+ * Read (and with reset != 0, clear) the current device's status word: X3_OK, or X3_ERR_TIMEOUT
+ * when a bounded device wait ran out since the last reset. Synchronises the device.
+ */
+x3_status conv_device_status(int reset);
+
+/* Thread-local description of the last error returned on this thread ("" if none). */
+const char* conv_last_error(void);
+
+/* Library version string. */
+const char* conv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* X3CONV_H */

@@ -1,0 +1,161 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every function that
+include/x3conv.h declares, validates descriptors and arguments before any launch, and plans
+tilings whose shared-memory staging covers every MMA read.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+import x3x3_convolution_gb300 as x3
+from x3x3_convolution_gb300 import build as xb
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "x3conv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    xb.build()
+    return x3.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(conv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("conv_plan_create", "conv_forward", "conv_stack_forward", "conv_plan_destroy",
+                     "conv_pack_weights", "conv_stack_workspace_bytes", "conv_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", xb.LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_version(lib):
+    assert "sm_103a" in x3.conv_version()
+
+
+def _status(desc):
+    import ctypes
+    plan = ctypes.c_void_p()
+    st = x3.load().conv_plan_create(ctypes.byref(desc), ctypes.byref(plan))
+    if plan.value:
+        x3.conv_plan_destroy(plan.value)
+    return st
+
+
+BAD = {
+    "dims4": dict(dims=4),
+    "zero_channels": dict(C_in=0),
+    "stride3": dict(stride=3),
+    "3d_stride2": dict(dims=3, layout="NDHWC", stride=2),
+    "2d_with_3d_layout": dict(layout="NDHWC"),
+    "3d_with_2d_layout": dict(dims=3, layout="NCHW"),
+    "unpatch_needs_12": dict(unpatchify2x2=True, C_out=16),
+    "zero_width": dict(W=0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BAD))
+def test_invalid_descriptors_rejected(lib, name):
+    kw = dict(dims=2, N=1, C_in=16, C_out=16, H=8, W=8, layout="NCHW", dtype="f16")
+    kw.update(BAD[name])
+    d = x3.make_desc(**kw)
+    if name == "dims4":
+        d.dims = 4
+    assert _status(d) == x3.X3_ERR_INVALID
+    assert x3.conv_last_error() != ""
+
+
+def test_forced_igemm_unsupported_is_reported(lib):
+    d = x3.make_desc(2, 1, 16, 16, 9, 9, layout="NCHW", dtype="f16", kernel="igemm")  # W % 8 != 0
+    assert _status(d) == x3.X3_ERR_UNSUPPORTED
+    d = x3.make_desc(2, 1, 16, 16, 9, 9, layout="NCHW", dtype="f16")
+    assert _status(d) == x3.X3_OK
+
+
+def test_forward_null_pointers_rejected_without_launch(lib):
+    p = x3.conv_plan_create(x3.make_desc(2, 1, 16, 16, 8, 8, dtype="f16"))
+    try:
+        st = lib.conv_forward(p, None, None, None, None, None, None)
+        assert st == x3.X3_ERR_INVALID
+        st = lib.conv_forward(p, 16, None, 256, None, 4096, None)  # bias required (has_bias=1)
+        assert st == x3.X3_ERR_INVALID
+        st = lib.conv_forward(p, 18, None, 256, 2, 4096, None)     # misaligned x
+        assert st == x3.X3_ERR_INVALID
+        st = lib.conv_pack_weights(p, 2, 100, None)                 # misaligned packed buffer
+        assert st == x3.X3_ERR_INVALID
+    finally:
+        x3.conv_plan_destroy(p)
+
+
+def test_stack_validation(lib):
+    a = x3.conv_plan_create(x3.make_desc(3, 1, 16, 32, 8, 8, D=2))
+    b = x3.conv_plan_create(x3.make_desc(3, 1, 16, 8, 8, 8, D=2))   # C_in 16 != 32
+    try:
+        with pytest.raises(x3.X3Error) as e:
+            x3.conv_stack_forward([a, b], 16, None, 0, [256, 256], [2, 2], 4096, 256, 1 << 20)
+        assert e.value.status == x3.X3_ERR_INVALID
+        c = x3.conv_plan_create(x3.make_desc(3, 1, 32, 8, 8, 8, D=2))
+        need = x3.conv_stack_workspace_bytes([a, c])
+        assert need >= 8 * 8 * 2 * 32 * 2
+        with pytest.raises(x3.X3Error) as e:
+            x3.conv_stack_forward([a, c], 16, None, 0, [256, 256], [2, 2], 4096, 256, need - 1)
+        assert e.value.status == x3.X3_ERR_OOM
+        x3.conv_plan_destroy(c)
+    finally:
+        x3.conv_plan_destroy(a)
+        x3.conv_plan_destroy(b)
+
+
+WORKLOADS = {
+    "conv2d_16x16_64": dict(dims=2, N=1, C_in=16, C_out=16, H=64, W=64, dtype="f16", layout="NCHW"),
+    "taesd_3to64_256": dict(dims=2, N=4, C_in=3, C_out=64, H=256, W=256, dtype="f16", layout="NCHW"),
+    "taesd_64_256": dict(dims=2, N=4, C_in=64, C_out=64, H=256, W=256, dtype="f16", layout="NCHW"),
+    "taesd_64_128": dict(dims=2, N=4, C_in=64, C_out=64, H=128, W=128, dtype="f16", layout="NCHW"),
+    "causal_256_88x156": dict(dims=3, N=1, C_in=256, C_out=256, D=4, H=88, W=156),
+    "causal_128_352x624": dict(dims=3, N=1, C_in=128, C_out=128, D=4, H=352, W=624),
+    "causal_256to128_176x312": dict(dims=3, N=1, C_in=256, C_out=128, D=4, H=176, W=312),
+    "head_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True),
+    "ragged_3d": dict(dims=3, N=2, C_in=40, C_out=72, D=3, H=7, W=301),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_igemm_plans_cover_their_reads(lib, name):
+    p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
+    try:
+        g = x3.conv_plan_describe(p)
+        assert g["kernel"] == "igemm_tcgen05"
+        P, Rt, Wt, NSUB, spr = g["P"], g["Rt"], g["Wt"], g["NSUB"], g["spr"]
+        assert P == Wt + 2 and P <= 256
+        # every output of the tile is covered by a subtile row
+        offs = [((s // spr) * P + (s % spr) * 128) if spr else 128 * s for s in range(NSUB)]
+        covered = set()
+        for o in offs:
+            covered.update(range(o, o + 128))
+        for r in range(Rt):
+            for c in range(Wt):
+                assert r * P + c in covered
+        # the furthest A read (tap kh=2, kw=2 of the last subtile row) stays inside one A stage
+        max_read = max(offs) + 127 + 2 * P + 2
+        kpl = g["CK"] // 8
+        assert (kpl - 1) * g["plane_stride"] + (max_read + 1) * 16 <= g["a_bytes"]
+        assert g["tmem_cols"] <= 512 and g["NSUB"] * g["BN"] * g["acc_bufs"] <= g["tmem_cols"]
+        assert g["smem_bytes"] <= 232448
+        assert g["tiles"] == g["col_tiles"] * g["row_tiles"] * g["frames"] * g["n_tiles"]
+        assert g["col_tiles"] * Wt >= g["W_out"] and g["row_tiles"] * Rt >= g["H_out"]
+    finally:
+        x3.conv_plan_destroy(p)

@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Integer-valued inputs ({-2..2}) must match bit for bit (every fp32 partial sum is exact, so only
+indexing, halo, padding, carry and epilogue can differ); random inputs must meet the relative
+max / rms tolerances. Sizes span several tiles and a ragged tail; both the tcgen05 kernel and the
+direct kernel are checked.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import x3x3_convolution_gb300 as x3
+from x3x3_convolution_gb300 import synth
+from tests.gpu_helpers import (assert_close, assert_exact, dev, host_values, oracle_sampled_3d, psnr,
+                               sample_positions, PSNR_MIN)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    x3.load()
+    yield
+    assert x3.conv_device_status(1) == x3.X3_OK
+
+
+def run2d(x, L, layout="NCHW", kernel="auto", expect=None):
+    N, C, H, W = x.shape if layout == "NCHW" else (x.shape[0], x.shape[3], x.shape[1], x.shape[2])
+    d = x3.make_desc(2, N, C, L.C_out, H, W, stride=L.stride, layout=layout, dtype=x.dtype, act=L.act,
+                     has_bias=L.b is not None, kernel=kernel)
+    conv = x3.Conv(d, dev(L.w), None if L.b is None else dev(L.b))
+    if expect:
+        assert conv.kernel_name == expect, conv.kernel_name
+    y = conv(dev(x))
+    torch.cuda.synchronize()
+    return host_values(y, x.dtype), conv
+
+
+def oracle2d(x, L, layout="NCHW"):
+    return oracle.conv2d(x.vals, L.w.vals, None if L.b is None else L.b.vals, stride=L.stride, act=L.act,
+                         layout=layout)
+
+
+# ------------------------------------------------------------------ 2D
+
+CASES_2D = [
+    # (N, C_in, C_out, H, W, stride, act)
+    (1, 16, 16, 64, 64, 1, "relu"),      # the 16->16 64x64 single conv
+    (2, 3, 64, 40, 264, 1, "relu"),      # 3-channel input, ragged width (264 = 2*128 + 8)
+    (1, 64, 64, 37, 136, 1, "relu"),     # ragged height and width
+    (2, 64, 48, 16, 64, 1, "none"),      # C_out not a multiple of the N tile
+    (1, 24, 16, 9, 8, 1, "relu"),        # C_in not a multiple of the channel chunk
+    (1, 1, 16, 1, 8, 1, "none"),         # a single row
+    (2, 64, 64, 34, 70, 2, "relu"),      # stride 2
+]
+
+
+@pytest.mark.parametrize("variant", ["int", "random"])
+@pytest.mark.parametrize("case", CASES_2D, ids=lambda c: "x".join(map(str, c[:6])))
+@pytest.mark.parametrize("kernel", ["auto", "direct"])
+def test_conv2d_nchw(case, variant, kernel):
+    N, Ci, Co, H, W, s, act = case
+    x, L = synth.conv2d_single(N=N, C=Ci, C_out=Co, H=H, W=W, stride=s, act=act, variant=variant,
+                               seed=2000 + sum(case[:6]))
+    got, conv = run2d(x, L, kernel=kernel)
+    if kernel == "auto" and s == 1:
+        assert conv.kernel_name == "igemm_tcgen05"
+    ref = oracle2d(x, L)
+    if variant == "int":
+        assert_exact(got, ref, "f16")
+    else:
+        assert_close(got, ref)
+
+
+@pytest.mark.parametrize("variant", ["int", "random"])
+@pytest.mark.parametrize("case", [(2, 16, 32, 20, 150, "relu"), (1, 64, 64, 9, 300, "none"),
+                                  (1, 8, 16, 3, 5, "none")], ids=str)
+def test_conv2d_nhwc_bf16(case, variant):
+    N, Ci, Co, H, W, act = case
+    key = 2100 + sum(case[:5])
+    x = synth.activation([key, 0], (N, H, W, Ci), "bf16", variant, ("uniform", -1.0, 1.0))
+    L = synth.make_layer([key], 2, Ci, Co, "bf16", act=act, variant=variant)
+    got, conv = run2d(x, L, layout="NHWC")
+    assert conv.kernel_name == "igemm_tcgen05"
+    ref = oracle2d(x, L, layout="NHWC")
+    if variant == "int":
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+
+
+# ------------------------------------------------------------------ 3D causal
+
+def run3d(x, carry, L, kernel="auto", unpatch=False, dtype="bf16"):
+    N, D, H, W, C = x.shape
+    d = x3.make_desc(3, N, C, L.C_out, H, W, D=D, layout="NDHWC", dtype=dtype, act=L.act,
+                     has_bias=L.b is not None, unpatchify2x2=unpatch, kernel=kernel)
+    conv = x3.Conv(d, dev(L.w), None if L.b is None else dev(L.b))
+    y = conv(dev(x), None if carry is None else dev(carry))
+    torch.cuda.synchronize()
+    return host_values(y, dtype), conv
+
+
+def oracle3d(x, carry, L):
+    return oracle.conv3d_causal(x.vals, L.w.vals, None if L.b is None else L.b.vals,
+                                carry=None if carry is None else carry.vals, act=L.act, layout="NDHWC")
+
+
+CASES_3D = [
+    # (N, C_in, C_out, D, H, W, act, with_carry)
+    (1, 128, 128, 2, 10, 300, "relu", True),
+    (1, 128, 128, 2, 10, 300, "relu", False),
+    (1, 256, 256, 1, 6, 156, "none", True),
+    (2, 32, 64, 3, 7, 41, "none", True),
+    (1, 40, 72, 2, 5, 19, "relu", True),      # channels not multiples of the chunk / N tile
+    (1, 16, 16, 4, 1, 8, "none", True),       # a single row
+    (1, 256, 128, 2, 9, 130, "none", True),
+]
+
+
+@pytest.mark.parametrize("variant", ["int", "random"])
+@pytest.mark.parametrize("case", CASES_3D, ids=lambda c: "x".join(map(str, c[:6])) + ("c" if c[7] else "z"))
+@pytest.mark.parametrize("kernel", ["auto", "direct"])
+def test_conv3d_causal(case, variant, kernel):
+    N, Ci, Co, D, H, W, act, with_carry = case
+    if kernel == "direct" and Ci * Co * H * W > 2_000_000:
+        pytest.skip("the direct kernel is checked on the smaller shapes")
+    x, carry, L = synth.conv3d_single(C_in=Ci, C_out=Co, D=D, H=H, W=W, N=N, variant=variant, act=act,
+                                      seed=3000 + sum(case[:6]), with_carry=with_carry)
+    got, conv = run3d(x, carry, L, kernel=kernel)
+    if kernel == "auto":
+        assert conv.kernel_name == "igemm_tcgen05"
+    ref = oracle3d(x, carry, L)
+    if variant == "int":
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+
+
+@pytest.mark.parametrize("variant", ["sparse1", "random"])
+def test_head_clamp_unpatchify(variant):
+    x, carry, L = synth.head(D=2, H=9, W=140, variant=variant, seed=3500)
+    got, conv = run3d(x, carry, L, unpatch=True)
+    assert conv.kernel_name == "igemm_tcgen05"
+    ref12 = oracle3d(x, carry, L)                                   # [1, D, H, W, 12]
+    ref = oracle.unpatchify2x2(ref12.transpose(0, 4, 1, 2, 3))      # [1, 3, D, 2H, 2W]
+    ref = ref.transpose(0, 2, 3, 4, 1)                              # [1, D, 2H, 2W, 3]
+    assert got.shape == ref.shape
+    if variant == "sparse1":
+        assert_exact(got, ref, "bf16")
+        assert np.max(np.abs(ref)) <= 1.0
+    else:
+        assert_close(got, ref)
+        assert psnr(got, ref) >= PSNR_MIN
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+
+FULL_3D = {
+    "causal_256_4x88x156": dict(C_in=256, C_out=256, D=4, H=88, W=156, act="none"),
+    "causal_128_4x352x624": dict(C_in=128, C_out=128, D=4, H=352, W=624, act="relu"),
+    "causal_256to128_4x176x312": dict(C_in=256, C_out=128, D=4, H=176, W=312, act="none"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL_3D))
+def test_full_size_sampled(name):
+    cfg = FULL_3D[name]
+    x, carry, L = synth.conv3d_single(N=1, seed=3900 + len(name), **cfg)
+    got, conv = run3d(x, carry, L)
+    assert conv.kernel_name == "igemm_tcgen05"
+    seq = np.concatenate([carry.vals, x.vals], axis=1)
+    pos = sample_positions(cfg["D"], cfg["H"], cfg["W"], 400, seed=len(name))
+    ref = oracle_sampled_3d(seq, L.w.vals, L.b.vals, cfg["act"], pos)
+    g = np.stack([got[0, t, h, w] for (t, h, w) in pos])
+    assert_close(g, ref)
+
+
+def test_full_size_head_sampled():
+    x, carry, L = synth.head(seed=3950)
+    got, conv = run3d(x, carry, L, unpatch=True)
+    assert conv.kernel_name == "igemm_tcgen05"
+    assert got.shape == (1, 4, 704, 1248, 3)
+    seq = np.concatenate([carry.vals, x.vals], axis=1)
+    pos = sample_positions(4, 352, 624, 400, seed=7)
+    ref = oracle_sampled_3d(seq, L.w.vals, L.b.vals, "clamp", pos)
+    g = np.stack([[got[0, t, 2 * h + (c // 2) % 2, 2 * w + c % 2, c // 4] for c in range(12)] for (t, h, w) in pos])
+    assert_close(g, ref)
+    assert psnr(g, ref) >= PSNR_MIN

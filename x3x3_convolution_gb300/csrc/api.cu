@@ -1,0 +1,291 @@
+// Host side of libx3conv: descriptor validation, plans, dispatch and the causal stack driver.
+//
+// Shape checks mirror the host wrapper of FastVideo wan22_vae_decode/solution/head.cu
+// (head_stencil: layout and size checks before any launch, device of the caller, launch on the
+// caller's stream, launch check afterwards), extended to close the hazard that wrapper's own
+// comment names: a tensor whose depth or height disagrees with the plan is rejected here rather
+// than read out of bounds.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "internal.h"
+
+namespace x3 {
+
+static thread_local char g_err[512] = "";
+
+x3_status fail(x3_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+static void clear_err() { g_err[0] = 0; }
+
+size_t in_elems(const x3_conv_plan* p) {
+    const x3_conv_desc& d = p->d;
+    return (size_t)d.N * d.C_in * (d.dims == 3 ? d.D : 1) * d.H * d.W;
+}
+
+size_t out_elems(const x3_conv_plan* p) {
+    const x3_conv_desc& d = p->d;
+    return (size_t)d.N * d.C_out * (d.dims == 3 ? d.D : 1) * p->H_out * p->W_out;
+}
+
+static bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+static x3_status validate(const x3_conv_desc* d) {
+    if (!d) return fail(X3_ERR_INVALID, "descriptor is NULL");
+    if (d->dims != 2 && d->dims != 3) return fail(X3_ERR_INVALID, "dims must be 2 or 3 (got %d)", d->dims);
+    if (d->N < 1 || d->C_in < 1 || d->C_out < 1 || d->H < 1 || d->W < 1)
+        return fail(X3_ERR_INVALID, "N, C_in, C_out, H, W must be >= 1");
+    if (d->dims == 2) {
+        if (d->D != 1 && d->D != 0) return fail(X3_ERR_INVALID, "2D descriptors have D = 1");
+        if (d->stride != 1 && d->stride != 2) return fail(X3_ERR_INVALID, "stride must be 1 or 2");
+        if (d->layout != X3_NCHW && d->layout != X3_NHWC)
+            return fail(X3_ERR_INVALID, "2D layout must be X3_NCHW or X3_NHWC");
+    } else {
+        if (d->D < 1) return fail(X3_ERR_INVALID, "3D descriptors need D >= 1");
+        if (d->stride != 1) return fail(X3_ERR_INVALID, "causal 3D convolution has stride 1");
+        if (d->layout != X3_NCDHW && d->layout != X3_NDHWC)
+            return fail(X3_ERR_INVALID, "3D layout must be X3_NCDHW or X3_NDHWC");
+    }
+    if (d->dtype != X3_F16 && d->dtype != X3_BF16) return fail(X3_ERR_INVALID, "dtype must be f16 or bf16");
+    if (d->act < X3_ACT_NONE || d->act > X3_ACT_CLAMP1) return fail(X3_ERR_INVALID, "bad activation");
+    if (d->has_bias != 0 && d->has_bias != 1) return fail(X3_ERR_INVALID, "has_bias must be 0 or 1");
+    if (d->unpatchify2x2 != 0 && d->unpatchify2x2 != 1) return fail(X3_ERR_INVALID, "unpatchify2x2 must be 0 or 1");
+    if (d->unpatchify2x2 && d->C_out != 12) return fail(X3_ERR_INVALID, "unpatchify2x2 needs C_out == 12");
+    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_DIRECT) return fail(X3_ERR_INVALID, "bad kernel choice");
+    // Every tensor must be indexable with 63-bit offsets and every per-image plane with 31 bits.
+    const long long frames = (long long)d->N * (d->dims == 3 ? d->D + 2 : 1);
+    const long long plane = (long long)d->H * d->W;
+    if (plane > (1LL << 30) || frames > (1LL << 30) || (long long)d->C_in > 65536 || (long long)d->C_out > 65536)
+        return fail(X3_ERR_INVALID, "tensor too large");
+    if ((double)frames * plane * (d->C_in > d->C_out ? d->C_in : d->C_out) > 9.0e18)
+        return fail(X3_ERR_INVALID, "tensor too large");
+    return X3_OK;
+}
+
+static int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return sms;
+}
+
+static size_t direct_packed_bytes(const x3_conv_desc& d) {
+    return (size_t)d.C_out * d.C_in * (d.dims == 3 ? 27 : 9) * 2;
+}
+
+}  // namespace x3
+
+using namespace x3;
+
+extern "C" {
+
+x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
+    clear_err();
+    if (!plan) return fail(X3_ERR_INVALID, "plan output pointer is NULL");
+    *plan = nullptr;
+    x3_status st = validate(desc);
+    if (st != X3_OK) return st;
+    x3_conv_plan* p = new (std::nothrow) x3_conv_plan();
+    if (!p) return fail(X3_ERR_OOM, "out of host memory");
+    p->d = *desc;
+    if (p->d.dims == 2) p->d.D = 1;
+    p->H_out = (p->d.H - 1) / p->d.stride + 1;
+    p->W_out = (p->d.W - 1) / p->d.stride + 1;
+    p->num_sms = device_sms();
+    bool igemm_ok = false;
+    const char* force = getenv("X3CONV_FORCE_KERNEL");
+    x3_kernel choice = p->d.kernel;
+    if (choice == X3_KERNEL_AUTO && force) {
+        if (!strcmp(force, "direct")) choice = X3_KERNEL_DIRECT;
+        else if (!strcmp(force, "igemm")) choice = X3_KERNEL_IGEMM;
+    }
+    if (choice != X3_KERNEL_DIRECT) igemm_ok = igemm_plan(p, p->num_sms);
+    if (choice == X3_KERNEL_IGEMM && !igemm_ok) {
+        delete p;
+        return fail(X3_ERR_UNSUPPORTED, "the tcgen05 implicit-GEMM kernel does not handle this descriptor");
+    }
+    if (igemm_ok) {
+        p->kind = K_IGEMM;
+        const IgemmGeom& g = p->g;
+        p->packed_bytes = (size_t)g.n_tiles * g.KT * g.n_chunks * 9 * g.b_bytes;
+    } else {
+        p->kind = K_DIRECT;
+        p->packed_bytes = direct_packed_bytes(p->d);
+    }
+    *plan = p;
+    return X3_OK;
+}
+
+void conv_plan_destroy(x3_conv_plan* plan) { delete plan; }
+
+const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
+    if (!plan) return "";
+    return plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
+}
+
+int conv_plan_launches(const x3_conv_plan* plan) { return plan ? 1 : 0; }
+
+int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
+    if (!plan) return snprintf(buf, len, "{}");
+    const IgemmGeom& g = plan->g;
+    if (plan->kind != K_IGEMM)
+        return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
+                        plan->H_out, plan->W_out, plan->num_sms);
+    return snprintf(buf, len,
+                    "{\"kernel\": \"igemm_tcgen05\", \"mode\": \"%s\", \"BN\": %d, \"n_tiles\": %d, \"CK\": %d, "
+                    "\"n_chunks\": %d, \"KT\": %d, \"NSUB\": %d, \"Rt\": %d, \"Wt\": %d, \"P\": %d, \"spr\": %d, "
+                    "\"plane_stride\": %d, \"a_bytes\": %d, \"raw_bytes\": %d, \"b_bytes\": %d, \"n_a\": %d, "
+                    "\"n_b\": %d, \"n_raw\": %d, \"acc_bufs\": %d, \"tmem_cols\": %d, \"col_tiles\": %d, "
+                    "\"row_tiles\": %d, \"frames\": %d, \"tiles\": %lld, \"smem_bytes\": %d, \"grid\": %d, "
+                    "\"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
+                    g.mode == STAGE_CL ? "channels_last_tma" : "nchw_tma_transpose", g.BN, g.n_tiles, g.CK,
+                    g.n_chunks, g.KT, g.NSUB, g.Rt, g.Wt, g.P, g.spr, g.plane_stride, g.a_bytes, g.raw_bytes,
+                    g.b_bytes, g.n_a, g.n_b, g.n_raw, g.acc_bufs, g.tmem_cols, g.col_tiles, g.row_tiles, g.frames,
+                    g.tiles, g.smem_bytes, g.grid, plan->H_out, plan->W_out, plan->num_sms);
+}
+
+size_t conv_packed_weight_bytes(const x3_conv_plan* plan) { return plan ? plan->packed_bytes : 0; }
+
+x3_status conv_pack_weights(const x3_conv_plan* plan, const void* w, void* w_packed, x3_stream_t stream) {
+    clear_err();
+    if (!plan || !w || !w_packed) return fail(X3_ERR_INVALID, "conv_pack_weights: NULL argument");
+    if (!aligned(w, 2) || !aligned(w_packed, 256))
+        return fail(X3_ERR_INVALID, "conv_pack_weights: w must be 2-byte and w_packed 256-byte aligned");
+    return launch_pack_weights(plan, w, w_packed, (cudaStream_t)stream);
+}
+
+x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carry, const void* w_packed,
+                       const void* bias, void* y, x3_stream_t stream) {
+    clear_err();
+    if (!plan || !x || !w_packed || !y) return fail(X3_ERR_INVALID, "conv_forward: NULL argument");
+    if (plan->d.has_bias && !bias) return fail(X3_ERR_INVALID, "conv_forward: plan has a bias but bias is NULL");
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w_packed, 256) || (carry && !aligned(carry, 16)) ||
+        (bias && !aligned(bias, 2)))
+        return fail(X3_ERR_INVALID, "conv_forward: x, y, carry need 16-byte alignment, w_packed 256-byte");
+    const void* c = plan->d.dims == 3 ? carry : nullptr;
+    const char* lo_y = (const char*)y;
+    const char* hi_y = lo_y + out_elems(plan) * 2;
+    const char* lo_x = (const char*)x;
+    const char* hi_x = lo_x + in_elems(plan) * 2;
+    if (lo_y < hi_x && lo_x < hi_y) return fail(X3_ERR_INVALID, "conv_forward: y overlaps x");
+    if (plan->kind == K_IGEMM) return launch_igemm(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
+    return launch_direct(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
+}
+
+size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers) {
+    if (!plans || n_layers < 1) return 0;
+    size_t biggest = 0;
+    for (int i = 0; i + 1 < n_layers; ++i) {
+        if (!plans[i]) return 0;
+        size_t b = out_elems(plans[i]) * 2;
+        b = (b + 255) & ~(size_t)255;
+        if (b > biggest) biggest = b;
+    }
+    return n_layers > 1 ? (n_layers > 2 ? 2 * biggest : biggest) : 0;
+}
+
+// Copy the last two frames of the sequence [history, input] of a layer into its carry buffer.
+static x3_status update_carry(const x3_conv_plan* p, const void* input, void* carry, int history_valid,
+                              cudaStream_t s) {
+    const x3_conv_desc& d = p->d;
+    const size_t plane = (size_t)d.H * d.W * 2;  // bytes of one channel plane of one frame
+    const int D = d.D;
+    cudaError_t e = cudaSuccess;
+    if (d.layout == X3_NDHWC) {
+        const size_t frame = plane * d.C_in;
+        if (D >= 2) {
+            e = cudaMemcpy2DAsync(carry, 2 * frame, (const char*)input + (size_t)(D - 2) * frame, (size_t)D * frame,
+                                  2 * frame, d.N, cudaMemcpyDeviceToDevice, s);
+        } else {
+            if (history_valid)
+                e = cudaMemcpy2DAsync(carry, 2 * frame, (const char*)carry + frame, 2 * frame, frame, d.N,
+                                      cudaMemcpyDeviceToDevice, s);
+            else
+                e = cudaMemset2DAsync(carry, 2 * frame, 0, frame, d.N, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpy2DAsync((char*)carry + frame, 2 * frame, input, frame, frame, d.N,
+                                      cudaMemcpyDeviceToDevice, s);
+        }
+    } else {  // NCDHW: rows are (n, c) with D or 2 frames each
+        const size_t rows = (size_t)d.N * d.C_in;
+        if (D >= 2) {
+            e = cudaMemcpy2DAsync(carry, 2 * plane, (const char*)input + (size_t)(D - 2) * plane, (size_t)D * plane,
+                                  2 * plane, rows, cudaMemcpyDeviceToDevice, s);
+        } else {
+            if (history_valid)
+                e = cudaMemcpy2DAsync(carry, 2 * plane, (const char*)carry + plane, 2 * plane, plane, rows,
+                                      cudaMemcpyDeviceToDevice, s);
+            else
+                e = cudaMemset2DAsync(carry, 2 * plane, 0, plane, rows, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpy2DAsync((char*)carry + plane, 2 * plane, input, plane, plane, rows,
+                                      cudaMemcpyDeviceToDevice, s);
+        }
+    }
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "carry update: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
+x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, const void* x, void* const* carries,
+                             int carry_valid, const void* const* w_packed, const void* const* bias, void* y,
+                             void* workspace, size_t workspace_bytes, x3_stream_t stream) {
+    clear_err();
+    if (!plans || n_layers < 1 || !x || !y || !w_packed || (!bias && n_layers > 0 && plans[0] && plans[0]->d.has_bias))
+        return fail(X3_ERR_INVALID, "conv_stack_forward: NULL argument");
+    for (int i = 0; i < n_layers; ++i) {
+        if (!plans[i] || !w_packed[i]) return fail(X3_ERR_INVALID, "conv_stack_forward: layer %d plan or weights NULL", i);
+        if (plans[i]->d.has_bias && (!bias || !bias[i])) return fail(X3_ERR_INVALID, "conv_stack_forward: layer %d bias NULL", i);
+        if (i + 1 < n_layers) {
+            const x3_conv_desc& a = plans[i]->d;
+            const x3_conv_desc& b = plans[i + 1]->d;
+            if (a.dims != b.dims || a.N != b.N || a.D != b.D || a.layout != b.layout || a.dtype != b.dtype ||
+                a.C_out != b.C_in || plans[i]->H_out != b.H || plans[i]->W_out != b.W || a.unpatchify2x2)
+                return fail(X3_ERR_INVALID, "conv_stack_forward: layer %d output does not match layer %d input", i, i + 1);
+        }
+    }
+    const size_t need = conv_stack_workspace_bytes(plans, n_layers);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(X3_ERR_OOM, "conv_stack_forward: workspace needs %zu bytes, got %zu", need, workspace_bytes);
+    if (workspace && !aligned(workspace, 256)) return fail(X3_ERR_INVALID, "conv_stack_forward: workspace must be 256-byte aligned");
+    const size_t half = n_layers > 2 ? need / 2 : need;
+    cudaStream_t s = (cudaStream_t)stream;
+    const void* in = x;
+    for (int i = 0; i < n_layers; ++i) {
+        void* out = (i == n_layers - 1) ? y : (char*)workspace + (size_t)(i % 2) * half;
+        void* carry = (plans[i]->d.dims == 3 && carries) ? carries[i] : nullptr;
+        x3_status st = conv_forward(plans[i], in, (carry && carry_valid) ? carry : nullptr, w_packed[i],
+                                    bias ? bias[i] : nullptr, out, stream);
+        if (st != X3_OK) return st;
+        if (carry) {
+            st = update_carry(plans[i], in, carry, carry_valid, s);
+            if (st != X3_OK) return st;
+        }
+        in = out;
+    }
+    return X3_OK;
+}
+
+x3_status conv_device_status(int reset) {
+    clear_err();
+    return read_device_status(reset);
+}
+
+const char* conv_last_error(void) { return g_err; }
+
+const char* conv_version(void) { return "x3conv 0.1 (sm_103a)"; }
+
+}  // extern "C"

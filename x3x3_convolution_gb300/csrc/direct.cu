@@ -1,0 +1,177 @@
+// Generic direct convolution (SIMT, fp32 accumulation) and the weight-packing kernels.
+//
+// The direct kernel is the library's total fallback: it handles every descriptor the ABI accepts
+// (2D/3D, either layout, f16/bf16, stride 1/2, any channel count, the unpatchify store). One
+// thread computes one output value with the summation of musetalk-bench
+// patches/taesd_conv.cuh.new, taesd_conv3x3_impl (accumulator starts at the bias, loops over
+// input channel and the 3x3 window with zero padding, ReLU, round-to-nearest store), widened to
+// the causal 3x3x3 window of FastVideo wan22_vae_decode/solution/head.cu (two carried frames
+// before the current ones, clamp to [-1,1] for the head).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace x3 {
+
+struct DirectArgs {
+    int dims, N, C_in, C_out, D, H, W, H_out, W_out, stride, act, unpatch, channels_last, has_carry;
+};
+
+__device__ __forceinline__ float ld_val(const __half* p, size_t i) { return __half2float(p[i]); }
+__device__ __forceinline__ float ld_val(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_val(__half* p, size_t i, float v) { p[i] = __float2half_rn(v); }
+__device__ __forceinline__ void st_val(__nv_bfloat16* p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) direct_conv_kernel(const T* __restrict__ x, const T* __restrict__ carry,
+                                                          const T* __restrict__ w, const T* __restrict__ bias,
+                                                          T* __restrict__ y, DirectArgs a) {
+    const int KT = a.dims == 3 ? 3 : 1;
+    const int Dout = a.dims == 3 ? a.D : 1;
+    const size_t total = (size_t)a.N * a.C_out * Dout * a.H_out * a.W_out;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        int n, co, t, oh, ow;
+        size_t r = idx;
+        if (a.channels_last) {
+            co = (int)(r % a.C_out); r /= a.C_out;
+            ow = (int)(r % a.W_out); r /= a.W_out;
+            oh = (int)(r % a.H_out); r /= a.H_out;
+            t = (int)(r % Dout); r /= Dout;
+            n = (int)r;
+        } else {
+            ow = (int)(r % a.W_out); r /= a.W_out;
+            oh = (int)(r % a.H_out); r /= a.H_out;
+            t = (int)(r % Dout); r /= Dout;
+            co = (int)(r % a.C_out); r /= a.C_out;
+            n = (int)r;
+        }
+        float acc = bias ? ld_val(bias, co) : 0.0f;
+        for (int ci = 0; ci < a.C_in; ++ci) {
+            for (int kt = 0; kt < KT; ++kt) {
+                // frame kt of the window: 3D reads [carry0, carry1, x0..] at t+kt; 2D reads x itself
+                const T* src;
+                int F, f;
+                if (a.dims == 3) {
+                    const int fr = t + kt;
+                    if (fr < 2) {
+                        if (!a.has_carry) continue;
+                        src = carry; F = 2; f = fr;
+                    } else {
+                        src = x; F = a.D; f = fr - 2;
+                    }
+                } else {
+                    src = x; F = 1; f = 0;
+                }
+                for (int kh = 0; kh < 3; ++kh) {
+                    const int ih = a.stride * oh + kh - 1;
+                    if (ih < 0 || ih >= a.H) continue;
+                    for (int kw = 0; kw < 3; ++kw) {
+                        const int iw = a.stride * ow + kw - 1;
+                        if (iw < 0 || iw >= a.W) continue;
+                        size_t xi;
+                        if (a.channels_last)
+                            xi = ((((size_t)n * F + f) * a.H + ih) * a.W + iw) * a.C_in + ci;
+                        else
+                            xi = (((size_t)n * a.C_in + ci) * F + f) * (size_t)a.H * a.W + (size_t)ih * a.W + iw;
+                        const size_t wi = (((size_t)co * a.C_in + ci) * KT + kt) * 9 + kh * 3 + kw;
+                        acc += ld_val(w, wi) * ld_val(src, xi);
+                    }
+                }
+            }
+        }
+        if (a.act == X3_ACT_RELU) acc = acc < 0.0f ? 0.0f : acc;
+        else if (a.act == X3_ACT_CLAMP1) acc = fminf(1.0f, fmaxf(-1.0f, acc));
+        size_t yi;
+        if (a.unpatch) {
+            const int rgb = co / 4, dy = (co / 2) % 2, dx = co % 2;
+            const size_t H2 = 2 * (size_t)a.H_out, W2 = 2 * (size_t)a.W_out;
+            const size_t hh = 2 * (size_t)oh + dy, ww = 2 * (size_t)ow + dx;
+            if (a.channels_last)
+                yi = ((((size_t)n * Dout + t) * H2 + hh) * W2 + ww) * 3 + rgb;
+            else
+                yi = ((((size_t)n * 3 + rgb) * Dout + t) * H2 + hh) * W2 + ww;
+        } else if (a.channels_last) {
+            yi = ((((size_t)n * Dout + t) * a.H_out + oh) * a.W_out + ow) * a.C_out + co;
+        } else {
+            yi = ((((size_t)n * a.C_out + co) * Dout + t) * a.H_out + oh) * (size_t)a.W_out + ow;
+        }
+        st_val(y, yi, acc);
+    }
+}
+
+x3_status launch_direct(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                        const void* bias, void* y, cudaStream_t s) {
+    const x3_conv_desc& d = p->d;
+    DirectArgs a;
+    a.dims = d.dims; a.N = d.N; a.C_in = d.C_in; a.C_out = d.C_out; a.D = d.D; a.H = d.H; a.W = d.W;
+    a.H_out = p->H_out; a.W_out = p->W_out; a.stride = d.stride; a.act = d.act; a.unpatch = d.unpatchify2x2;
+    a.channels_last = (d.layout == X3_NHWC || d.layout == X3_NDHWC);
+    a.has_carry = carry != nullptr;
+    const size_t total = out_elems(p);
+    const int threads = 256;
+    size_t blocks = (total + threads - 1) / threads;
+    const size_t cap = (size_t)p->num_sms * 64;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (d.dtype == X3_F16)
+        direct_conv_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)x, (const __half*)carry,
+                                                                        (const __half*)w_packed, (const __half*)bias,
+                                                                        (__half*)y, a);
+    else
+        direct_conv_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)carry, (const __nv_bfloat16*)w_packed,
+            (const __nv_bfloat16*)bias, (__nv_bfloat16*)y, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "direct kernel launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
+// ------------------------------------------------------------------ weight packing
+
+// Packed layout of the implicit-GEMM weights: blocks ordered [n-tile][kt][chunk][kh*3+kw]; one
+// block is the K-major no-swizzle canonical tile of BN output channels x CK input channels:
+// [CK/8 planes][BN rows][8 consecutive input channels]. Channels past C_out / C_in are zero.
+struct PackArgs {
+    int C_in, C_out, KT, BN, CK, n_chunks, n_tiles;
+};
+
+__global__ void __launch_bounds__(256) pack_igemm_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                         PackArgs a, size_t total) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        size_t r = i;
+        const int e = (int)(r % 8); r /= 8;
+        const int nrow = (int)(r % a.BN); r /= a.BN;
+        const int j = (int)(r % (a.CK / 8)); r /= (a.CK / 8);
+        const int tap = (int)(r % 9); r /= 9;
+        const int cc = (int)(r % a.n_chunks); r /= a.n_chunks;
+        const int kt = (int)(r % a.KT); r /= a.KT;
+        const int nt = (int)r;
+        const int co = nt * a.BN + nrow;
+        const int ci = cc * a.CK + j * 8 + e;
+        uint16_t v = 0;
+        if (co < a.C_out && ci < a.C_in) v = w[(((size_t)co * a.C_in + ci) * a.KT + kt) * 9 + tap];
+        out[i] = v;
+    }
+}
+
+x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s) {
+    if (p->kind == K_DIRECT) {
+        cudaError_t e = cudaMemcpyAsync(w_packed, w, p->packed_bytes, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
+    const IgemmGeom& g = p->g;
+    PackArgs a{p->d.C_in, p->d.C_out, g.KT, g.BN, g.CK, g.n_chunks, g.n_tiles};
+    const size_t total = p->packed_bytes / 2;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pack_igemm_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, a, total);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
+}  // namespace x3

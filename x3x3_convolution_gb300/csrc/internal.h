@@ -1,0 +1,84 @@
+// Internal definitions shared by the host API and the kernels of libx3conv.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "x3conv.h"
+
+namespace x3 {
+
+enum KernelKind { K_DIRECT = 0, K_IGEMM = 1 };
+
+// A-operand staging modes of the implicit-GEMM engine.
+enum StageMode {
+    STAGE_CL = 0,    // channels-last input: TMA writes the halo straight into K-major planes
+    STAGE_NCHW = 1   // channels-first 2D input: TMA loads a raw tile, warps transpose it
+};
+
+// Tiling of the tcgen05 implicit GEMM. A tile is Rt output rows x Wt output columns of one output
+// frame and BN output channels. Its halo (Rt+2 rows x P columns, P = Wt + 2) sits in shared
+// memory as a raster of positions; output raster position m = r*P + c (c < Wt valid) reads halo
+// position m + kh*P + kw for tap (kh, kw). The tile's M rows are NSUB subtiles of 128 raster
+// positions starting at sub_off(s).
+struct IgemmGeom {
+    int mode;          // StageMode
+    int BN;            // output channels per tile (16, 64 or 128)
+    int n_tiles;       // ceil(C_out / BN)
+    int CK;            // input channels per staged chunk (16 or 32)
+    int n_chunks;      // ceil(C_in / CK)
+    int KT;            // temporal taps: 3 (causal 3D) or 1 (2D)
+    int NSUB;          // 128-row MMA subtiles per tile
+    int Rt, Wt, P;     // output rows / columns per tile, halo raster pitch in positions
+    int spr;           // row-aligned subtile mapping: subtiles per output row; 0 = flat (128*s)
+    int halo_rows;     // Rt + 2
+    int plane_pos;     // positions per K-major plane (halo_rows * P)
+    int plane_stride;  // bytes between planes (plane_pos * 16)
+    int a_bytes;       // bytes of one A stage (CK/8 planes + read slack)
+    int a_tx_bytes;    // bytes the TMA writes into one A stage
+    int raw_w;         // NCHW: columns of the raw tile (Wt + 16)
+    int raw_bytes;     // NCHW: bytes of one raw stage
+    int b_bytes;       // bytes of one packed weight block (BN x CK)
+    int n_a, n_b, n_raw; // pipeline depths
+    int tmem_cols;     // TMEM columns allocated (power of two >= 32)
+    int acc_bufs;      // accumulator buffers in TMEM (1 or 2)
+    int col_tiles, row_tiles, frames;
+    long long tiles;   // col_tiles * row_tiles * frames * n_tiles
+    int smem_bytes;    // dynamic shared memory per CTA
+    int grid;          // persistent CTAs
+};
+
+}  // namespace x3
+
+struct x3_conv_plan {
+    x3_conv_desc d;
+    int H_out, W_out;
+    x3::KernelKind kind;
+    x3::IgemmGeom g;
+    size_t packed_bytes;
+    int num_sms;
+};
+
+namespace x3 {
+
+// Set the thread-local error string and return the status.
+x3_status fail(x3_status s, const char* fmt, ...);
+
+// Bytes per element of the storage types.
+inline int elem_bytes(x3_dtype) { return 2; }
+
+// Elements of one activation tensor / frame.
+size_t in_elems(const x3_conv_plan* p);
+size_t out_elems(const x3_conv_plan* p);
+
+// Kernel launchers (return X3_OK or an error with the message set).
+x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s);
+x3_status launch_direct(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                        const void* bias, void* y, cudaStream_t s);
+x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                       const void* bias, void* y, cudaStream_t s);
+bool igemm_plan(x3_conv_plan* p, int num_sms);  // fills p->g; false if the engine can't run it
+x3_status read_device_status(int reset);
+
+}  // namespace x3
