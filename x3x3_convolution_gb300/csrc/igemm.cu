@@ -55,6 +55,7 @@ struct IgemmArgs {
     int BN, n_tiles, CK, n_chunks, KT, NSUB, Rt, Wt, P, spr, halo_rows, plane_stride, a_bytes, a_tx_bytes;
     int raw_w, raw_bytes, raw_tx_bytes, b_bytes, n_a, n_b, n_raw, acc_bufs, tmem_cols;
     int col_tiles, row_tiles, frames;
+    int scr_pitch;  // epilogue scratch row pitch in bytes (0 = direct stores)
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -139,11 +140,11 @@ __device__ __forceinline__ float bias_at(const void* bias, int co) {
 
 // Store 16 accumulator columns [co0, co0+16) of one output position.
 template <bool BF16>
-__device__ __forceinline__ void store_chunk(const IgemmArgs& a, const uint32_t (&v)[16], int co0, int n, int t,
-                                            int oh, int ow) {
+__device__ __forceinline__ void store_chunk(const IgemmArgs& a, const uint32_t (&v)[16], const float* bias16, int co0,
+                                            int n, int t, int oh, int ow) {
     float f[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = act_apply(__uint_as_float(v[i]) + bias_at<BF16>(a.bias, co0 + i), a.act);
+    for (int i = 0; i < 16; ++i) f[i] = act_apply(__uint_as_float(v[i]) + bias16[i], a.act);
     if (a.out_kind == OUT_CL) {
         uint16_t* y = reinterpret_cast<uint16_t*>(a.y) +
                       ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co0;
@@ -213,6 +214,8 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
     const uint32_t s_tmem = bar_drain + 8u;
     const uint32_t s_abort = s_tmem + 4u;
     const uint32_t s_junk = (s_abort + 4u + 127u) & ~127u;  // NCHW: 16 bytes per transposer lane
+    const uint32_t s_bias = s_junk + (MODE == STAGE_NCHW ? 4u * 32u * 16u : 0u);  // BN floats
+    const uint32_t s_scr = (s_bias + 4u * (uint32_t)a.BN + 127u) & ~127u;      // 4 warps x 32 rows x scr_pitch
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + (s_abort - base));
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + (s_tmem - base));
 
@@ -333,39 +336,60 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
         if (lane == 0) {
             uint32_t a_cnt = 0, b_cnt = 0, it = 0;
             bool ok = true;
-            const uint32_t ldA = (uint32_t)a.plane_stride;     // bytes between K-adjacent core matrices of A
-            const uint32_t ldB = (uint32_t)a.BN * 16u;         // ... of B
+            // Descriptor words: the high word (SBO = 128 bytes between 8-row core-matrix groups,
+            // version 1) never changes; the low word is (start address >> 4) | (LBO >> 4) << 16, so
+            // every offset below is added in 16-byte units to the low word only.
+            const uint32_t hi = (128u >> 4) | (1u << 14);
+            const uint32_t a_lo0 = ((sA >> 4) & 0x3FFFu) | ((uint32_t)(a.plane_stride >> 4) << 16);
+            const uint32_t b_lo0 = ((sB >> 4) & 0x3FFFu) | ((uint32_t)((a.BN * 16) >> 4) << 16);
+            const uint32_t a_stage16 = (uint32_t)a.a_bytes >> 4, b_stage16 = (uint32_t)a.b_bytes >> 4;
+            const uint32_t a_ks16 = (uint32_t)(2 * a.plane_stride) >> 4, b_ks16 = (uint32_t)(2 * a.BN * 16) >> 4;
             const int ksteps = a.CK / 16;
+            const int nsub = a.NSUB;
+            uint32_t soff[8], dcol[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                soff[s] = s < nsub ? (uint32_t)sub_off(a, s) : 0u;  // raster offset = 16-byte units
+                dcol[s] = (uint32_t)(s * a.BN);
+            }
             for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x, ++it) {
                 const uint32_t ab = it % a.acc_bufs;
                 if (!wait_bar(bar_acc_empty + 8 * ab, ((it / a.acc_bufs) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t d0 = tmem_base + ab * (uint32_t)(a.NSUB * a.BN);
+                const uint32_t d0 = tmem_base + ab * (uint32_t)(nsub * a.BN);
                 uint32_t acc = 0;
                 for (int kt = 0; kt < a.KT && ok; ++kt) {
                     for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
                         const uint32_t sa = a_cnt % a.n_a;
                         if (!wait_bar(bar_a_full + 8 * sa, (a_cnt / a.n_a) & 1u, abort_flag)) { ok = false; break; }
                         ptx::tc_fence_after();
-                        const uint32_t abase = sA + sa * a.a_bytes;
-                        for (int tap = 0; tap < 9; ++tap) {
-                            const int kh = tap / 3, kw = tap % 3;
-                            const uint32_t sb = b_cnt % a.n_b;
-                            if (!wait_bar(bar_b_full + 8 * sb, (b_cnt / a.n_b) & 1u, abort_flag)) { ok = false; break; }
-                            ptx::tc_fence_after();
-                            const uint32_t bbase = sB + sb * a.b_bytes;
-                            const uint32_t shift = (uint32_t)(kh * a.P + kw) * 16u;
-                            for (int ks = 0; ks < ksteps; ++ks) {
-                                const uint64_t bdesc = ptx::desc_noswizzle(bbase + (uint32_t)ks * 2u * ldB, ldB, 128u);
-                                for (int s = 0; s < a.NSUB; ++s) {
-                                    const uint32_t aaddr = abase + (uint32_t)ks * 2u * ldA + shift + (uint32_t)sub_off(a, s) * 16u;
-                                    const uint64_t adesc = ptx::desc_noswizzle(aaddr, ldA, 128u);
-                                    ptx::mma_f16(d0 + (uint32_t)(s * a.BN), adesc, bdesc, a.idesc, acc);
+                        const uint32_t a_lo_stage = a_lo0 + sa * a_stage16;
+                        uint32_t tap_off = 0;
+                        for (int kh = 0; kh < 3 && ok; ++kh, tap_off += (uint32_t)a.P) {
+                            for (int kw = 0; kw < 3; ++kw) {
+                                const uint32_t sb = b_cnt % a.n_b;
+                                if (!wait_bar(bar_b_full + 8 * sb, (b_cnt / a.n_b) & 1u, abort_flag)) { ok = false; break; }
+                                ptx::tc_fence_after();
+                                const uint32_t b_lo = b_lo0 + sb * b_stage16;
+                                const uint32_t a_lo = a_lo_stage + tap_off + (uint32_t)kw;
+#pragma unroll
+                                for (int ks = 0; ks < 2; ++ks) {
+                                    if (ks < ksteps) {
+                                        const uint64_t bdesc = ((uint64_t)hi << 32) | (uint64_t)(b_lo + ks * b_ks16);
+                                        const uint32_t a_lo_k = a_lo + ks * a_ks16;
+#pragma unroll
+                                        for (int s = 0; s < 8; ++s) {
+                                            if (s < nsub) {
+                                                const uint64_t adesc = ((uint64_t)hi << 32) | (uint64_t)(a_lo_k + soff[s]);
+                                                ptx::mma_f16(d0 + dcol[s], adesc, bdesc, a.idesc, acc);
+                                            }
+                                        }
+                                        acc = 1;
+                                    }
                                 }
-                                acc = 1;
+                                ptx::mma_commit(bar_b_empty + 8 * sb);
+                                ++b_cnt;
                             }
-                            ptx::mma_commit(bar_b_empty + 8 * sb);
-                            ++b_cnt;
                         }
                         if (!ok) break;
                         ptx::mma_commit(bar_a_empty + 8 * sa);
@@ -384,6 +408,11 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue (TMEM -> global)
         const int quarter = warp & 3;
+        const int ew = warp - 2;
+        float* s_bias_f = reinterpret_cast<float*>(sbase + (s_bias - base));
+        uint8_t* scr = sbase + (s_scr - base) + (size_t)ew * 32 * a.scr_pitch;
+        const bool staged = a.scr_pitch > 0;
+        int cur_nt = -1;
         uint32_t it = 0;
         for (long long tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++it) {
             const uint32_t ab = it % a.acc_bufs;
@@ -391,6 +420,15 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
             ptx::tc_fence_after();
             const TileCoord tc = decode_tile(a, tile);
             const int n = tc.fr / a.dout, t = tc.fr % a.dout;
+            if (tc.nt != cur_nt) {  // stage this N tile's bias (fp32) once for the four epilogue warps
+                ptx::named_bar_sync(1, 128);
+                for (int i = threadIdx.x - 64; i < a.BN; i += 128) {
+                    const int co = tc.nt * a.BN + i;
+                    s_bias_f[i] = co < a.C_out ? bias_at<BF16>(a.bias, co) : 0.0f;
+                }
+                ptx::named_bar_sync(1, 128);
+                cur_nt = tc.nt;
+            }
             for (int s = 0; s < a.NSUB; ++s) {
                 const int m = sub_off(a, s) + quarter * 32 + lane;
                 const int r = m / a.P, c = m % a.P;
@@ -398,12 +436,55 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
                 const bool valid = (c < a.Wt) && (r < a.Rt) && (oh < a.H_out) && (ow < a.W_out);
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * (uint32_t)(a.NSUB * a.BN) +
                                        (uint32_t)(s * a.BN);
-                for (int ch = 0; ch < a.BN; ch += 16) {
-                    uint32_t v[16];
-                    ptx::tmem_ld16(taddr + (uint32_t)ch, v);
-                    ptx::tmem_ld_wait();
-                    const int co0 = tc.nt * a.BN + ch;
-                    if (valid && co0 < a.C_out) store_chunk<BF16>(a, v, co0, n, t, oh, ow);
+                if (staged) {
+                    // channels-last: this thread's position row (BN values, rounded) goes to the warp's
+                    // scratch, then the warp writes whole rows of BN*2 contiguous bytes per position.
+                    uint8_t* row = scr + (size_t)lane * a.scr_pitch;
+                    for (int ch = 0; ch < a.BN; ch += 32) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(taddr + (uint32_t)ch, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w4;
+                            const float* bb = s_bias_f + ch + q * 8;
+                            w4.x = pack2<BF16>(act_apply(__uint_as_float(v[q * 8 + 0]) + bb[0], a.act),
+                                               act_apply(__uint_as_float(v[q * 8 + 1]) + bb[1], a.act));
+                            w4.y = pack2<BF16>(act_apply(__uint_as_float(v[q * 8 + 2]) + bb[2], a.act),
+                                               act_apply(__uint_as_float(v[q * 8 + 3]) + bb[3], a.act));
+                            w4.z = pack2<BF16>(act_apply(__uint_as_float(v[q * 8 + 4]) + bb[4], a.act),
+                                               act_apply(__uint_as_float(v[q * 8 + 5]) + bb[5], a.act));
+                            w4.w = pack2<BF16>(act_apply(__uint_as_float(v[q * 8 + 6]) + bb[6], a.act),
+                                               act_apply(__uint_as_float(v[q * 8 + 7]) + bb[7], a.act));
+                            *reinterpret_cast<uint4*>(row + (ch + q * 8) * 2) = w4;
+                        }
+                    }
+                    const unsigned long long my_off =
+                        valid ? ((((unsigned long long)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (unsigned long long)a.C_out
+                              : ~0ull;
+                    __syncwarp();
+                    const int lpr = a.BN / 8;  // lanes per row: 16 bytes = 8 channels each
+                    const int rpi = 32 / lpr;  // rows per store instruction
+                    const int seg = lane % lpr;
+                    const int co = tc.nt * a.BN + seg * 8;
+                    uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
+                    for (int r0 = 0; r0 < 32; r0 += rpi) {
+                        const int rr = r0 + lane / lpr;
+                        const unsigned long long off = __shfl_sync(0xffffffffu, my_off, rr);
+                        if (off != ~0ull && co < a.C_out) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(scr + (size_t)rr * a.scr_pitch + seg * 16);
+                            *reinterpret_cast<uint4*>(y + off + co) = q;
+                        }
+                    }
+                    __syncwarp();
+                } else {
+                    for (int ch = 0; ch < a.BN; ch += 16) {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(taddr + (uint32_t)ch, v);
+                        ptx::tmem_ld_wait();
+                        const int co0 = tc.nt * a.BN + ch;
+                        if (valid && co0 < a.C_out) store_chunk<BF16>(a, v, s_bias_f + ch, co0, n, t, oh, ow);
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -485,7 +566,8 @@ static bool fill_smem(IgemmGeom& g, int max_read_pos) {
         g.raw_w = 0;
         g.raw_bytes = 0;
     }
-    const int fixed = 128 /*align*/ + 512 /*barriers*/ + (g.mode == STAGE_NCHW ? 4 * 32 * 16 + 128 : 0);
+    const int fixed = 128 /*align*/ + 512 /*barriers*/ + (g.mode == STAGE_NCHW ? 4 * 32 * 16 + 128 : 0) +
+                      4 * g.BN + 128 /*bias*/ + 4 * 32 * g.scr_pitch /*epilogue scratch*/;
     // preferred depths, shrunk until the stages fit
     const int a_opts[2] = {2, 1};
     const int r_opts[2] = {2, 1};
@@ -543,6 +625,8 @@ bool igemm_plan(x3_conv_plan* p, int num_sms) {
     g.BN = d.C_out <= 16 ? 16 : d.C_out <= 32 ? 32 : d.C_out <= 64 ? 64 : 128;
     g.n_tiles = (d.C_out + g.BN - 1) / g.BN;
     g.CK = d.C_in <= 16 ? 16 : 32;
+    // channels-last outputs with whole 16-byte channel groups go through the epilogue's smem transpose
+    g.scr_pitch = (g.mode == STAGE_CL && !d.unpatchify2x2 && d.C_out % 8 == 0 && g.BN >= 32) ? 2 * g.BN + 16 : 0;
     g.n_chunks = (d.C_in + g.CK - 1) / g.CK;
     const int H_out = p->H_out, W_out = p->W_out;
     const int frames = d.N * (d.dims == 3 ? d.D : 1);
@@ -667,6 +751,7 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     a.raw_tx_bytes = g.CK * g.halo_rows * g.raw_w * 2; a.b_bytes = g.b_bytes; a.n_a = g.n_a; a.n_b = g.n_b;
     a.n_raw = g.n_raw; a.acc_bufs = g.acc_bufs; a.tmem_cols = g.tmem_cols;
     a.col_tiles = g.col_tiles; a.row_tiles = g.row_tiles; a.frames = g.frames; a.tiles = g.tiles;
+    a.scr_pitch = g.scr_pitch;
     a.idesc = ptx::idesc_f16(128, g.BN, bf16);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
 

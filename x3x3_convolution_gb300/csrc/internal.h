@@ -42,6 +42,7 @@ struct IgemmGeom {
     int b_bytes;       // bytes of one packed weight block (BN x CK)
     int n_a, n_b, n_raw; // pipeline depths
     int tmem_cols;     // TMEM columns allocated (power of two >= 32)
+    int scr_pitch;     // epilogue scratch row pitch (bytes) for coalesced channels-last stores; 0 = none
     int acc_bufs;      // accumulator buffers in TMEM (1 or 2)
     int col_tiles, row_tiles, frames;
     long long tiles;   // col_tiles * row_tiles * frames * n_tiles
