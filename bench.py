@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the convolution hot path on GB300: one step = one decoder pass over synthetic data.
+
+The step runs every stage of the path through the library's C ABI:
+  * taesd  - TAESD-like 2D chain, NCHW f16, N=4, 3x256x256: 3->64, 3x 64->64, 64->64 stride 2,
+             2x 64->64 at 128x128, all with bias + ReLU (conv_stack_forward, 7 layers);
+  * stack  - causal 3x3x3 stack, NDHWC bf16: two chained 128->128 layers with ReLU over 4 frames
+             (+2 carried) at 352x624 (conv_stack_forward with per-layer carries);
+  * l3     - causal 256->128 over 4 frames (+2 carried) at 176x312 (conv_forward);
+  * head   - conv_out head: causal 256->12 over 4 frames (+2 carried) at 352x624, bias, clamp to
+             [-1,1], 2x2 unpatchify to 4x704x1248 RGB (conv_forward).
+value = total convolution FLOP of the step / step time (TFLOP/s, whole job over all ranks).
+Also reported: decoder-stack ms per frame (stack + l3 + head over the 4 frames), per-stage times,
+the roofline fraction of the dominant kernel, an end-to-end number with host buffers, the SM
+clocks seen during the timed region, and the CPU oracle timed on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica of the step (weak scaling, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "conv TFLOP/s & HBM GB/s vs roofline; decoder-stack ms/frame, 1 GB300"
+WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f16) + causal 3x3x3 "
+            "stack (2x 128->128 @4+2x352x624, 256->128 @4+2x176x312, NDHWC bf16) + conv_out head "
+            "(256->12 @4+2x352x624, clamp, 2x2 unpatchify)")
+FRAMES = 4
+STAGES = ["taesd", "stack", "l3", "head"]
+
+
+def flop2d(N, Ci, Co, Ho, Wo):
+    return 2.0 * N * Ci * Co * 9 * Ho * Wo
+
+
+def flop3d(Ci, Co, D, H, W):
+    return 2.0 * Ci * Co * 27 * D * H * W
+
+
+def stage_cost():
+    """FLOP and algorithmic bytes (input read once incl. carried frames, output written once,
+    weights, bias) of each stage."""
+    from x3x3_convolution_gb300.synth import TAESD_CHAIN
+    f_taesd, b_taesd, H, W = 0.0, 0.0, 256, 256
+    for ci, co, s in TAESD_CHAIN:
+        Ho, Wo = (H - 1) // s + 1, (W - 1) // s + 1
+        f_taesd += flop2d(4, ci, co, Ho, Wo)
+        b_taesd += 2.0 * (4 * ci * H * W + 4 * co * Ho * Wo + co * ci * 9 + co)
+        H, W = Ho, Wo
+    b_l1 = 2.0 * (6 * 352 * 624 * 128 + 4 * 352 * 624 * 128 + 128 * 128 * 27 + 128)
+    flops = {"taesd": f_taesd, "stack": 2 * flop3d(128, 128, 4, 352, 624), "l3": flop3d(256, 128, 4, 176, 312),
+             "head": flop3d(256, 12, 4, 352, 624)}
+    nbytes = {"taesd": b_taesd, "stack": 2 * b_l1,
+              "l3": 2.0 * (6 * 176 * 312 * 256 + 4 * 176 * 312 * 128 + 256 * 128 * 27 + 128),
+              "head": 2.0 * (6 * 352 * 624 * 256 + 4 * 352 * 624 * 12 + 256 * 12 * 27 + 12)}
+    return flops, nbytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class Workload:
+    """All layers of the decoder pass, with packed weights, inputs, carries and outputs on the GPU."""
+
+    def __init__(self, device, seed_base=0):
+        import torch
+        import x3x3_convolution_gb300 as x3
+        from x3x3_convolution_gb300 import synth
+        dev = device
+        xt, layers = synth.taesd_chain(seed=1002 + seed_base)
+        convs, H, W = [], 256, 256
+        for L in layers:
+            d = x3.make_desc(2, 4, L.C_in, L.C_out, H, W, stride=L.stride, layout="NCHW", dtype="f16", act="relu")
+            convs.append(x3.Conv(d, L.w.torch(dev), L.b.torch(dev)))
+            H, W = convs[-1].H_out, convs[-1].W_out
+        self.taesd = x3.ConvStack(convs)
+        self.taesd_x = xt.torch(dev)
+        self.taesd_y = torch.empty(convs[-1].out_shape(), dtype=torch.float16, device=dev)
+        st = synth.conv3d_stack(seed=1004 + seed_base)
+        sc = []
+        for L in st["layers"]:
+            d = x3.make_desc(3, 1, L.C_in, L.C_out, 352, 624, D=FRAMES, act=L.act)
+            sc.append(x3.Conv(d, L.w.torch(dev), L.b.torch(dev)))
+        self.stack = x3.ConvStack(sc)
+        self.stack_x = st["x"].torch(dev)
+        self.stack_carries = [c.torch(dev).contiguous() for c in st["carries"]]
+        self.stack_y = torch.empty(sc[-1].out_shape(), dtype=torch.bfloat16, device=dev)
+        L3 = st["L3"]
+        self.l3 = x3.Conv(x3.make_desc(3, 1, 256, 128, 176, 312, D=FRAMES, act="none"), L3.w.torch(dev),
+                          L3.b.torch(dev))
+        self.l3_x = st["x3"].torch(dev)
+        self.l3_c = st["carry3"].torch(dev)
+        self.l3_y = torch.empty(self.l3.out_shape(), dtype=torch.bfloat16, device=dev)
+        hx, hc, HL = synth.head(seed=1005 + seed_base)
+        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, D=FRAMES, act="clamp", unpatchify2x2=True),
+                            HL.w.torch(dev), HL.b.torch(dev))
+        self.head_x = hx.torch(dev)
+        self.head_c = hc.torch(dev)
+        self.head_y = torch.empty(self.head.out_shape(), dtype=torch.bfloat16, device=dev)
+        self.kernels_per_step = len(convs) + len(sc) + 2
+        self.plans = {"taesd": [x3.conv_plan_describe(c.plan) for c in convs],
+                      "stack": x3.conv_plan_describe(sc[0].plan),
+                      "l3": x3.conv_plan_describe(self.l3.plan),
+                      "head": x3.conv_plan_describe(self.head.plan)}
+        self.carry_valid = False
+
+    def inputs(self):
+        return [self.taesd_x, self.stack_x, self.l3_x, self.head_x]
+
+    def outputs(self):
+        return [self.taesd_y, self.stack_y, self.l3_y, self.head_y]
+
+    def step(self, stream, ev=None):
+        """One decoder pass; ev: optional 5 CUDA events recorded between the stages."""
+        if ev:
+            ev[0].record(stream)
+        self.taesd(self.taesd_x, out=self.taesd_y, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        self.stack(self.stack_x, carries=self.stack_carries, carry_valid=self.carry_valid, out=self.stack_y,
+                   stream=stream)
+        self.carry_valid = True
+        if ev:
+            ev[2].record(stream)
+        self.l3(self.l3_x, self.l3_c, out=self.l3_y, stream=stream)
+        if ev:
+            ev[3].record(stream)
+        self.head(self.head_x, self.head_c, out=self.head_y, stream=stream)
+        if ev:
+            ev[4].record(stream)
+
+
+def cpu_baseline(target_s=12.0):
+    """The oracle, as it stands, on the host cores, on a bounded sample of the dominant stage: the
+    causal 128->128 layer at 352x624 restricted to a band of output rows of one frame."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(77)
+    C, W = 128, 624
+    w = (rng.standard_normal((C, C, 3, 3, 3)) * 0.03).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, C).astype(np.float32)
+
+    def run(rows):
+        x = rng.standard_normal((1, 1, rows, W, C)).astype(np.float32)
+        c = rng.standard_normal((1, 2, rows, W, C)).astype(np.float32)
+        t0 = time.perf_counter()
+        oracle.conv3d_causal(x, w, b, carry=c, act="relu", layout="NDHWC")
+        return time.perf_counter() - t0
+
+    dt = run(4)
+    rows = int(max(4, min(352, 4 * target_s / max(dt, 1e-3))))
+    dt = run(rows)
+    fl = flop3d(C, C, 1, rows, W)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
+            "sample": f"causal 128->128 3x3x3 layer, 1 output frame x {rows} rows x 624 cols (of 4 x 352 x 624), "
+                      f"{fl / 1e9:.1f} GFLOP in {dt:.1f} s", "seconds": dt}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def reduce_max(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: rank 0 times it on the host cores; other ranks do nothing."""
+    if rank != 0:
+        return
+    cb = cpu_baseline()
+    fl, _ = stage_cost()
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sum(fl.values()) / (cb["value"] * 1e12) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "note": "CPU oracle (plain fp32 loops) on a bounded sample of the "
+                                                     "workload; ms_per_step extrapolated from its FLOP rate"},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    import x3x3_convolution_gb300 as x3
+    x3.load()
+
+    dev = f"cuda:{local}"
+    wl = Workload(dev, seed_base=rank)
+    stream = torch.cuda.current_stream()
+    fl, nb = stage_cost()
+    total_flop = sum(fl.values())
+
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    st = x3.conv_device_status(1)
+    if st != x3.X3_OK:
+        raise RuntimeError(f"device status after warm-up: {st} {x3.conv_last_error()}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        wl.step(stream, evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_per_step = reduce_max(world, t0.elapsed_time(t1)) / args.steps
+    stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, name in enumerate(STAGES)}
+    st = x3.conv_device_status(1)
+    if st != x3.X3_OK:
+        raise RuntimeError(f"device status after the timed steps: {st} {x3.conv_last_error()}")
+
+    e2e = None
+    if not args.no_e2e:
+        # end to end through host buffers: H2D of the step's inputs from pinned memory, the step,
+        # D2H of its outputs, all inside the timed region
+        hin = [t.cpu().pin_memory() for t in wl.inputs()]
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in wl.outputs()]
+        h2d = sum(t.numel() * t.element_size() for t in hin)
+        d2h = sum(t.numel() * t.element_size() for t in hout)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 10))
+        barrier(world)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            for h, d in zip(hin, wl.inputs()):
+                d.copy_(h, non_blocking=True)
+            wl.step(stream)
+            for h, d in zip(hout, wl.outputs()):
+                h.copy_(d, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(world, e0.elapsed_time(e1)) / n_e2e
+        e2e = {"value": world * total_flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    peaks = load_peaks()
+    # dominant kernel: the causal 128->128 tcgen05 implicit GEMM, launched twice per step by the stack
+    # stage; its per-launch time is the stage time over 2 (which also carries the two 2-frame carry copies)
+    launch_ms = stage_ms["stack"] / 2
+    achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "igemm_conv_kernel (channels-last) causal 128->128 @4+2x352x624",
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms}
+    stages = {}
+    for k in STAGES:
+        t = stage_ms[k] * 1e-3
+        stages[k] = {"ms": stage_ms[k], "tflops": fl[k] / t / 1e12, "gbs": nb[k] / t / 1e9,
+                     "frac_tensor": fl[k] / t / 1e12 / peaks["bf16_tflops"],
+                     "frac_hbm": nb[k] / t / 1e9 / peaks["hbm_gbs"]}
+    line = {
+        "metric": METRIC, "value": world * total_flop / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f16 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (each step streams ~3 GB; no explicit flush)",
+                   "frames_per_pass": FRAMES},
+        "decoder_ms_per_frame": (stage_ms["stack"] + stage_ms["l3"] + stage_ms["head"]) / FRAMES,
+        "stages": stages, "roofline": roofline, "gpu_launches": wl.kernels_per_step * args.steps,
+        "clocks": clk, "e2e": e2e,
+        "plans": {k: (v if k != "taesd" else [p.get("kernel") for p in v]) for k, v in wl.plans.items()},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline()
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
