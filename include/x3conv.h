@@ -167,6 +167,35 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
                              size_t workspace_bytes, x3_stream_t stream);
 
 /*
+ * Size of the scratch buffer built into the library for conv_stack_forward_noalloc: 32 MiB of
+ * device memory, held on every GPU that loads the library until the process exits.
+ */
+#define X3_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * conv_stack_forward without a workspace argument, for callers that must not allocate device
+ * memory (a plug-in inside a framework that owns every allocation, a pipeline that forbids
+ * allocation after start-up, a caller whose memory is fully reserved by its own pool). The
+ * pages have no counterpart of this entry point; it is an addition of this library.
+ *
+ * Arguments and results are those of conv_stack_forward; the caller still provides inputs,
+ * outputs, carries and packed weights. The intermediate activations live in the library's own
+ * X3_NOALLOC_SCRATCH_BYTES device buffer instead of a caller workspace, and this function calls
+ * no allocator.
+ *   - Stacks whose conv_stack_workspace_bytes exceeds X3_NOALLOC_SCRATCH_BYTES are rejected with
+ *     X3_ERR_OOM before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the buffer's device address;
+ *     make that first call before capturing any stream.
+ *   - All calls on a device share the one buffer and it keeps the last call's contents (each
+ *     layer overwrites every intermediate value it produces, so nothing needs clearing). Calls
+ *     whose work overlaps on the GPU - on different streams, or from different threads - race on
+ *     it: serialise them.
+ */
+x3_status conv_stack_forward_noalloc(const x3_conv_plan* const* plans, int n_layers, const void* x,
+                                     void* const* carries, int carry_valid, const void* const* w_packed,
+                                     const void* const* bias, void* y, x3_stream_t stream);
+
+/*
  * Read (and with reset != 0, clear) the current device's status word: X3_OK, or X3_ERR_TIMEOUT
  * when a bounded device wait ran out since the last reset. Synchronises the device.
  */
