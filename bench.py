@@ -364,7 +364,7 @@ def main():
     achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "igemm_conv_kernel (channels-last) causal 128->128 @4+2x352x624",
+                "traffic": None, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms}
     stages = {}
     for k in STAGES:

@@ -130,7 +130,28 @@ WORKLOADS = {
     "causal_256to128_176x312": dict(dims=3, N=1, C_in=256, C_out=128, D=4, H=176, W=312),
     "head_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True),
     "ragged_3d": dict(dims=3, N=2, C_in=40, C_out=72, D=3, H=7, W=301),
+    "ragged_3d_wide": dict(dims=3, N=2, C_in=40, C_out=136, D=3, H=7, W=301),
+    "nhwc_2d_256": dict(dims=2, N=3, C_in=64, C_out=256, H=33, W=97, layout="NHWC"),
 }
+
+
+def _check_sw128_plan(g):
+    """Channels-last swapped engine: 256-position windows of strip rasters of pitch P."""
+    P, HR, Wt = g["P"], g["HR"], g["Wt"]
+    assert P == Wt + 2 and P <= 256 and HR <= 256
+    # the furthest halo row read: a window starting at offset P-1 of a row (or 0 when P divides
+    # 256), its last position, tap (kh=2, kw=2)
+    pos_off_max = 0 if 256 % P == 0 else P - 1
+    assert (pos_off_max + 255 + 2 * P + 2 + 1) * 128 <= g["h_bytes"]
+    # the rows a window touches, plus one above and below, are all staged
+    for win in range(min(g["windows"], 4 * P)):
+        m0 = 256 * win
+        r0 = m0 // P
+        last_row = (m0 + 255) // P
+        assert last_row + 1 - (r0 - 1) + 1 <= HR
+    assert g["h_bytes"] % 1024 == 0 and g["smem_bytes"] <= 232448
+    assert g["strips"] * Wt >= g["W_out"] and g["windows"] * 256 >= g["H_out"] * P
+    assert g["tiles"] == g["strips"] * g["windows"] * g["frames"] * g["n_tiles"]
 
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
@@ -138,6 +159,9 @@ def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
+        if g["kernel"] == "igemm_tcgen05_sw128":
+            _check_sw128_plan(g)
+            return
         assert g["kernel"] == "igemm_tcgen05"
         P, Rt, Wt, NSUB, spr = g["P"], g["Rt"], g["Wt"], g["NSUB"], g["spr"]
         assert P == Wt + 2 and P <= 256

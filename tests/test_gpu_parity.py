@@ -67,7 +67,7 @@ def test_conv2d_nchw(case, variant, kernel):
                                seed=2000 + sum(case[:6]))
     got, conv = run2d(x, L, kernel=kernel)
     if kernel == "auto" and s == 1:
-        assert conv.kernel_name == "igemm_tcgen05"
+        assert conv.kernel_name.startswith("igemm_tcgen05")
     ref = oracle2d(x, L)
     if variant == "int":
         assert_exact(got, ref, "f16")
@@ -84,7 +84,7 @@ def test_conv2d_nhwc_bf16(case, variant):
     x = synth.activation([key, 0], (N, H, W, Ci), "bf16", variant, ("uniform", -1.0, 1.0))
     L = synth.make_layer([key], 2, Ci, Co, "bf16", act=act, variant=variant)
     got, conv = run2d(x, L, layout="NHWC")
-    assert conv.kernel_name == "igemm_tcgen05"
+    assert conv.kernel_name.startswith("igemm_tcgen05")
     ref = oracle2d(x, L, layout="NHWC")
     if variant == "int":
         assert_exact(got, ref, "bf16")
@@ -118,21 +118,29 @@ CASES_3D = [
     (1, 40, 72, 2, 5, 19, "relu", True),      # channels not multiples of the chunk / N tile
     (1, 16, 16, 4, 1, 8, "none", True),       # a single row
     (1, 256, 128, 2, 9, 130, "none", True),
+    (2, 40, 136, 3, 7, 301, "relu", True),   # two 128-channel output tiles, ragged everything
+    (1, 64, 256, 2, 5, 700, "none", False),  # wide rows: several strips
 ]
 
 
 @pytest.mark.parametrize("variant", ["int", "random"])
 @pytest.mark.parametrize("case", CASES_3D, ids=lambda c: "x".join(map(str, c[:6])) + ("c" if c[7] else "z"))
-@pytest.mark.parametrize("kernel", ["auto", "direct"])
-def test_conv3d_causal(case, variant, kernel):
+@pytest.mark.parametrize("kernel", ["auto", "nsub", "direct"])
+def test_conv3d_causal(case, variant, kernel, monkeypatch):
+    """auto: the planner's engine (the swapped 128-byte-swizzle engine when C_out >= 96);
+    nsub: the positions-as-M engine forced; direct: the SIMT kernel."""
     N, Ci, Co, D, H, W, act, with_carry = case
     if kernel == "direct" and Ci * Co * H * W > 2_000_000:
         pytest.skip("the direct kernel is checked on the smaller shapes")
+    if kernel == "nsub":
+        monkeypatch.setenv("X3CONV_FORCE_KERNEL", "igemm_nsub")
     x, carry, L = synth.conv3d_single(C_in=Ci, C_out=Co, D=D, H=H, W=W, N=N, variant=variant, act=act,
                                       seed=3000 + sum(case[:6]), with_carry=with_carry)
-    got, conv = run3d(x, carry, L, kernel=kernel)
-    if kernel == "auto":
+    got, conv = run3d(x, carry, L, kernel="auto" if kernel == "nsub" else kernel)
+    if kernel == "nsub":
         assert conv.kernel_name == "igemm_tcgen05"
+    elif kernel == "auto":
+        assert conv.kernel_name == ("igemm_tcgen05_sw128" if Co >= 96 else "igemm_tcgen05")
     ref = oracle3d(x, carry, L)
     if variant == "int":
         assert_exact(got, ref, "bf16")
@@ -171,7 +179,7 @@ def test_full_size_sampled(name):
     cfg = FULL_3D[name]
     x, carry, L = synth.conv3d_single(N=1, seed=3900 + len(name), **cfg)
     got, conv = run3d(x, carry, L)
-    assert conv.kernel_name == "igemm_tcgen05"
+    assert conv.kernel_name.startswith("igemm_tcgen05")
     seq = np.concatenate([carry.vals, x.vals], axis=1)
     pos = sample_positions(cfg["D"], cfg["H"], cfg["W"], 400, seed=len(name))
     ref = oracle_sampled_3d(seq, L.w.vals, L.b.vals, cfg["act"], pos)

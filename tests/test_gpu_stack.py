@@ -149,3 +149,22 @@ def test_stack2d_taesd_like(variant):
         ref32 = oracle.conv2d_chain(x.vals, [dict(w=L.w.vals, b=L.b.vals, stride=L.stride, act="relu")
                                              for L in layers])
         assert_close(got, ref32)
+
+
+def test_stack3d_wide_channels():
+    """Chained 64->128->128 layers: the 128-channel layers run on the swapped-operand engine."""
+    chans, acts = [64, 128, 128], ["relu", "none"]
+    D, H, W = 2, 6, 140
+    layers = make_3d_layers(chans, acts, "random", 4500)
+    x = synth.activation([4500, 0], (1, D, H, W, 64), "bf16", "random", ("normal", 1.0))
+    carries = [synth.activation([4500, 3, i], (1, 2, H, W, c), "bf16", "random", ("normal", 1.0))
+               for i, c in enumerate(chans[:-1])]
+    convs, stack = build_stack(layers, D, H, W)
+    assert all(c.kernel_name == "igemm_tcgen05_sw128" for c in convs)
+    cdev = [dev(c).contiguous() for c in carries]
+    got = host_values(stack(dev(x), carries=cdev, carry_valid=True), "bf16")
+    torch.cuda.synchronize()
+    want, want_carries = oracle_rounded_chain_3d(x.vals, [c.vals for c in carries], layers)
+    assert_close(got, want)
+    assert np.array_equal(host_values(cdev[0], "bf16"), want_carries[0])
+    assert_close(host_values(cdev[1], "bf16"), want_carries[1])

@@ -113,12 +113,17 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         if (!strcmp(force, "direct")) choice = X3_KERNEL_DIRECT;
         else if (!strcmp(force, "igemm")) choice = X3_KERNEL_IGEMM;
     }
-    if (choice != X3_KERNEL_DIRECT) igemm_ok = igemm_plan(p, p->num_sms);
-    if (choice == X3_KERNEL_IGEMM && !igemm_ok) {
+    bool cl_ok = false;
+    if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) cl_ok = igemm_cl_plan(p, p->num_sms);
+    if (choice != X3_KERNEL_DIRECT && !cl_ok) igemm_ok = igemm_plan(p, p->num_sms);
+    if (choice == X3_KERNEL_IGEMM && !igemm_ok && !cl_ok) {
         delete p;
-        return fail(X3_ERR_UNSUPPORTED, "the tcgen05 implicit-GEMM kernel does not handle this descriptor");
+        return fail(X3_ERR_UNSUPPORTED, "the tcgen05 implicit-GEMM kernels do not handle this descriptor");
     }
-    if (igemm_ok) {
+    if (cl_ok) {
+        p->kind = K_IGEMM_CL;
+        p->packed_bytes = (size_t)p->cl.n_tiles * p->cl.KT * p->cl.n_chunks * 9 * (128 * 64 * 2);
+    } else if (igemm_ok) {
         p->kind = K_IGEMM;
         const IgemmGeom& g = p->g;
         p->packed_bytes = (size_t)g.n_tiles * g.KT * g.n_chunks * 9 * g.b_bytes;
@@ -134,7 +139,7 @@ void conv_plan_destroy(x3_conv_plan* plan) { delete plan; }
 
 const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
     if (!plan) return "";
-    return plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
+    return plan->kind == K_IGEMM_CL ? "igemm_tcgen05_sw128" : plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
 }
 
 int conv_plan_launches(const x3_conv_plan* plan) { return plan ? 1 : 0; }
@@ -142,6 +147,17 @@ int conv_plan_launches(const x3_conv_plan* plan) { return plan ? 1 : 0; }
 int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
     if (!plan) return snprintf(buf, len, "{}");
     const IgemmGeom& g = plan->g;
+    if (plan->kind == K_IGEMM_CL) {
+        const ClGeom& c = plan->cl;
+        return snprintf(buf, len,
+                        "{\"kernel\": \"igemm_tcgen05_sw128\", \"mode\": \"channels_last_sw128_swapped\", "
+                        "\"BM\": 128, \"BN\": 256, \"CK\": 64, \"n_tiles\": %d, \"n_chunks\": %d, \"KT\": %d, "
+                        "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
+                        "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"tiles\": %lld, "
+                        "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
+                        c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
+                        c.n_w, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms);
+    }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
                         plan->H_out, plan->W_out, plan->num_sms);
@@ -182,6 +198,8 @@ x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carr
     const char* lo_x = (const char*)x;
     const char* hi_x = lo_x + in_elems(plan) * 2;
     if (lo_y < hi_x && lo_x < hi_y) return fail(X3_ERR_INVALID, "conv_forward: y overlaps x");
+    if (plan->kind == K_IGEMM_CL)
+        return launch_igemm_cl(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
     if (plan->kind == K_IGEMM) return launch_igemm(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
     return launch_direct(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
 }

@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
     const uint32_t s_tmem = bar_drain + 8u;
     const uint32_t s_abort = s_tmem + 4u;
     const uint32_t s_junk = (s_abort + 4u + 127u) & ~127u;  // NCHW: 16 bytes per transposer lane
-    const uint32_t s_bias = s_junk + (MODE == STAGE_NCHW ? 4u * 32u * 16u : 0u);  // BN floats
-    const uint32_t s_scr = (s_bias + 4u * (uint32_t)a.BN + 127u) & ~127u;      // 4 warps x 32 rows x scr_pitch
+    const uint32_t s_bias = s_junk + (MODE == STAGE_NCHW ? 4u * 32u * 16u : 0u);  // 4 warps x BN floats
+    const uint32_t s_scr = (s_bias + 16u * (uint32_t)a.BN + 127u) & ~127u;     // 4 warps x 32 rows x scr_pitch
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + (s_abort - base));
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + (s_tmem - base));
 
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
         // ------------------------------------------------------------ epilogue (TMEM -> global)
         const int quarter = warp & 3;
         const int ew = warp - 2;
-        float* s_bias_f = reinterpret_cast<float*>(sbase + (s_bias - base));
+        float* s_bias_f = reinterpret_cast<float*>(sbase + (s_bias - base)) + ew * a.BN;
         uint8_t* scr = sbase + (s_scr - base) + (size_t)ew * 32 * a.scr_pitch;
         const bool staged = a.scr_pitch > 0;
         int cur_nt = -1;
@@ -420,13 +420,13 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
             ptx::tc_fence_after();
             const TileCoord tc = decode_tile(a, tile);
             const int n = tc.fr / a.dout, t = tc.fr % a.dout;
-            if (tc.nt != cur_nt) {  // stage this N tile's bias (fp32) once for the four epilogue warps
-                ptx::named_bar_sync(1, 128);
-                for (int i = threadIdx.x - 64; i < a.BN; i += 128) {
+            if (tc.nt != cur_nt) {  // this warp's copy of the N tile's bias (fp32); no cross-warp barrier
+                __syncwarp();
+                for (int i = lane; i < a.BN; i += 32) {
                     const int co = tc.nt * a.BN + i;
                     s_bias_f[i] = co < a.C_out ? bias_at<BF16>(a.bias, co) : 0.0f;
                 }
-                ptx::named_bar_sync(1, 128);
+                __syncwarp();
                 cur_nt = tc.nt;
             }
             for (int s = 0; s < a.NSUB; ++s) {
@@ -567,7 +567,7 @@ static bool fill_smem(IgemmGeom& g, int max_read_pos) {
         g.raw_bytes = 0;
     }
     const int fixed = 128 /*align*/ + 512 /*barriers*/ + (g.mode == STAGE_NCHW ? 4 * 32 * 16 + 128 : 0) +
-                      4 * g.BN + 128 /*bias*/ + 4 * 32 * g.scr_pitch /*epilogue scratch*/;
+                      16 * g.BN + 128 /*bias*/ + 4 * 32 * g.scr_pitch /*epilogue scratch*/;
     // preferred depths, shrunk until the stages fit
     const int a_opts[2] = {2, 1};
     const int r_opts[2] = {2, 1};
@@ -783,6 +783,22 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     if (st != X3_OK) return st;
     mc = mx;
     return bf16 ? launch_t<STAGE_NCHW, true>(mx, mc, a, g, s) : launch_t<STAGE_NCHW, false>(mx, mc, a, g, s);
+}
+
+// Device address of the status word on the current device, for kernels compiled in other files.
+x3_status device_status_word(unsigned int** out) {
+    static unsigned int* ptrs[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(X3_ERR_CUDA, "status word: no current device");
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_x3_status);
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
+        ptrs[dev] = (unsigned int*)p;
+    }
+    *out = ptrs[dev];
+    return X3_OK;
 }
 
 x3_status read_device_status(int reset) {

@@ -1,0 +1,473 @@
+// Channels-last tcgen05 implicit-GEMM engine with output channels as M and positions as N.
+//
+// The causal 3x3x3 convolution of FastVideo wan22_vae_decode/solution/head.cu (bf16 storage, fp32
+// accumulation of all 27 taps, bias, one rounding at the store) for channels-last layers with at
+// least 128 output channels. Each MMA is tcgen05.mma kind::f16 with
+//   A = packed weights  (M = 128 output channels x K = 16 input channels, K-major, no swizzle),
+//   B = input halo      (N = 256 output positions x K = 16 input channels, K-major, 128-byte swizzle),
+//   D = fp32 accumulator in TMEM (128 lanes = channels x 256 columns = positions).
+// Why this arrangement: with N = 256 each MMA reads 12 KB of operands for 1 MFLOP instead of the
+// 8 KB per 0.5 MFLOP of a 128x128 tile, which keeps the tensor core's shared-memory operand reads
+// below the SM's shared-memory bandwidth and leaves room for the TMA writes of the next stages.
+//
+// Tiling. The output plane is cut into vertical strips Wt columns wide; each strip is walked as a
+// raster of pitch P = Wt + 2 (two junk columns per row), and a tile is a window of 256 consecutive
+// raster positions of one frame. Its halo (the rows the window touches plus one above and below,
+// P positions each, 64 channels per stage) is staged once per (temporal tap, 64-channel chunk) by
+// one TMA box with the 128-byte swizzle: every position is one 128-byte row, so the nine spatial
+// taps are nine row offsets (kh*P + kw) of the same staged halo and every such offset reads
+// conflict-free. Out-of-image boxes are zero-filled by the TMA unit (the zero padding); missing
+// carried frames are read at an out-of-range frame coordinate (zeros).
+//
+// Roles (one persistent CTA per SM): warp 0 issues the TMA loads (halo) and bulk copies (weights),
+// warp 1 owns TMEM and one thread issues the MMAs, warps 2-5 drain TMEM (two accumulator buffers,
+// so the epilogue of one tile overlaps the MMAs of the next), add the bias, apply the activation,
+// round once and write channels-last rows through a shared-memory transpose. Every wait is bounded
+// (1 s); a wait that runs out sets the device status word and every role gives up cleanly.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace x3 {
+
+namespace {
+
+constexpr int kSmemLimit = 232448;
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr int kBM = 128;        // output channels per tile (MMA M)
+constexpr int kBNP = 256;       // positions per tile (MMA N)
+constexpr int kCK = 64;         // input channels per staged chunk (one 128-byte swizzle row)
+constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one tap, one chunk)
+constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
+
+struct ClArgs {
+    int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
+    int KT, n_chunks, n_tiles, Wt, P, HR, strips, windows, frames;
+    int h_bytes, h_tx_bytes, n_h, n_w;
+    long long tiles;
+    uint32_t idesc;
+    const uint8_t* w;
+    const void* bias;
+    void* y;
+    unsigned int* status;  // the library's device status word
+};
+
+struct ClTile {
+    int nt, win, strip, fr;
+};
+
+__device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long t) {
+    ClTile c;
+    c.nt = (int)(t % a.n_tiles);
+    t /= a.n_tiles;
+    c.win = (int)(t % a.windows);
+    t /= a.windows;
+    c.strip = (int)(t % a.strips);
+    t /= a.strips;
+    c.fr = (int)t;
+    return c;
+}
+
+__device__ __forceinline__ bool cl_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t spins = 0;
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                atomicOr(status, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float cl_act(float v, int act) {
+    if (act == X3_ACT_RELU) return fmaxf(v, 0.0f);
+    if (act == X3_ACT_CLAMP1) return fminf(1.0f, fmaxf(-1.0f, v));
+    return v;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t cl_round(float v) {
+    if (BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        return *reinterpret_cast<uint16_t*>(&h);
+    } else {
+        __half h = __float2half_rn(v);
+        return *reinterpret_cast<uint16_t*>(&h);
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(192, 1)
+    igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
+                    const __grid_constant__ ClArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
+    uint8_t* sbase = smem_raw + (base - raw_base);
+    const uint32_t sH = base;                                      // halo stages (1024-aligned)
+    const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
+    const uint32_t sStage = sW + (uint32_t)(a.n_w * kWBlock);      // epilogue transpose tile
+    const uint32_t sBar = sStage + 4u * 32u * kStagePitch;
+    const uint32_t bar_h_full = sBar;
+    const uint32_t bar_h_empty = bar_h_full + 8u * a.n_h;
+    const uint32_t bar_w_full = bar_h_empty + 8u * a.n_h;
+    const uint32_t bar_w_empty = bar_w_full + 8u * a.n_w;
+    const uint32_t bar_acc_full = bar_w_empty + 8u * a.n_w;
+    const uint32_t bar_acc_empty = bar_acc_full + 16u;
+    const uint32_t bar_drain = bar_acc_empty + 16u;
+    const uint32_t s_tmem = bar_drain + 8u;
+    const uint32_t s_abort = s_tmem + 4u;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + (s_abort - base));
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + (s_tmem - base));
+    uint8_t* stage_ptr = sbase + (sStage - base);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.n_h; ++i) {
+            ptx::mbar_init(bar_h_full + 8 * i, 1);
+            ptx::mbar_init(bar_h_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < a.n_w; ++i) {
+            ptx::mbar_init(bar_w_full + 8 * i, 1);
+            ptx::mbar_init(bar_w_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar_acc_full + 8 * i, 1);
+            ptx::mbar_init(bar_acc_empty + 8 * i, 4);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_x);
+        ptx::prefetch_tmap(&tm_c);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(s_tmem, 512u);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t h_cnt = 0, w_cnt = 0;
+            bool ok = true;
+            for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
+                const ClTile tc = cl_decode(a, tile);
+                const int n = tc.fr / a.dout, t = tc.fr % a.dout;
+                const int r0 = (tc.win * kBNP) / a.P;
+                const int ow0 = tc.strip * a.Wt;
+                for (int kt = 0; kt < a.KT && ok; ++kt) {
+                    const void* map = &tm_x;
+                    int fcoord;
+                    if (a.KT == 3) {
+                        const int f = t + kt;  // frame of [carry0, carry1, x0, ...] read by tap kt
+                        if (f >= 2) fcoord = n * a.D + (f - 2);
+                        else if (a.has_carry) { map = &tm_c; fcoord = n * 2 + f; }
+                        else fcoord = -1;  // out of range: zeros
+                    } else {
+                        fcoord = n;
+                    }
+                    for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                        const uint32_t sh = h_cnt % a.n_h;
+                        if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
+                        ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
+                        ++h_cnt;
+                        const uint8_t* wblk =
+                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * 9) * (size_t)kWBlock;
+                        for (int tap = 0; tap < 9; ++tap) {
+                            const uint32_t sw = w_cnt % a.n_w;
+                            if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                            ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
+                            ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
+                                           bar_w_full + 8 * sw);
+                            ++w_cnt;
+                        }
+                    }
+                }
+            }
+            if (!ok) {  // wait (bounded) for the copies already issued into each stage
+                volatile int dummy = 0;
+                for (uint32_t i = 0; i < (uint32_t)a.n_h && i < h_cnt; ++i) {
+                    const uint32_t last = i + ((h_cnt - 1 - i) / a.n_h) * a.n_h;
+                    cl_wait(bar_h_full + 8 * i, (last / a.n_h) & 1u, &dummy, a.status);
+                }
+                for (uint32_t i = 0; i < (uint32_t)a.n_w && i < w_cnt; ++i) {
+                    const uint32_t last = i + ((w_cnt - 1 - i) / a.n_w) * a.n_w;
+                    cl_wait(bar_w_full + 8 * i, (last / a.n_w) & 1u, &dummy, a.status);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (one thread)
+        if (lane == 0) {
+            uint32_t h_cnt = 0, w_cnt = 0, it = 0;
+            bool ok = true;
+            // A (weights), no swizzle: SBO = 128 B between 8-row groups, LBO = 2 KB between the two
+            // 8-channel halves of a 16-channel K step; version 1 in bits 46-47.
+            const uint32_t a_hi = (128u >> 4) | (1u << 14);
+            const uint32_t a_lo0 = ((sW >> 4) & 0x3FFFu) | ((uint32_t)((kBM * 16) >> 4) << 16);
+            // B (halo), 128-byte swizzle: SBO = 1024 B between 8-row groups, LBO encoded 1 (unused by
+            // the swizzled K-major layout), version 1, layout type 2 (128-byte swizzle) in bits 61-63,
+            // base offset 0. The tensor core applies the swizzle to the absolute shared-memory address
+            // bits, exactly as the TMA unit wrote them, so a start shifted by any whole number of
+            // 128-byte rows (a spatial tap) or by 32-byte K steps needs no base-offset correction;
+            // the integer-exact parity tests pin this.
+            const uint32_t b_hi_fixed = (1024u >> 4) | (1u << 14) | (2u << 29);
+            for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x, ++it) {
+                const ClTile tc = cl_decode(a, tile);
+                const int pos_off = (tc.win * kBNP) % a.P;
+                const uint32_t ab = it & 1u;
+                if (!cl_wait(bar_acc_empty + 8 * ab, ((it >> 1) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + ab * (uint32_t)kBNP;
+                uint32_t acc = 0;
+                for (int kt = 0; kt < a.KT && ok; ++kt) {
+                    for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                        const uint32_t sh = h_cnt % a.n_h;
+                        if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
+                        for (int kh = 0; kh < 3 && ok; ++kh) {
+                            for (int kw = 0; kw < 3; ++kw) {
+                                const uint32_t sw = w_cnt % a.n_w;
+                                if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
+                                ptx::tc_fence_after();
+                                const uint32_t a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
+                                const uint32_t row_addr = hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
+                                const uint32_t b_hi = b_hi_fixed;
+#pragma unroll
+                                for (int ks = 0; ks < kCK / 16; ++ks) {
+                                    const uint64_t adesc = ((uint64_t)a_hi << 32) |
+                                                           (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kBM * 16) >> 4));
+                                    const uint32_t baddr = row_addr + (uint32_t)ks * 32u;
+                                    const uint64_t bdesc = ((uint64_t)b_hi << 32) |
+                                                           (uint64_t)(((baddr >> 4) & 0x3FFFu) | (1u << 16));
+                                    ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
+                                    acc = 1;
+                                }
+                                ptx::mma_commit(bar_w_empty + 8 * sw);
+                                ++w_cnt;
+                            }
+                        }
+                        if (!ok) break;
+                        ptx::mma_commit(bar_h_empty + 8 * sh);
+                        ++h_cnt;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_acc_full + 8 * ab);
+            }
+            ptx::mma_commit(bar_drain);
+            volatile int dummy = 0;
+            cl_wait(bar_drain, 0, &dummy, a.status);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue: TMEM -> channels-last rows
+        const int q = warp & 3;            // TMEM lane quarter = output channels 32q .. 32q+31
+        const int ew = warp - 2;           // 0..3: this warp's staging block
+        uint32_t it = 0;
+        int cur_nt = -1;
+        float bias_r = 0.0f;
+        uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
+        for (long long tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++it) {
+            const uint32_t ab = it & 1u;
+            if (!cl_wait(bar_acc_full + 8 * ab, (it >> 1) & 1u, abort_flag, a.status)) break;
+            ptx::tc_fence_after();
+            const ClTile tc = cl_decode(a, tile);
+            const int n = tc.fr / a.dout, t = tc.fr % a.dout;
+            const int co_lane = tc.nt * kBM + q * 32 + lane;
+            if (tc.nt != cur_nt) {
+                bias_r = 0.0f;
+                if (a.bias && co_lane < a.C_out) {
+                    const uint16_t raw = __ldg(reinterpret_cast<const unsigned short*>(a.bias) + co_lane);
+                    bias_r = BF16 ? __uint_as_float((uint32_t)raw << 16) : __half2float(__ushort_as_half(raw));
+                }
+                cur_nt = tc.nt;
+            }
+            const int m0 = tc.win * kBNP;
+            const int ow0 = tc.strip * a.Wt;
+            // Each warp transposes its own 32 channels x 32 positions through a private staging
+            // block (no barrier across warps), then writes 64 contiguous bytes per position row.
+            uint8_t* wst = stage_ptr + ew * 32 * kStagePitch;
+            for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
+                ptx::tmem_ld_wait();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
+                        cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = k * 8 + (lane >> 2);
+                    const int seg = lane & 3;
+                    const int m = m0 + chunk * 32 + row;
+                    const int oh = m / a.P, c = m % a.P;
+                    const int ow = ow0 + c;
+                    const int co = tc.nt * kBM + q * 32 + seg * 8;
+                    if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
+                        const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
+                        const size_t off =
+                            ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
+                        *reinterpret_cast<uint4*>(y + off) = val;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_acc_empty + 8 * ab);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem_base, 512u);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, uint64_t W, uint64_t H,
+                       uint64_t F, uint32_t box_w, uint32_t box_h) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return fail(X3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+        }
+        fn = (EncodeTiledFn)f;
+    }
+    cuuint64_t gd[4] = {C, W, H, F};
+    cuuint64_t gs[3] = {C * 2, C * 2 * W, C * 2 * W * H};
+    cuuint32_t bd[4] = {(cuuint32_t)kCK, box_w, box_h, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(ptr), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(X3_ERR_CUDA, "cuTensorMapEncodeTiled (128-byte swizzle) failed (%d)", (int)r);
+    return X3_OK;
+}
+
+}  // namespace
+
+bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
+    const x3_conv_desc& d = p->d;
+    if (d.stride != 1 || d.unpatchify2x2) return false;
+    if (!(d.dims == 3 ? d.layout == X3_NDHWC : d.layout == X3_NHWC)) return false;
+    if (d.C_in % 8 != 0 || d.C_out % 8 != 0 || d.C_out < 96) return false;
+    ClGeom g;
+    memset(&g, 0, sizeof g);
+    g.KT = d.dims == 3 ? 3 : 1;
+    g.n_chunks = (d.C_in + kCK - 1) / kCK;
+    g.n_tiles = (d.C_out + kBM - 1) / kBM;
+    g.frames = d.N * (d.dims == 3 ? d.D : 1);
+    const int H_out = p->H_out, W_out = p->W_out;
+    const int fixed = 1024 + 4 * 32 * kStagePitch + 512;
+    bool found = false;
+    long long best_cost = -1;
+    int cands[80], nc = 0;
+    for (int k = 1; k <= 64; ++k) cands[nc++] = (W_out + k - 1) / k;
+    cands[nc++] = 30; cands[nc++] = 62; cands[nc++] = 126; cands[nc++] = 254;  // P divides 256
+    for (int ci = 0; ci < nc; ++ci) {
+        const int Wt = cands[ci];
+        const int P = Wt + 2;
+        if (P > 256) continue;
+        // halo rows of a 256-position window starting anywhere in a row, plus one above and below
+        const int HR = ((256 % P) == 0 ? 256 / P : (P - 1 + 255) / P + 1) + 2;
+        if (HR > 256) continue;
+        const int need_pos = ((256 % P) == 0 ? 0 : P - 1) + 255 + 2 * P + 2 + 1;
+        const int pos = HR * P > need_pos ? HR * P : need_pos;
+        const int h_bytes = (pos * 128 + 1023) / 1024 * 1024;
+        int n_w = (kSmemLimit - fixed - 2 * h_bytes) / kWBlock;
+        if (n_w > 6) n_w = 6;
+        if (n_w < 3) continue;
+        const int strips = (W_out + Wt - 1) / Wt;
+        const int windows = (int)(((long long)H_out * P + 255) / 256);
+        const long long tiles = (long long)strips * windows * g.frames * g.n_tiles;
+        const long long waves = (tiles + num_sms - 1) / num_sms;
+        // every tile costs the same MMA work: rank by waves, then by weight-ring depth and halo size
+        const long long cost = waves * 100000 + (6 - n_w) * 10000 + (long long)HR * P;
+        if (!found || cost < best_cost) {
+            found = true;
+            best_cost = cost;
+            g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
+            g.n_h = 2; g.n_w = n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
+            g.smem_bytes = fixed + 2 * h_bytes + n_w * kWBlock;
+        }
+    }
+    if (!found) return false;
+    g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
+    p->cl = g;
+    // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64
+    p->g.BN = kBM; p->g.CK = kCK; p->g.n_chunks = g.n_chunks; p->g.n_tiles = g.n_tiles; p->g.KT = g.KT;
+    p->g.b_bytes = kWBlock;
+    return true;
+}
+
+x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                          const void* bias, void* y, cudaStream_t s) {
+    const x3_conv_desc& d = p->d;
+    const ClGeom& g = p->cl;
+    const bool bf16 = d.dtype == X3_BF16;
+    ClArgs a;
+    memset(&a, 0, sizeof a);
+    a.C_in = d.C_in; a.C_out = d.C_out; a.N = d.N; a.D = d.D; a.H = d.H; a.W = d.W;
+    a.H_out = p->H_out; a.W_out = p->W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
+    a.has_carry = carry != nullptr;
+    a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
+    a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
+    a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
+    a.idesc = ptx::idesc_f16(kBM, kBNP, bf16);
+    a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
+    x3_status st0 = device_status_word(&a.status);
+    if (st0 != X3_OK) return st0;
+    CUtensorMap mx, mc;
+    const uint64_t frames_x = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
+    x3_status st = encode_sw128(&mx, bf16, x, d.C_in, d.W, d.H, frames_x, (uint32_t)g.P, (uint32_t)g.HR);
+    if (st != X3_OK) return st;
+    if (carry) {
+        st = encode_sw128(&mc, bf16, carry, d.C_in, d.W, d.H, (uint64_t)d.N * 2, (uint32_t)g.P, (uint32_t)g.HR);
+        if (st != X3_OK) return st;
+    } else {
+        mc = mx;
+    }
+    auto k = bf16 ? igemm_cl_kernel<true> : igemm_cl_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
+    k<<<g.grid, 192, g.smem_bytes, s>>>(mx, mc, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
+}  // namespace x3

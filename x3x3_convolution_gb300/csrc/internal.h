@@ -9,7 +9,7 @@
 
 namespace x3 {
 
-enum KernelKind { K_DIRECT = 0, K_IGEMM = 1 };
+enum KernelKind { K_DIRECT = 0, K_IGEMM = 1, K_IGEMM_CL = 2 };
 
 // A-operand staging modes of the implicit-GEMM engine.
 enum StageMode {
@@ -50,6 +50,20 @@ struct IgemmGeom {
     int grid;          // persistent CTAs
 };
 
+// Tiling of the channels-last engine with output channels as M (128 per tile) and 256 output
+// positions as N: vertical strips Wt columns wide walked as rasters of pitch P = Wt + 2, a tile being
+// a window of 256 consecutive raster positions of one frame; the halo of a window (HR rows of P
+// positions, 64 channels, 128-byte swizzle) is staged once per temporal tap and channel chunk.
+struct ClGeom {
+    int KT, n_chunks, n_tiles;   // temporal taps, 64-channel chunks, 128-channel output tiles
+    int Wt, P, HR;               // strip width, raster pitch, halo rows staged per window
+    int strips, windows, frames; // tiles = strips * windows * frames * n_tiles
+    int h_bytes, h_tx_bytes;     // bytes of one halo stage (1024-aligned) / written by its TMA box
+    int n_h, n_w;                // halo stages, weight-block stages
+    long long tiles;
+    int smem_bytes, grid;
+};
+
 }  // namespace x3
 
 struct x3_conv_plan {
@@ -57,6 +71,7 @@ struct x3_conv_plan {
     int H_out, W_out;
     x3::KernelKind kind;
     x3::IgemmGeom g;
+    x3::ClGeom cl;
     size_t packed_bytes;
     int num_sms;
 };
@@ -80,6 +95,10 @@ x3_status launch_direct(const x3_conv_plan* p, const void* x, const void* carry,
 x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                        const void* bias, void* y, cudaStream_t s);
 bool igemm_plan(x3_conv_plan* p, int num_sms);  // fills p->g; false if the engine can't run it
+bool igemm_cl_plan(x3_conv_plan* p, int num_sms);  // fills p->cl (+ packing fields of p->g)
+x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                          const void* bias, void* y, cudaStream_t s);
 x3_status read_device_status(int reset);
+x3_status device_status_word(unsigned int** out);  // device address of the timeout status word
 
 }  // namespace x3
