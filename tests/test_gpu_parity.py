@@ -54,7 +54,10 @@ CASES_2D = [
     (2, 64, 48, 16, 64, 1, "none"),      # C_out not a multiple of the N tile
     (1, 24, 16, 9, 8, 1, "relu"),        # C_in not a multiple of the channel chunk
     (1, 1, 16, 1, 8, 1, "none"),         # a single row
-    (2, 64, 64, 34, 70, 2, "relu"),      # stride 2
+    (2, 64, 64, 34, 70, 2, "relu"),      # stride 2, width not a multiple of 8 (direct kernel)
+    (2, 64, 64, 34, 72, 2, "relu"),      # stride 2 on the tensor cores (phase planes)
+    (1, 16, 32, 33, 136, 2, "none"),     # stride 2, odd height, ragged output tile
+    (1, 3, 64, 9, 264, 2, "relu"),       # stride 2, 3 input channels
 ]
 
 
@@ -66,7 +69,7 @@ def test_conv2d_nchw(case, variant, kernel):
     x, L = synth.conv2d_single(N=N, C=Ci, C_out=Co, H=H, W=W, stride=s, act=act, variant=variant,
                                seed=2000 + sum(case[:6]))
     got, conv = run2d(x, L, kernel=kernel)
-    if kernel == "auto" and s == 1:
+    if kernel == "auto" and W % 8 == 0:
         assert conv.kernel_name.startswith("igemm_tcgen05")
     ref = oracle2d(x, L)
     if variant == "int":

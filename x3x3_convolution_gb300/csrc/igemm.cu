@@ -54,6 +54,7 @@ struct IgemmArgs {
     int act, out_kind, has_carry;
     int BN, n_tiles, CK, n_chunks, KT, NSUB, Rt, Wt, P, spr, halo_rows, plane_stride, a_bytes, a_tx_bytes;
     int raw_w, raw_bytes, raw_tx_bytes, b_bytes, n_a, n_b, n_raw, acc_bufs, tmem_cols;
+    int stride, raw_rows, phase_stride;  // NCHW: input stride, raw tile rows, bytes between phase planes
     int col_tiles, row_tiles, frames;
     int scr_pitch;  // epilogue scratch row pitch in bytes (0 = direct stores)
     long long tiles;
@@ -291,8 +292,8 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
                             const uint32_t st = r_cnt % a.n_raw;
                             if (!wait_bar(bar_r_empty + 8 * st, ((r_cnt / a.n_raw) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_r_full + 8 * st, (uint32_t)a.raw_tx_bytes);
-                            ptx::tma_load_4d(sRaw + st * a.raw_bytes, &tm_x, bar_r_full + 8 * st, tc.ow0 - 8,
-                                             tc.oh0 - 1, cc * a.CK, n);
+                            ptx::tma_load_4d(sRaw + st * a.raw_bytes, &tm_x, bar_r_full + 8 * st,
+                                             a.stride * tc.ow0 - 8, a.stride * tc.oh0 - 1, cc * a.CK, n);
                             ++r_cnt;
                         }
                         const uint8_t* wblk = a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * 9) * a.b_bytes;
@@ -346,7 +347,14 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
             const uint32_t a_ks16 = (uint32_t)(2 * a.plane_stride) >> 4, b_ks16 = (uint32_t)(2 * a.BN * 16) >> 4;
             const int ksteps = a.CK / 16;
             const int nsub = a.NSUB;
-            uint32_t soff[8], dcol[8];
+            uint32_t soff[8], dcol[8], toff[9];
+            for (int tap = 0; tap < 9; ++tap) {
+                const int kh = tap / 3, kw = tap % 3;
+                toff[tap] = a.stride == 1
+                                ? (uint32_t)(kh * a.P + kw)
+                                : (uint32_t)((((kh & 1) * 2 + (kw & 1)) * a.phase_stride) >> 4) +
+                                      (uint32_t)((kh >> 1) * a.P + (kw >> 1));
+            }
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 soff[s] = s < nsub ? (uint32_t)sub_off(a, s) : 0u;  // raster offset = 16-byte units
@@ -364,14 +372,13 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
                         if (!wait_bar(bar_a_full + 8 * sa, (a_cnt / a.n_a) & 1u, abort_flag)) { ok = false; break; }
                         ptx::tc_fence_after();
                         const uint32_t a_lo_stage = a_lo0 + sa * a_stage16;
-                        uint32_t tap_off = 0;
-                        for (int kh = 0; kh < 3 && ok; ++kh, tap_off += (uint32_t)a.P) {
+                        for (int kh = 0; kh < 3 && ok; ++kh) {
                             for (int kw = 0; kw < 3; ++kw) {
                                 const uint32_t sb = b_cnt % a.n_b;
                                 if (!wait_bar(bar_b_full + 8 * sb, (b_cnt / a.n_b) & 1u, abort_flag)) { ok = false; break; }
                                 ptx::tc_fence_after();
                                 const uint32_t b_lo = b_lo0 + sb * b_stage16;
-                                const uint32_t a_lo = a_lo_stage + tap_off + (uint32_t)kw;
+                                const uint32_t a_lo = a_lo_stage + toff[kh * 3 + kw];
 #pragma unroll
                                 for (int ks = 0; ks < 2; ++ks) {
                                     if (ks < ksteps) {
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
         const int tw = warp - 6;  // 0..3
         uint32_t a_cnt = 0, r_cnt = 0;
         const int kb_n = a.raw_w / 8;                       // 8-column blocks per raw row
-        const int nblk = kpl * a.halo_rows * kb_n;          // 8x8 blocks per stage
+        const int nblk = kpl * a.raw_rows * kb_n;           // 8x8 blocks per stage
         const uint32_t junk = s_junk + (uint32_t)(tw * 32 + lane) * 16u;
         bool ok = true;
         for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
@@ -514,14 +521,21 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
                     if (blk < nblk) {
                         const int kb = blk % kb_n;
                         const int rest = blk / kb_n;
-                        const int hr = rest % a.halo_rows;
-                        const int j = rest / a.halo_rows;
+                        const int hr = rest % a.raw_rows;
+                        const int j = rest / a.raw_rows;
                         // source row i: channel 8j+i, halo row hr, raw columns 8kb..8kb+7
-                        lds_addr = raw + (uint32_t)(((8 * j + i) * a.halo_rows + hr) * a.raw_w + 8 * kb) * 2u;
+                        lds_addr = raw + (uint32_t)(((8 * j + i) * a.raw_rows + hr) * a.raw_w + 8 * kb) * 2u;
                         // destination row i: raw column 8kb+i = halo position 8kb+i-7 of row hr
                         const int q = 8 * kb + i - 7;
-                        if (q >= 0 && q < a.P)
-                            sts_addr = A + (uint32_t)j * a.plane_stride + (uint32_t)(hr * a.P + q) * 16u;
+                        if (a.stride == 1) {
+                            if (q >= 0 && q < a.P)
+                                sts_addr = A + (uint32_t)j * a.plane_stride + (uint32_t)(hr * a.P + q) * 16u;
+                        } else if (q >= 0 && q <= 2 * a.Wt) {
+                            // stride 2: de-interleave into the (row parity, column parity) phase planes
+                            const uint32_t ph = (uint32_t)((hr & 1) * 2 + (q & 1));
+                            sts_addr = A + ph * (uint32_t)a.phase_stride + (uint32_t)j * a.plane_stride +
+                                       (uint32_t)((hr >> 1) * a.P + (q >> 1)) * 16u;
+                        }
                     } else {
                         lds_addr = raw;
                     }
@@ -555,13 +569,15 @@ static bool fill_smem(IgemmGeom& g, int max_read_pos) {
     const int kpl = g.CK / 8;
     g.plane_pos = g.halo_rows * g.P;
     g.plane_stride = round_up(g.plane_pos * 16, 128);
+    const int phases = g.stride == 1 ? 1 : 4;
+    g.phase_stride = kpl * g.plane_stride;
     const int last_plane_pos = max_read_pos + 1 > g.plane_pos ? max_read_pos + 1 : g.plane_pos;
-    g.a_bytes = round_up((kpl - 1) * g.plane_stride + last_plane_pos * 16, 128);
+    g.a_bytes = round_up((phases * kpl - 1) * g.plane_stride + last_plane_pos * 16, 128);
     g.a_tx_bytes = kpl * g.plane_pos * 16;
     g.b_bytes = g.BN * g.CK * 2;
     if (g.mode == STAGE_NCHW) {
-        g.raw_w = g.Wt + 16;
-        g.raw_bytes = round_up(g.CK * g.halo_rows * g.raw_w * 2, 128);
+        g.raw_w = g.stride * g.Wt + 16;
+        g.raw_bytes = round_up(g.CK * g.raw_rows * g.raw_w * 2, 128);
     } else {
         g.raw_w = 0;
         g.raw_bytes = 0;
@@ -608,7 +624,8 @@ bool igemm_plan(x3_conv_plan* p, int num_sms) {
     const x3_conv_desc& d = p->d;
     IgemmGeom g;
     memset(&g, 0, sizeof g);
-    if (d.stride != 1) return false;
+    g.stride = d.stride;
+    if (d.stride != 1 && !(d.dims == 2 && d.layout == X3_NCHW)) return false;
     if (d.dims == 3) {
         if (d.layout != X3_NDHWC) return false;
         g.mode = STAGE_CL;
@@ -646,19 +663,23 @@ bool igemm_plan(x3_conv_plan* p, int num_sms) {
         const int Wt = wt_cands[ci], spr = spr_cands[ci];
         const int P = Wt + 2;
         if (Wt < 1 || P > 256) continue;
-        if (g.mode == STAGE_NCHW && (Wt % 8 != 0 || Wt + 16 > 256)) continue;
+        if (g.mode == STAGE_NCHW && (Wt % 8 != 0 || g.stride * Wt + 16 > 256)) continue;
         for (int bufs = 2; bufs >= 1; --bufs) {
             int nsub_cap = 512 / (g.BN * bufs);
             if (nsub_cap > 8) nsub_cap = 8;
             for (int Rt = 1; Rt <= 64; ++Rt) {
                 IgemmGeom c = g;
-                c.Wt = Wt; c.P = P; c.spr = spr; c.Rt = Rt; c.halo_rows = Rt + 2;
+                c.Wt = Wt; c.P = P; c.spr = spr; c.Rt = Rt;
+                // stride 2 stages Rt+1 rows per phase plane (even rows: 0,2,..,2Rt; odd: 1,..,2Rt-1)
+                c.halo_rows = c.stride == 1 ? Rt + 2 : Rt + 1;
+                c.raw_rows = c.stride == 1 ? Rt + 2 : 2 * Rt + 1;
                 c.acc_bufs = bufs;
                 c.NSUB = spr ? Rt * spr : (Rt * P + 127) / 128;
                 if (c.NSUB > nsub_cap || c.halo_rows > 256) break;
                 int max_read;
-                if (spr) max_read = (Rt - 1) * P + (spr - 1) * 128 + 127 + 2 * P + 2;
-                else max_read = c.NSUB * 128 - 1 + 2 * P + 2;
+                const int tap_reach = c.stride == 1 ? 2 * P + 2 : P + 1;  // furthest tap offset
+                if (spr) max_read = (Rt - 1) * P + (spr - 1) * 128 + 127 + tap_reach;
+                else max_read = c.NSUB * 128 - 1 + tap_reach;
                 if (!fill_smem(c, max_read)) break;
                 int cols = c.NSUB * c.BN * bufs, tc = 32;
                 while (tc < cols) tc *= 2;
@@ -748,7 +769,8 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     a.BN = g.BN; a.n_tiles = g.n_tiles; a.CK = g.CK; a.n_chunks = g.n_chunks; a.KT = g.KT; a.NSUB = g.NSUB;
     a.Rt = g.Rt; a.Wt = g.Wt; a.P = g.P; a.spr = g.spr; a.halo_rows = g.halo_rows; a.plane_stride = g.plane_stride;
     a.a_bytes = g.a_bytes; a.a_tx_bytes = g.a_tx_bytes; a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes;
-    a.raw_tx_bytes = g.CK * g.halo_rows * g.raw_w * 2; a.b_bytes = g.b_bytes; a.n_a = g.n_a; a.n_b = g.n_b;
+    a.raw_tx_bytes = g.CK * g.raw_rows * g.raw_w * 2; a.b_bytes = g.b_bytes; a.n_a = g.n_a; a.n_b = g.n_b;
+    a.stride = g.stride; a.raw_rows = g.raw_rows; a.phase_stride = g.phase_stride;
     a.n_raw = g.n_raw; a.acc_bufs = g.acc_bufs; a.tmem_cols = g.tmem_cols;
     a.col_tiles = g.col_tiles; a.row_tiles = g.row_tiles; a.frames = g.frames; a.tiles = g.tiles;
     a.scr_pitch = g.scr_pitch;
@@ -778,7 +800,7 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     }
     const uint64_t dims[4] = {(uint64_t)d.W, (uint64_t)d.H, (uint64_t)d.C_in, (uint64_t)d.N};
     const uint64_t strides[3] = {(uint64_t)d.W * 2, (uint64_t)d.W * d.H * 2, (uint64_t)d.W * d.H * d.C_in * 2};
-    const uint32_t box[4] = {(uint32_t)g.raw_w, (uint32_t)g.halo_rows, (uint32_t)g.CK, 1};
+    const uint32_t box[4] = {(uint32_t)g.raw_w, (uint32_t)g.raw_rows, (uint32_t)g.CK, 1};
     st = encode4d(&mx, bf16, x, dims, strides, box);
     if (st != X3_OK) return st;
     mc = mx;

@@ -32,7 +32,10 @@ struct IgemmGeom {
     int NSUB;          // 128-row MMA subtiles per tile
     int Rt, Wt, P;     // output rows / columns per tile, halo raster pitch in positions
     int spr;           // row-aligned subtile mapping: subtiles per output row; 0 = flat (128*s)
-    int halo_rows;     // Rt + 2
+    int halo_rows;     // rows per staged plane: Rt + 2 (stride 1) or Rt + 1 per phase plane (stride 2)
+    int stride;        // 1, or 2 (NCHW only: four phase planes)
+    int raw_rows;      // NCHW: rows of the raw tile (Rt + 2, or 2 Rt + 1 for stride 2)
+    int phase_stride;  // bytes between the phase planes of a stride-2 stage
     int plane_pos;     // positions per K-major plane (halo_rows * P)
     int plane_stride;  // bytes between planes (plane_pos * 16)
     int a_bytes;       // bytes of one A stage (CK/8 planes + read slack)
