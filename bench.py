@@ -270,6 +270,29 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(wl, args, stream, fl, nb):
+    """Warm up, then time `steps` runs of one stage alone (CUDA events); one JSON line."""
+    import torch
+    fn = {"taesd": lambda: wl.taesd(wl.taesd_x, out=wl.taesd_y, stream=stream),
+          "stack": lambda: wl.stack(wl.stack_x, carries=wl.stack_carries, carry_valid=True, out=wl.stack_y,
+                                    stream=stream),
+          "l3": lambda: wl.l3(wl.l3_x, wl.l3_c, out=wl.l3_y, stream=stream),
+          "head": lambda: wl.head(wl.head_x, wl.head_c, out=wl.head_y, stream=stream)}[args.stage]
+    for _ in range(args.warmup):
+        fn()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"stage": args.stage, "ms": ms, "tflops": fl[args.stage] / (ms * 1e-3) / 1e12,
+                      "gbs": nb[args.stage] / (ms * 1e-3) / 1e9, "plan": wl.plans[args.stage]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -278,6 +301,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", choices=STAGES, default=None,
+                    help="run only this stage per step (for profiler captures); prints its per-launch time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -303,6 +328,9 @@ def main():
     fl, nb = stage_cost()
     total_flop = sum(fl.values())
 
+    if args.stage:
+        run_stage(wl, args, stream, fl, nb)
+        return
     for _ in range(args.warmup):
         wl.step(stream)
     torch.cuda.synchronize()
