@@ -141,16 +141,16 @@ def _check_sw128_plan(g):
     assert P == Wt + 2 and P <= 256 and HR <= 256
     # the furthest halo row read: a window starting at offset P-1 of a row (or 0 when P divides
     # 256), its last position, tap (kh=2, kw=2)
-    pos_off_max = 0 if 256 % P == 0 else P - 1
-    assert (pos_off_max + 255 + 2 * P + 2 + 1) * 128 <= g["h_bytes"]
-    # the rows a window touches, plus one above and below, are all staged
+    adv = g["win_adv"]
+    assert adv == (254 if g["kwm"] else 256)
+    # furthest halo row read by a window: its start offset in the first row, its last column,
+    # kh = 2 (+2P) and, unless kw is folded into M, kw = 2 (+2); every such row is staged by the box
     for win in range(min(g["windows"], 4 * P)):
-        m0 = 256 * win
-        r0 = m0 // P
-        last_row = (m0 + 255) // P
-        assert last_row + 1 - (r0 - 1) + 1 <= HR
+        pos_off = (adv * win) % P
+        need = pos_off + 255 + 2 * P + (0 if g["kwm"] else 2) + 1
+        assert need <= HR * P and need * 128 <= g["h_bytes"]
     assert g["h_bytes"] % 1024 == 0 and g["smem_bytes"] <= 232448
-    assert g["strips"] * Wt >= g["W_out"] and g["windows"] * 256 >= g["H_out"] * P
+    assert g["strips"] * Wt >= g["W_out"] and g["windows"] * adv >= g["H_out"] * P
     assert g["tiles"] == g["strips"] * g["windows"] * g["frames"] * g["n_tiles"]
 
 
@@ -159,7 +159,7 @@ def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
-        if g["kernel"] == "igemm_tcgen05_sw128":
+        if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head"):
             _check_sw128_plan(g)
             return
         assert g["kernel"] == "igemm_tcgen05"

@@ -151,11 +151,13 @@ def test_conv3d_causal(case, variant, kernel, monkeypatch):
         assert_close(got, ref)
 
 
+@pytest.mark.parametrize("shape", [(2, 9, 140), (3, 5, 300), (1, 17, 33)], ids=str)
 @pytest.mark.parametrize("variant", ["sparse1", "random"])
-def test_head_clamp_unpatchify(variant):
-    x, carry, L = synth.head(D=2, H=9, W=140, variant=variant, seed=3500)
+def test_head_clamp_unpatchify(variant, shape):
+    D, H, W = shape
+    x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3500 + H)
     got, conv = run3d(x, carry, L, unpatch=True)
-    assert conv.kernel_name == "igemm_tcgen05"
+    assert conv.kernel_name == "igemm_tcgen05_sw128_head"
     ref12 = oracle3d(x, carry, L)                                   # [1, D, H, W, 12]
     ref = oracle.unpatchify2x2(ref12.transpose(0, 4, 1, 2, 3))      # [1, 3, D, 2H, 2W]
     ref = ref.transpose(0, 2, 3, 4, 1)                              # [1, D, 2H, 2W, 3]
@@ -193,7 +195,7 @@ def test_full_size_sampled(name):
 def test_full_size_head_sampled():
     x, carry, L = synth.head(seed=3950)
     got, conv = run3d(x, carry, L, unpatch=True)
-    assert conv.kernel_name == "igemm_tcgen05"
+    assert conv.kernel_name == "igemm_tcgen05_sw128_head"
     assert got.shape == (1, 4, 704, 1248, 3)
     seq = np.concatenate([carry.vals, x.vals], axis=1)
     pos = sample_positions(4, 352, 624, 400, seed=7)

@@ -157,7 +157,39 @@ __global__ void __launch_bounds__(256) pack_igemm_kernel(const uint16_t* __restr
     }
 }
 
+// Packed layout of the head form of the channels-last engine: blocks ordered [kt][chunk][kh], each
+// the K-major canonical A tile of 128 rows x 64 input channels, [8 planes][128 rows][8 channels],
+// where row 32*g + kw*10 + r carries tap (kt, kh, kw) of output channel 10*g + r (zero elsewhere).
+__global__ void __launch_bounds__(256) pack_kwm_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                       int C_in, int C_out, int KT, int n_chunks, size_t total) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        size_t r = i;
+        const int e = (int)(r % 8); r /= 8;
+        const int row = (int)(r % 128); r /= 128;
+        const int j = (int)(r % 8); r /= 8;
+        const int kh = (int)(r % 3); r /= 3;
+        const int cc = (int)(r % n_chunks); r /= n_chunks;
+        const int kt = (int)r;
+        const int g = row / 32, within = row % 32;
+        const int kw = within / 10, co = g * 10 + within % 10;
+        const int ci = cc * 64 + j * 8 + e;
+        uint16_t v = 0;
+        if (within < 30 && co < C_out && ci < C_in) v = w[(((size_t)co * C_in + ci) * KT + kt) * 9 + kh * 3 + kw];
+        out[i] = v;
+    }
+}
+
 x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s) {
+    if (p->kind == K_IGEMM_CL && p->cl.kwm) {
+        const size_t total = p->packed_bytes / 2;
+        size_t blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        pack_kwm_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, p->d.C_in,
+                                                        p->d.C_out, p->cl.KT, p->cl.n_chunks, total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
     if (p->kind == K_DIRECT) {
         cudaError_t e = cudaMemcpyAsync(w_packed, w, p->packed_bytes, cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return fail(X3_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));

@@ -44,11 +44,15 @@ constexpr int kBNP = 256;       // positions per tile (MMA N)
 constexpr int kCK = 64;         // input channels per staged chunk (one 128-byte swizzle row)
 constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one tap, one chunk)
 constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
+constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
+constexpr int kStageWarpBytes = 32 * kSPitch * 4;  // per-warp staging block (covers both uses)
 
 struct ClArgs {
     int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
     int KT, n_chunks, n_tiles, Wt, P, HR, strips, windows, frames;
     int h_bytes, h_tx_bytes, n_h, n_w;
+    int win_adv;     // raster positions between consecutive windows (256, or 254 when kw is folded into M)
+    int ngroups;     // kw folded into M: channel groups (10 channels x 3 kw per TMEM lane quarter)
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -107,7 +111,11 @@ __device__ __forceinline__ uint16_t cl_round(float v) {
     }
 }
 
-template <bool BF16>
+// KWM (the conv_out head form): the MMA's M rows are (kw, output channel) triples, quarter g of the
+// 128 TMEM lanes holding kw*10 + r for channel 10g + r, so one MMA covers the three horizontal taps
+// of a row of the window and the K loop runs over (kt, kh, channel) only; the epilogue adds the three
+// kw partial sums with their one- and two-column shifts, all inside one warp's lane quarter.
+template <bool BF16, bool KWM>
 __global__ void __launch_bounds__(192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -118,7 +126,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
     const uint32_t sStage = sW + (uint32_t)(a.n_w * kWBlock);      // epilogue transpose tile
-    const uint32_t sBar = sStage + 4u * 32u * kStagePitch;
+    const uint32_t sBar = sStage + 4u * (uint32_t)kStageWarpBytes;
     const uint32_t bar_h_full = sBar;
     const uint32_t bar_h_empty = bar_h_full + 8u * a.n_h;
     const uint32_t bar_w_full = bar_h_empty + 8u * a.n_h;
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(192, 1)
             for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
                 const ClTile tc = cl_decode(a, tile);
                 const int n = tc.fr / a.dout, t = tc.fr % a.dout;
-                const int r0 = (tc.win * kBNP) / a.P;
+                const int r0 = (tc.win * a.win_adv) / a.P;
                 const int ow0 = tc.strip * a.Wt;
                 for (int kt = 0; kt < a.KT && ok; ++kt) {
                     const void* map = &tm_x;
@@ -192,9 +200,10 @@ __global__ void __launch_bounds__(192, 1)
                         ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
                         ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                         ++h_cnt;
+                        constexpr int kTaps = KWM ? 3 : 9;
                         const uint8_t* wblk =
-                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * 9) * (size_t)kWBlock;
-                        for (int tap = 0; tap < 9; ++tap) {
+                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTaps) * (size_t)kWBlock;
+                        for (int tap = 0; tap < kTaps; ++tap) {
                             const uint32_t sw = w_cnt % a.n_w;
                             if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t b_hi_fixed = (1024u >> 4) | (1u << 14) | (2u << 29);
             for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x, ++it) {
                 const ClTile tc = cl_decode(a, tile);
-                const int pos_off = (tc.win * kBNP) % a.P;
+                const int pos_off = (tc.win * a.win_adv) % a.P;
                 const uint32_t ab = it & 1u;
                 if (!cl_wait(bar_acc_empty + 8 * ab, ((it >> 1) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                 ptx::tc_fence_after();
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(192, 1)
                         ptx::tc_fence_after();
                         const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
                         for (int kh = 0; kh < 3 && ok; ++kh) {
-                            for (int kw = 0; kw < 3; ++kw) {
+                            for (int kw = 0; kw < (KWM ? 1 : 3); ++kw) {
                                 const uint32_t sw = w_cnt % a.n_w;
                                 if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
                                 ptx::tc_fence_after();
@@ -290,6 +299,16 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t it = 0;
         int cur_nt = -1;
         float bias_r = 0.0f;
+        float bias_g[10];
+#pragma unroll
+        for (int r = 0; r < 10; ++r) {
+            const int co = q * 10 + r;
+            bias_g[r] = 0.0f;
+            if (KWM && a.bias && co < a.C_out) {
+                const uint16_t raw = __ldg(reinterpret_cast<const unsigned short*>(a.bias) + co);
+                bias_g[r] = BF16 ? __uint_as_float((uint32_t)raw << 16) : __half2float(__ushort_as_half(raw));
+            }
+        }
         uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
         for (long long tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++it) {
             const uint32_t ab = it & 1u;
@@ -306,34 +325,77 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 cur_nt = tc.nt;
             }
-            const int m0 = tc.win * kBNP;
+            const int m0 = tc.win * a.win_adv;
             const int ow0 = tc.strip * a.Wt;
-            // Each warp transposes its own 32 channels x 32 positions through a private staging
-            // block (no barrier across warps), then writes 64 contiguous bytes per position row.
-            uint8_t* wst = stage_ptr + ew * 32 * kStagePitch;
-            for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
-                uint32_t v[32];
-                ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
-                ptx::tmem_ld_wait();
-                __syncwarp();
+            if (KWM) {
+                // Lane kw*10 + r of quarter q holds the partial sums of channel 10q + r over the taps
+                // with that kw, at every window column; output column j adds kw = 0, 1, 2 at columns
+                // j, j+1, j+2 (its left, centre and right input columns).
+                if (q < a.ngroups) {
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * kStageWarpBytes);
+                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                        uint32_t v[32], e2[2] = {0u, 0u};
+                        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP +
+                                               (uint32_t)(chunk * 32);
+                        ptx::tmem_ld32(taddr, v);
+                        if (chunk + 1 < kBNP / 32) ptx::tmem_ld2(taddr + 32u, e2);
+                        ptx::tmem_ld_wait();
+                        __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
-                        cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
-                __syncwarp();
+                        for (int j = 0; j < 32; ++j) S[lane * kSPitch + j] = __uint_as_float(v[j]);
+                        S[lane * kSPitch + 32] = __uint_as_float(e2[0]);
+                        S[lane * kSPitch + 33] = __uint_as_float(e2[1]);
+                        __syncwarp();
+                        const int jw = chunk * 32 + lane;  // column of the window
+                        const int m = m0 + jw;
+                        const int oh = m / a.P, c = m % a.P;
+                        const int ow = ow0 + c;
+                        if (jw < a.win_adv && c < a.Wt && ow < a.W_out && oh < a.H_out) {
+                            const size_t W2 = 2 * (size_t)a.W_out;
+                            const size_t row0 = (((size_t)n * a.dout + t) * 2 * (size_t)a.H_out + 2 * (size_t)oh);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int row = k * 8 + (lane >> 2);
-                    const int seg = lane & 3;
-                    const int m = m0 + chunk * 32 + row;
-                    const int oh = m / a.P, c = m % a.P;
-                    const int ow = ow0 + c;
-                    const int co = tc.nt * kBM + q * 32 + seg * 8;
-                    if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
-                        const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
-                        const size_t off =
-                            ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
-                        *reinterpret_cast<uint4*>(y + off) = val;
+                            for (int r = 0; r < 10; ++r) {
+                                const int co = q * 10 + r;
+                                if (co < a.C_out) {
+                                    const float acc = S[r * kSPitch + lane] + S[(10 + r) * kSPitch + lane + 1] +
+                                                      S[(20 + r) * kSPitch + lane + 2] + bias_g[r];
+                                    // unpatchify: channel co = rgb*4 + dy*2 + dx -> pixel (2oh+dy, 2ow+dx)
+                                    const int rgb = co >> 2, dy = (co >> 1) & 1, dx = co & 1;
+                                    y[((row0 + dy) * W2 + 2 * (size_t)ow + dx) * 3 + rgb] =
+                                        cl_round<BF16>(cl_act(acc, a.act));
+                                }
+                            }
+                        }
+                    }
+                }
+            } else {
+                // Each warp transposes its own 32 channels x 32 positions through a private staging
+                // block (no barrier across warps), then writes 64 contiguous bytes per position row.
+                uint8_t* wst = stage_ptr + ew * kStageWarpBytes;
+                for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
+                    ptx::tmem_ld_wait();
+                    __syncwarp();
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
+                            cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
+                    __syncwarp();
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = k * 8 + (lane >> 2);
+                        const int seg = lane & 3;
+                        const int m = m0 + chunk * 32 + row;
+                        const int oh = m / a.P, c = m % a.P;
+                        const int ow = ow0 + c;
+                        const int co = tc.nt * kBM + q * 32 + seg * 8;
+                        if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
+                            const size_t off =
+                                ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
+                            *reinterpret_cast<uint4*>(y + off) = val;
+                        }
                     }
                 }
             }
@@ -382,17 +444,23 @@ x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, u
 
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     const x3_conv_desc& d = p->d;
-    if (d.stride != 1 || d.unpatchify2x2) return false;
+    if (d.stride != 1) return false;
     if (!(d.dims == 3 ? d.layout == X3_NDHWC : d.layout == X3_NHWC)) return false;
-    if (d.C_in % 8 != 0 || d.C_out % 8 != 0 || d.C_out < 96) return false;
+    if (d.C_in % 8 != 0) return false;
     ClGeom g;
     memset(&g, 0, sizeof g);
+    // the conv_out head (12 channels to unpatchified RGB) runs in the kw-folded form
+    g.kwm = d.unpatchify2x2 ? 1 : 0;
+    if (!g.kwm && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
+    g.win_adv = g.kwm ? kBNP - 2 : kBNP;
+    g.ngroups = g.kwm ? (d.C_out + 9) / 10 : 0;
+    if (g.kwm && g.ngroups > 4) return false;
     g.KT = d.dims == 3 ? 3 : 1;
     g.n_chunks = (d.C_in + kCK - 1) / kCK;
     g.n_tiles = (d.C_out + kBM - 1) / kBM;
     g.frames = d.N * (d.dims == 3 ? d.D : 1);
     const int H_out = p->H_out, W_out = p->W_out;
-    const int fixed = 1024 + 4 * 32 * kStagePitch + 512;
+    const int fixed = 1024 + 4 * kStageWarpBytes + 512;
     bool found = false;
     long long best_cost = -1;
     int cands[80], nc = 0;
@@ -403,16 +471,19 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
         const int P = Wt + 2;
         if (P > 256) continue;
         // halo rows of a 256-position window starting anywhere in a row, plus one above and below
-        const int HR = ((256 % P) == 0 ? 256 / P : (P - 1 + 255) / P + 1) + 2;
+        // furthest B row read: window start offset within its row (0 when windows of 256 tile the
+        // rows exactly), the window's last column, kh = 2 (+2P) and, unless folded into M, kw = 2 (+2)
+        const int pos_off_max = (g.win_adv == 256 && (256 % P) == 0) ? 0 : P - 1;
+        const int need_pos = pos_off_max + 255 + 2 * P + (g.kwm ? 0 : 2) + 1;
+        const int HR = (need_pos + P - 1) / P;
         if (HR > 256) continue;
-        const int need_pos = ((256 % P) == 0 ? 0 : P - 1) + 255 + 2 * P + 2 + 1;
         const int pos = HR * P > need_pos ? HR * P : need_pos;
         const int h_bytes = (pos * 128 + 1023) / 1024 * 1024;
         int n_w = (kSmemLimit - fixed - 2 * h_bytes) / kWBlock;
         if (n_w > 6) n_w = 6;
         if (n_w < 3) continue;
         const int strips = (W_out + Wt - 1) / Wt;
-        const int windows = (int)(((long long)H_out * P + 255) / 256);
+        const int windows = (int)(((long long)H_out * P + g.win_adv - 1) / g.win_adv);
         const long long tiles = (long long)strips * windows * g.frames * g.n_tiles;
         const long long waves = (tiles + num_sms - 1) / num_sms;
         // every tile costs the same MMA work: rank by waves, then by weight-ring depth and halo size
@@ -428,7 +499,8 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     if (!found) return false;
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
     p->cl = g;
-    // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64
+    // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
+    // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
     p->g.BN = kBM; p->g.CK = kCK; p->g.n_chunks = g.n_chunks; p->g.n_tiles = g.n_tiles; p->g.KT = g.KT;
     p->g.b_bytes = kWBlock;
     return true;
@@ -447,6 +519,7 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
+    a.win_adv = g.win_adv; a.ngroups = g.ngroups;
     a.idesc = ptx::idesc_f16(kBM, kBNP, bf16);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
     x3_status st0 = device_status_word(&a.status);
@@ -461,7 +534,8 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
     } else {
         mc = mx;
     }
-    auto k = bf16 ? igemm_cl_kernel<true> : igemm_cl_kernel<false>;
+    auto k = g.kwm ? (bf16 ? igemm_cl_kernel<true, true> : igemm_cl_kernel<false, true>)
+                   : (bf16 ? igemm_cl_kernel<true, false> : igemm_cl_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
     k<<<g.grid, 192, g.smem_bytes, s>>>(mx, mc, a);

@@ -63,6 +63,9 @@ struct ClGeom {
     int strips, windows, frames; // tiles = strips * windows * frames * n_tiles
     int h_bytes, h_tx_bytes;     // bytes of one halo stage (1024-aligned) / written by its TMA box
     int n_h, n_w;                // halo stages, weight-block stages
+    int kwm;                     // 1: kw folded into M (the conv_out head form, unpatchify epilogue)
+    int win_adv;                 // raster positions between consecutive windows (256, or 254 when kwm)
+    int ngroups;                 // kwm: groups of 10 output channels (one TMEM lane quarter each)
     long long tiles;
     int smem_bytes, grid;
 };
