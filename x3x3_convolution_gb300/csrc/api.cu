@@ -140,6 +140,7 @@ void conv_plan_destroy(x3_conv_plan* plan) { delete plan; }
 const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
     if (!plan) return "";
     if (plan->kind == K_IGEMM_CL && plan->cl.kwm) return "igemm_tcgen05_sw128_head";
+    if (plan->kind == K_IGEMM_CL && plan->cl.nchw) return "igemm_tcgen05_sw128_nchw";
     return plan->kind == K_IGEMM_CL ? "igemm_tcgen05_sw128" : plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
 }
 
@@ -154,10 +155,10 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
                         "{\"kernel\": \"igemm_tcgen05_sw128\", \"mode\": \"channels_last_sw128_swapped\", "
                         "\"BM\": 128, \"BN\": 256, \"CK\": 64, \"n_tiles\": %d, \"n_chunks\": %d, \"KT\": %d, "
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
-                        "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"win_adv\": %d, \"tiles\": %lld, "
+                        "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
-                        c.n_w, c.kwm, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms);
+                        c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",

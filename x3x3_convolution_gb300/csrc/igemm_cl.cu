@@ -52,6 +52,7 @@ struct ClArgs {
     int KT, n_chunks, n_tiles, Wt, P, HR, strips, windows, frames;
     int h_bytes, h_tx_bytes, n_h, n_w;
     int win_adv;     // raster positions between consecutive windows (256, or 254 when kw is folded into M)
+    int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW: raw tile columns, stage bytes, TMA bytes, stages
     int ngroups;     // kw folded into M: channel groups (10 channels x 3 kw per TMEM lane quarter)
     long long tiles;
     uint32_t idesc;
@@ -115,8 +116,11 @@ __device__ __forceinline__ uint16_t cl_round(float v) {
 // 128 TMEM lanes holding kw*10 + r for channel 10g + r, so one MMA covers the three horizontal taps
 // of a row of the window and the K loop runs over (kt, kh, channel) only; the epilogue adds the three
 // kw partial sums with their one- and two-column shifts, all inside one warp's lane quarter.
-template <bool BF16, bool KWM>
-__global__ void __launch_bounds__(192, 1)
+// NC (NCHW 2D input and output): the producer loads raw [16 channels][HR rows][Wt+16 columns] tiles,
+// four transposer warps (6-9) turn them into the swizzled position rows with ldmatrix.trans /
+// stmatrix (shifting the halo by one column on the way), and the epilogue writes NCHW planes.
+template <bool BF16, bool KWM, bool NC>
+__global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -126,7 +130,9 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
     const uint32_t sStage = sW + (uint32_t)(a.n_w * kWBlock);      // epilogue transpose tile
-    const uint32_t sBar = sStage + 4u * (uint32_t)kStageWarpBytes;
+    const uint32_t sRaw = sStage + 4u * (uint32_t)kStageWarpBytes;           // NCHW raw tiles (128-aligned)
+    const uint32_t sJunk = sRaw + (uint32_t)(a.n_raw * a.raw_bytes);         // NCHW: 16 B per transposer lane
+    const uint32_t sBar = sJunk + (NC ? 4u * 32u * 16u : 0u);
     const uint32_t bar_h_full = sBar;
     const uint32_t bar_h_empty = bar_h_full + 8u * a.n_h;
     const uint32_t bar_w_full = bar_h_empty + 8u * a.n_h;
@@ -134,7 +140,9 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t bar_acc_full = bar_w_empty + 8u * a.n_w;
     const uint32_t bar_acc_empty = bar_acc_full + 16u;
     const uint32_t bar_drain = bar_acc_empty + 16u;
-    const uint32_t s_tmem = bar_drain + 8u;
+    const uint32_t bar_r_full = bar_drain + 8u;
+    const uint32_t bar_r_empty = bar_r_full + 8u * a.n_raw;
+    const uint32_t s_tmem = bar_r_empty + 8u * a.n_raw;
     const uint32_t s_abort = s_tmem + 4u;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + (s_abort - base));
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + (s_tmem - base));
@@ -145,8 +153,12 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.n_h; ++i) {
-            ptx::mbar_init(bar_h_full + 8 * i, 1);
+            ptx::mbar_init(bar_h_full + 8 * i, NC ? 4 : 1);  // NCHW: one arrival per transposer warp
             ptx::mbar_init(bar_h_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < a.n_raw; ++i) {
+            ptx::mbar_init(bar_r_full + 8 * i, 1);
+            ptx::mbar_init(bar_r_empty + 8 * i, 4);
         }
         for (int i = 0; i < a.n_w; ++i) {
             ptx::mbar_init(bar_w_full + 8 * i, 1);
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t h_cnt = 0, w_cnt = 0;
+            uint32_t h_cnt = 0, w_cnt = 0, r_cnt = 0;
             bool ok = true;
             for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
                 const ClTile tc = cl_decode(a, tile);
@@ -195,11 +207,25 @@ __global__ void __launch_bounds__(192, 1)
                         fcoord = n;
                     }
                     for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
-                        const uint32_t sh = h_cnt % a.n_h;
-                        if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
-                        ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
-                        ++h_cnt;
+                        if (NC) {
+                            // raw NCHW slices of 16 channels for the transposers (aligned 8 columns left)
+                            const int nsc = (min(a.C_in - cc * kCK, kCK) + 15) / 16;
+                            for (int sc = 0; sc < nsc; ++sc) {
+                                const uint32_t sr = r_cnt % a.n_raw;
+                                if (!cl_wait(bar_r_empty + 8 * sr, ((r_cnt / a.n_raw) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                                ptx::mbar_arrive_expect_tx(bar_r_full + 8 * sr, (uint32_t)a.raw_tx_bytes);
+                                ptx::tma_load_4d(sRaw + sr * a.raw_bytes, &tm_x, bar_r_full + 8 * sr, ow0 - 8, r0 - 1,
+                                                 cc * kCK + 16 * sc, n);
+                                ++r_cnt;
+                            }
+                            if (!ok) break;
+                        } else {
+                            const uint32_t sh = h_cnt % a.n_h;
+                            if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                            ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
+                            ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
+                            ++h_cnt;
+                        }
                         constexpr int kTaps = KWM ? 3 : 9;
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTaps) * (size_t)kWBlock;
@@ -223,6 +249,10 @@ __global__ void __launch_bounds__(192, 1)
                 for (uint32_t i = 0; i < (uint32_t)a.n_w && i < w_cnt; ++i) {
                     const uint32_t last = i + ((w_cnt - 1 - i) / a.n_w) * a.n_w;
                     cl_wait(bar_w_full + 8 * i, (last / a.n_w) & 1u, &dummy, a.status);
+                }
+                for (uint32_t i = 0; i < (uint32_t)a.n_raw && i < r_cnt; ++i) {
+                    const uint32_t last = i + ((r_cnt - 1 - i) / a.n_raw) * a.n_raw;
+                    cl_wait(bar_r_full + 8 * i, (last / a.n_raw) & 1u, &dummy, a.status);
                 }
             }
         }
@@ -267,6 +297,7 @@ __global__ void __launch_bounds__(192, 1)
                                 const uint32_t b_hi = b_hi_fixed;
 #pragma unroll
                                 for (int ks = 0; ks < kCK / 16; ++ks) {
+                                    if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
                                     const uint64_t adesc = ((uint64_t)a_hi << 32) |
                                                            (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kBM * 16) >> 4));
                                     const uint32_t baddr = row_addr + (uint32_t)ks * 32u;
@@ -292,7 +323,7 @@ __global__ void __launch_bounds__(192, 1)
             cl_wait(bar_drain, 0, &dummy, a.status);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue: TMEM -> channels-last rows
         const int q = warp & 3;            // TMEM lane quarter = output channels 32q .. 32q+31
         const int ew = warp - 2;           // 0..3: this warp's staging block
@@ -369,32 +400,61 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             } else {
-                // Each warp transposes its own 32 channels x 32 positions through a private staging
-                // block (no barrier across warps), then writes 64 contiguous bytes per position row.
-                uint8_t* wst = stage_ptr + ew * kStageWarpBytes;
-                for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
-                    ptx::tmem_ld_wait();
-                    __syncwarp();
-    #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
-                            cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
-                    __syncwarp();
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = k * 8 + (lane >> 2);
-                        const int seg = lane & 3;
-                        const int m = m0 + chunk * 32 + row;
-                        const int oh = m / a.P, c = m % a.P;
-                        const int ow = ow0 + c;
-                        const int co = tc.nt * kBM + q * 32 + seg * 8;
-                        if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
-                            const size_t off =
-                                ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
-                            *reinterpret_cast<uint4*>(y + off) = val;
+                if (NC) {
+                    // NCHW: this warp's 32 channels x 32 positions are transposed through its staging
+                    // block so that each store instruction writes 32 consecutive positions of a channel.
+                    uint16_t* T = reinterpret_cast<uint16_t*>(stage_ptr + ew * kStageWarpBytes);  // [32][34]
+                    const int co_base = tc.nt * kBM + q * 32;
+                    if (co_base < a.C_out) {
+                        for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                            uint32_t v[32];
+                            ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP +
+                                               (uint32_t)(chunk * 32), v);
+                            ptx::tmem_ld_wait();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                T[lane * 34 + j] = cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
+                            __syncwarp();
+                            const int m = m0 + chunk * 32 + lane;
+                            const int oh = m / a.P, c = m % a.P;
+                            const int ow = ow0 + c;
+                            if (c < a.Wt && ow < a.W_out && oh < a.H_out) {
+                                const size_t plane = (size_t)a.H_out * a.W_out;
+                                uint16_t* yp = y + ((size_t)n * a.C_out + co_base) * plane + (size_t)oh * a.W_out + ow;
+                                const int nco = min(32, a.C_out - co_base);
+                                for (int r = 0; r < nco; ++r) yp[(size_t)r * plane] = T[r * 34 + lane];
+                            }
+                        }
+                    }
+                } else {
+                    // Each warp transposes its own 32 channels x 32 positions through a private staging
+                    // block (no barrier across warps), then writes 64 contiguous bytes per position row.
+                    uint8_t* wst = stage_ptr + ew * kStageWarpBytes;
+                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
+                        ptx::tmem_ld_wait();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
+                                cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int row = k * 8 + (lane >> 2);
+                            const int seg = lane & 3;
+                            const int m = m0 + chunk * 32 + row;
+                            const int oh = m / a.P, c = m % a.P;
+                            const int ow = ow0 + c;
+                            const int co = tc.nt * kBM + q * 32 + seg * 8;
+                            if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
+                                const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
+                                const size_t off =
+                                    ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
+                                *reinterpret_cast<uint4*>(y + off) = val;
+                            }
                         }
                     }
                 }
@@ -402,6 +462,61 @@ __global__ void __launch_bounds__(192, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_acc_empty + 8 * ab);
+        }
+    } else if (NC) {
+        // ------------------------------------------------------------ transposers (NCHW -> swizzled rows)
+        const int tw = warp - 6;
+        const int kb_n = a.raw_w / 8;      // 8-column blocks per raw row
+        const uint32_t junk = sJunk + (uint32_t)(tw * 32 + lane) * 16u;
+        uint32_t h_cnt = 0, r_cnt = 0;
+        bool ok = true;
+        for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
+            for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                const uint32_t sh = h_cnt % a.n_h;
+                if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                const uint32_t hst = sH + sh * (uint32_t)a.h_bytes;
+                const int nsc = (min(a.C_in - cc * kCK, kCK) + 15) / 16;
+                for (int sc = 0; sc < nsc; ++sc) {
+                    const uint32_t sr = r_cnt % a.n_raw;
+                    if (!cl_wait(bar_r_full + 8 * sr, (r_cnt / a.n_raw) & 1u, abort_flag, a.status)) { ok = false; break; }
+                    const uint32_t raw = sRaw + sr * (uint32_t)a.raw_bytes;
+                    // rows of 8x8 blocks: item = (8-channel group j, halo row hr); each ldmatrix.x4 /
+                    // stmatrix.x4 pair moves four consecutive 8-column blocks of one item
+                    const int i = lane & 7;
+                    for (int item = tw; item < 2 * a.HR; item += 4) {
+                        const int j = item >= a.HR ? 1 : 0;
+                        const int hr = item - j * a.HR;
+                        const uint32_t src_row = raw + (uint32_t)(((8 * j + i) * a.HR + hr) * a.raw_w) * 2u;
+                        const uint32_t dst_row = hst + (uint32_t)(hr * a.P) * 128u + (uint32_t)(2 * sc + j) * 16u;
+                        for (int kb0 = 0; kb0 < kb_n; kb0 += 4) {
+                            const int kb = kb0 + (lane >> 3);
+                            uint32_t lds_addr = raw, sts_addr = junk;
+                            if (kb < kb_n) {
+                                // source row i: channel 8j+i, raw columns 8kb..8kb+7; destination row i:
+                                // raw column 8kb+i = halo column 8kb+i-7 of row hr, 16-byte chunk 2sc+j of
+                                // the position's 128-byte row, swizzled on the absolute address
+                                lds_addr = src_row + (uint32_t)kb * 16u;
+                                const int col = 8 * kb + i - 7;
+                                if (col >= 0 && col < a.P) {
+                                    const uint32_t addr = dst_row + (uint32_t)col * 128u;
+                                    sts_addr = addr ^ (((addr >> 7) & 7u) << 4);
+                                }
+                            }
+                            uint32_t r0v, r1v, r2v, r3v;
+                            ptx::ldsm_x4_trans(lds_addr, r0v, r1v, r2v, r3v);
+                            ptx::stsm_x4(sts_addr, r0v, r1v, r2v, r3v);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar_r_empty + 8 * sr);
+                    ++r_cnt;
+                }
+                if (!ok) break;
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_h_full + 8 * sh);
+                ++h_cnt;
+            }
         }
     }
 
@@ -440,18 +555,50 @@ x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, u
     return X3_OK;
 }
 
+// Plain (unswizzled) tensor map of an NCHW tensor for the raw 16-channel slices.
+x3_status encode_nchw_raw(CUtensorMap* m, bool bf16, const void* ptr, uint64_t W, uint64_t H, uint64_t C, uint64_t N,
+                          uint32_t box_w, uint32_t box_h) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return fail(X3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+        }
+        fn = (EncodeTiledFn)f;
+    }
+    cuuint64_t gd[4] = {W, H, C, N};
+    cuuint64_t gs[3] = {W * 2, W * H * 2, W * H * C * 2};
+    cuuint32_t bd[4] = {box_w, box_h, 16, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(ptr), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(X3_ERR_CUDA, "cuTensorMapEncodeTiled (NCHW raw) failed (%d)", (int)r);
+    return X3_OK;
+}
+
 }  // namespace
 
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     const x3_conv_desc& d = p->d;
     if (d.stride != 1) return false;
-    if (!(d.dims == 3 ? d.layout == X3_NDHWC : d.layout == X3_NHWC)) return false;
-    if (d.C_in % 8 != 0) return false;
     ClGeom g;
     memset(&g, 0, sizeof g);
+    // NCHW 2D input (raw tiles transposed in shared memory) or channels-last input (swizzled TMA boxes)
+    g.nchw = (d.dims == 2 && d.layout == X3_NCHW) ? 1 : 0;
+    if (g.nchw) {
+        if (d.W % 8 != 0 || d.unpatchify2x2) return false;  // 16-byte aligned rows for the raw TMA boxes
+    } else {
+        if (!(d.dims == 3 ? d.layout == X3_NDHWC : d.layout == X3_NHWC)) return false;
+        if (d.C_in % 8 != 0) return false;
+    }
     // the conv_out head (12 channels to unpatchified RGB) runs in the kw-folded form
     g.kwm = d.unpatchify2x2 ? 1 : 0;
-    if (!g.kwm && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
+    if (!g.kwm && !g.nchw && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
     g.win_adv = g.kwm ? kBNP - 2 : kBNP;
     g.ngroups = g.kwm ? (d.C_out + 9) / 10 : 0;
     if (g.kwm && g.ngroups > 4) return false;
@@ -460,16 +607,16 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     g.n_tiles = (d.C_out + kBM - 1) / kBM;
     g.frames = d.N * (d.dims == 3 ? d.D : 1);
     const int H_out = p->H_out, W_out = p->W_out;
-    const int fixed = 1024 + 4 * kStageWarpBytes + 512;
+    const int fixed = 1024 + 4 * kStageWarpBytes + 512 + (g.nchw ? 4 * 32 * 16 : 0);
     bool found = false;
     long long best_cost = -1;
     int cands[80], nc = 0;
     for (int k = 1; k <= 64; ++k) cands[nc++] = (W_out + k - 1) / k;
     cands[nc++] = 30; cands[nc++] = 62; cands[nc++] = 126; cands[nc++] = 254;  // P divides 256
     for (int ci = 0; ci < nc; ++ci) {
-        const int Wt = cands[ci];
+        const int Wt = g.nchw ? (cands[ci] + 7) / 8 * 8 : cands[ci];  // NCHW: strips start 16-byte aligned
         const int P = Wt + 2;
-        if (P > 256) continue;
+        if (P > 256 || (g.nchw && Wt + 16 > 256)) continue;
         // halo rows of a 256-position window starting anywhere in a row, plus one above and below
         // furthest B row read: window start offset within its row (0 when windows of 256 tile the
         // rows exactly), the window's last column, kh = 2 (+2P) and, unless folded into M, kw = 2 (+2)
@@ -479,7 +626,15 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
         if (HR > 256) continue;
         const int pos = HR * P > need_pos ? HR * P : need_pos;
         const int h_bytes = (pos * 128 + 1023) / 1024 * 1024;
-        int n_w = (kSmemLimit - fixed - 2 * h_bytes) / kWBlock;
+        // NCHW raw slices: 16 channels x HR rows x (Wt + 16) columns, two stages
+        const int raw_w = Wt + 16;
+        const int raw_bytes = g.nchw ? (16 * HR * raw_w * 2 + 127) / 128 * 128 : 0;
+        int n_raw = 0;
+        if (g.nchw) {
+            n_raw = 2;
+            while (n_raw < 4 && fixed + 2 * h_bytes + (n_raw + 1) * raw_bytes + 3 * kWBlock <= kSmemLimit) ++n_raw;
+        }
+        int n_w = (kSmemLimit - fixed - 2 * h_bytes - n_raw * raw_bytes) / kWBlock;
         if (n_w > 6) n_w = 6;
         if (n_w < 3) continue;
         const int strips = (W_out + Wt - 1) / Wt;
@@ -487,13 +642,16 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
         const long long tiles = (long long)strips * windows * g.frames * g.n_tiles;
         const long long waves = (tiles + num_sms - 1) / num_sms;
         // every tile costs the same MMA work: rank by waves, then by weight-ring depth and halo size
-        const long long cost = waves * 100000 + (6 - n_w) * 10000 + (long long)HR * P;
+        const long long cost = waves * 100000 + (6 - n_w) * 10000 + (g.nchw ? (4 - n_raw) * 20000 : 0) +
+                               (long long)HR * P;
         if (!found || cost < best_cost) {
             found = true;
             best_cost = cost;
             g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
             g.n_h = 2; g.n_w = n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
-            g.smem_bytes = fixed + 2 * h_bytes + n_w * kWBlock;
+            g.raw_w = g.nchw ? raw_w : 0; g.raw_bytes = raw_bytes; g.n_raw = n_raw;
+            g.raw_tx_bytes = g.nchw ? 16 * HR * raw_w * 2 : 0;
+            g.smem_bytes = fixed + 2 * h_bytes + n_w * kWBlock + n_raw * raw_bytes;
         }
     }
     if (!found) return false;
@@ -520,25 +678,35 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
     a.win_adv = g.win_adv; a.ngroups = g.ngroups;
+    a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes; a.raw_tx_bytes = g.raw_tx_bytes; a.n_raw = g.n_raw;
     a.idesc = ptx::idesc_f16(kBM, kBNP, bf16);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
     x3_status st0 = device_status_word(&a.status);
     if (st0 != X3_OK) return st0;
     CUtensorMap mx, mc;
-    const uint64_t frames_x = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
-    x3_status st = encode_sw128(&mx, bf16, x, d.C_in, d.W, d.H, frames_x, (uint32_t)g.P, (uint32_t)g.HR);
-    if (st != X3_OK) return st;
-    if (carry) {
-        st = encode_sw128(&mc, bf16, carry, d.C_in, d.W, d.H, (uint64_t)d.N * 2, (uint32_t)g.P, (uint32_t)g.HR);
+    x3_status st;
+    if (g.nchw) {
+        st = encode_nchw_raw(&mx, bf16, x, d.W, d.H, d.C_in, d.N, (uint32_t)g.raw_w, (uint32_t)g.HR);
         if (st != X3_OK) return st;
-    } else {
         mc = mx;
+    } else {
+        const uint64_t frames_x = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
+        st = encode_sw128(&mx, bf16, x, d.C_in, d.W, d.H, frames_x, (uint32_t)g.P, (uint32_t)g.HR);
+        if (st != X3_OK) return st;
+        if (carry) {
+            st = encode_sw128(&mc, bf16, carry, d.C_in, d.W, d.H, (uint64_t)d.N * 2, (uint32_t)g.P, (uint32_t)g.HR);
+            if (st != X3_OK) return st;
+        } else {
+            mc = mx;
+        }
     }
-    auto k = g.kwm ? (bf16 ? igemm_cl_kernel<true, true> : igemm_cl_kernel<false, true>)
-                   : (bf16 ? igemm_cl_kernel<true, false> : igemm_cl_kernel<false, false>);
+    void (*k)(CUtensorMap, CUtensorMap, ClArgs);
+    if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
+    else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false> : igemm_cl_kernel<false, true, false>;
+    else k = bf16 ? igemm_cl_kernel<true, false, false> : igemm_cl_kernel<false, false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
-    k<<<g.grid, 192, g.smem_bytes, s>>>(mx, mc, a);
+    k<<<g.grid, g.nchw ? 320 : 192, g.smem_bytes, s>>>(mx, mc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl launch: %s", cudaGetErrorString(e));
     return X3_OK;

@@ -64,6 +64,8 @@ struct ClGeom {
     int h_bytes, h_tx_bytes;     // bytes of one halo stage (1024-aligned) / written by its TMA box
     int n_h, n_w;                // halo stages, weight-block stages
     int kwm;                     // 1: kw folded into M (the conv_out head form, unpatchify epilogue)
+    int nchw;                    // 1: NCHW 2D input/output (raw slices transposed in shared memory)
+    int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW raw-slice staging
     int win_adv;                 // raster positions between consecutive windows (256, or 254 when kwm)
     int ngroups;                 // kwm: groups of 10 output channels (one TMEM lane quarter each)
     long long tiles;
