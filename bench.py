@@ -38,6 +38,7 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
             "(256->12 @4+2x352x624, clamp, 2x2 unpatchify)")
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
+TRAFFIC_DOMINANT_BYTES = 876.3e6
 
 
 def flop2d(N, Ci, Co, Ho, Wo):
@@ -392,7 +393,9 @@ def main():
     achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
+                # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, from the ncu
+                # capture summarised in profiles/igemm_cl_causal128_4x352x624.md (algorithmic: 563.2 MB)
+                "traffic": TRAFFIC_DOMINANT_BYTES, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms}
     stages = {}
     for k in STAGES:
