@@ -239,13 +239,8 @@ def dist_setup():
 
 
 def reduce_max(world, value):
-    if world == 1:
-        return value
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from x3x3_convolution_gb300 import dist as xd
+    return xd.max_over_ranks(value) if world > 1 else value
 
 
 def barrier(world):
@@ -321,7 +316,14 @@ def main():
         __graft_entry__.build()
     barrier(world)
     import x3x3_convolution_gb300 as x3
-    x3.load()
+    from x3x3_convolution_gb300 import dist as xd
+    try:
+        x3.load()
+        loaded = True
+    except Exception:
+        loaded = False
+    if not (xd.agree_all(loaded) if world > 1 else loaded):  # every rank runs the kernels, or none does
+        raise RuntimeError("the CUDA library did not load on every rank")
 
     dev = f"cuda:{local}"
     wl = Workload(dev, seed_base=rank)

@@ -201,6 +201,16 @@ x3_status conv_stack_forward_noalloc(const x3_conv_plan* const* plans, int n_lay
  */
 x3_status conv_device_status(int reset);
 
+/*
+ * Self-test of the bounded-wait path: launches one small kernel whose single thread waits on a
+ * shared-memory mbarrier that nothing ever arrives at, with a limit of `limit_ms` milliseconds
+ * (1..2000), using the same bounded wait as the convolution kernels. When the limit runs out the
+ * kernel records X3_ERR_TIMEOUT in the device status word and returns; conv_device_status then
+ * reports it and the context stays usable. Errors: X3_ERR_INVALID (limit out of range),
+ * X3_ERR_CUDA (launch failure).
+ */
+x3_status conv_selftest_wait_timeout(int limit_ms, x3_stream_t stream);
+
 /* Thread-local description of the last error returned on this thread ("" if none). */
 const char* conv_last_error(void);
 

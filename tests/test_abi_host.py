@@ -43,6 +43,11 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
+def test_selftest_limits_validated_on_host(lib):
+    for bad in (0, -5, 2001):
+        assert lib.conv_selftest_wait_timeout(bad, None) == x3.X3_ERR_INVALID
+
+
 def test_version(lib):
     assert "sm_103a" in x3.conv_version()
 

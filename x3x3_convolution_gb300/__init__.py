@@ -66,6 +66,7 @@ def load():
         "conv_stack_workspace_bytes": ([pp, i], sz),
         "conv_stack_forward": ([pp, i, vp, pp, i, pp, pp, vp, vp, sz, vp], i),
         "conv_device_status": ([i], i),
+        "conv_selftest_wait_timeout": ([i, vp], i),
         "conv_last_error": ([], ctypes.c_char_p),
         "conv_version": ([], ctypes.c_char_p),
     }
@@ -144,6 +145,10 @@ def conv_stack_forward(plans, x: int, carries, carry_valid: int, w_packed, bias,
 
 def conv_device_status(reset: int = 0) -> int:
     return load().conv_device_status(reset)
+
+
+def conv_selftest_wait_timeout(limit_ms: int, stream: int = 0) -> None:
+    _check(load().conv_selftest_wait_timeout(int(limit_ms), stream))
 
 
 def conv_last_error() -> str:

@@ -304,6 +304,11 @@ x3_status conv_device_status(int reset) {
     return read_device_status(reset);
 }
 
+x3_status conv_selftest_wait_timeout(int limit_ms, x3_stream_t stream) {
+    clear_err();
+    return selftest_wait_timeout(limit_ms, (cudaStream_t)stream);
+}
+
 const char* conv_last_error(void) { return g_err; }
 
 const char* conv_version(void) { return "x3conv 0.1 (sm_103a)"; }

@@ -807,6 +807,25 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     return bf16 ? launch_t<STAGE_NCHW, true>(mx, mc, a, g, s) : launch_t<STAGE_NCHW, false>(mx, mc, a, g, s);
 }
 
+// One thread waits, bounded, on an mbarrier nobody arrives at; the wait runs out after limit_ns and
+// the status word records the timeout, exactly as in the convolution kernels.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = ptx::smem_u32(&bar);
+    ptx::mbar_init(b, 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(b, 0)) {
+        if (ptx::globaltimer() - t0 > limit_ns) {
+            atomicOr(&g_x3_status, 1u);
+            break;
+        }
+    }
+}
+
 // Device address of the status word on the current device, for kernels compiled in other files.
 x3_status device_status_word(unsigned int** out) {
     static unsigned int* ptrs[64];
@@ -820,6 +839,14 @@ x3_status device_status_word(unsigned int** out) {
         ptrs[dev] = (unsigned int*)p;
     }
     *out = ptrs[dev];
+    return X3_OK;
+}
+
+x3_status selftest_wait_timeout(int limit_ms, cudaStream_t s) {
+    if (limit_ms < 1 || limit_ms > 2000) return fail(X3_ERR_INVALID, "limit_ms must be in 1..2000");
+    selftest_wait_kernel<<<1, 32, 0, s>>>((uint64_t)limit_ms * 1000000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
     return X3_OK;
 }
 

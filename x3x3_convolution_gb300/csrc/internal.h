@@ -107,6 +107,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms);  // fills p->cl (+ packing fie
 x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                           const void* bias, void* y, cudaStream_t s);
 x3_status read_device_status(int reset);
+x3_status selftest_wait_timeout(int limit_ms, cudaStream_t s);
 x3_status device_status_word(unsigned int** out);  // device address of the timeout status word
 
 }  // namespace x3
