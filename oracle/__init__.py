@@ -66,6 +66,8 @@ def configure(lib):
     lib.oracle_unpatchify2x2.restype = None
     lib.oracle_max_threads.argtypes = [ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_head_two_pass.argtypes = [f32p, f32p, f32p, f32p, f32p] + [ctypes.c_int] * 7
+    lib.oracle_head_two_pass.restype = ctypes.c_int
     return lib
 
 
@@ -147,6 +149,31 @@ def conv3d_causal(x, w, b=None, carry=None, act: str = "none", layout: str = "NC
                                       C_out, D, H, W, ACT[act], int(threads))
     if rc != 0:
         raise ValueError("oracle_conv3d_causal: bad arguments")
+    return y.transpose(0, 2, 3, 4, 1).copy() if layout == "NDHWC" else y
+
+
+def head_two_pass(x, w, b=None, carry=None, round_g: bool = True, layout: str = "NCDHW", threads: int = 0):
+    """The conv_out head (256->12 causal 3x3x3, clamp) computed as the head.cu page's two passes:
+    a temporal-only convolution into a 108-channel plane g (rounded to bf16 when round_g), then the
+    nine spatial taps summed in fp32 from g plus the bias, then the clamp. Returns fp32 (unrounded)
+    [N,12,D,H,W] in ``layout`` (the caller rounds once to the storage type)."""
+    x = np.asarray(x)
+    if layout == "NDHWC":
+        x = x.transpose(0, 4, 1, 2, 3)
+        if carry is not None:
+            carry = np.asarray(carry).transpose(0, 4, 1, 2, 3)
+    x = _f32(x)
+    w = _f32(w)
+    N, C_in, D, H, W = x.shape
+    if w.shape != (12, C_in, 3, 3, 3):
+        raise ValueError(f"weight shape {w.shape}")
+    cc = None if carry is None else _f32(carry)
+    bb = None if b is None else _f32(b)
+    y = np.empty((N, 12, D, H, W), np.float32)
+    rc = _load().oracle_head_two_pass(_ptr(x), _ptr(cc), _ptr(w), _ptr(bb), _ptr(y), N, C_in, D, H, W,
+                                      int(bool(round_g)), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_head_two_pass: bad arguments")
     return y.transpose(0, 2, 3, 4, 1).copy() if layout == "NDHWC" else y
 
 

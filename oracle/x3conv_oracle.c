@@ -30,6 +30,7 @@
  * zero padding conv3d applies in the plane); the 12 head channels map to RGB by c = rgb*4+dy*2+dx.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -234,4 +235,73 @@ void oracle_unpatchify2x2(const float* y12, float* rgb, int N, int D, int H, int
                             for (int w = 0; w < W; ++w)
                                 rgb[((((size_t)n * 3 + c) * D + t) * (2 * H) + 2 * h + dy) * (2 * (size_t)W) + 2 * w + dx] =
                                     y12[((((size_t)n * 12 + c * 4 + dy * 2 + dx) * D + t) * H + h) * W + w];
+}
+
+/* ---------------------------------------------------------------- two-pass head (the page's split) */
+
+/*
+ * The conv_out head computed in two passes, following the value path the FastVideo
+ * wan22_vae_decode/solution/head.cu header comment describes:
+ *   pass 1, temporal-only 3x1x1 convolution into the plane g with 9*12 channels:
+ *     g[n,t,h,w,(i*3+j)*12+c] = R16( sum_{ci,kt} w[c,ci,kt,i,j] * xt[n,ci,t+kt,h,w] )
+ *     (one fp32 accumulator over the 3 temporal taps and all input channels, then one rounding to
+ *     bf16 when round_g != 0; kept in fp32 when round_g == 0);
+ *   pass 2, the nine spatial taps, as head_stencil_kernel sums them: an fp32 accumulator starting at
+ *   the bias, adding g of the neighbour (h+i-1, w+j-1) for i, j = 0..2 in that order, skipping
+ *   neighbours outside the plane (the zero padding), then clamp to [-1,1] (the caller rounds once).
+ * x: [N][C_in][D][H][W]; carry: [N][C_in][2][H][W] or NULL; w: [12][C_in][3][3][3]; b: [12] or NULL;
+ * y: [N][12][D][H][W]. Returns 0, or -1 on a bad argument.
+ */
+int oracle_head_two_pass(const float* x, const float* carry, const float* w, const float* b, float* y,
+                         int N, int C_in, int D, int H, int W, int round_g, int nthreads)
+{
+    if (N < 0 || C_in <= 0 || D <= 0 || H <= 0 || W <= 0) return -1;
+    const size_t plane = (size_t)H * W;
+    const size_t gsize = (size_t)N * D * plane * 108;
+    float* g = (float*)malloc(gsize * sizeof(float));
+    if (!g) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int n = 0; n < N; ++n)
+        for (int t = 0; t < D; ++t)
+            for (int h = 0; h < H; ++h)
+                for (int wo = 0; wo < W; ++wo)
+                    for (int k = 0; k < 108; ++k) {
+                        const int i = k / 36, j = (k / 12) % 3, c = k % 12;
+                        float acc = 0.0f;
+                        for (int ci = 0; ci < C_in; ++ci)
+                            for (int kt = 0; kt < 3; ++kt) {
+                                const int f = t + kt;
+                                float v;
+                                if (f < 2) {
+                                    if (!carry) continue;
+                                    v = carry[(((size_t)n * C_in + ci) * 2 + f) * plane + (size_t)h * W + wo];
+                                } else {
+                                    v = x[(((size_t)n * C_in + ci) * D + (f - 2)) * plane + (size_t)h * W + wo];
+                                }
+                                acc += w[((((size_t)c * C_in + ci) * 3 + kt) * 3 + i) * 3 + j] * v;
+                            }
+                        if (round_g) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));
+                        g[((((size_t)n * D + t) * H + h) * W + wo) * 108 + k] = acc;
+                    }
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int n = 0; n < N; ++n)
+        for (int c = 0; c < 12; ++c)
+            for (int t = 0; t < D; ++t)
+                for (int h = 0; h < H; ++h)
+                    for (int wo = 0; wo < W; ++wo) {
+                        float acc = b ? b[c] : 0.0f;
+                        for (int i = 0; i < 3; ++i) {
+                            const int hh = h + i - 1;
+                            if (hh < 0 || hh >= H) continue;
+                            for (int j = 0; j < 3; ++j) {
+                                const int ww = wo + j - 1;
+                                if (ww < 0 || ww >= W) continue;
+                                acc += g[((((size_t)n * D + t) * H + hh) * W + ww) * 108 + (i * 3 + j) * 12 + c];
+                            }
+                        }
+                        y[((((size_t)n * 12 + c) * D + t) * H + h) * W + wo] = apply_act(acc, ORACLE_ACT_CLAMP1);
+                    }
+    free(g);
+    return 0;
 }

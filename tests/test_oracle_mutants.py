@@ -31,6 +31,9 @@ MUTANTS = {
     "bf16_truncates": ("if (rem > 0x8000u || (rem == 0x8000u && (keep & 1u))) keep += 1u;", ""),
     "unpatchify_dy_dx_swapped": ("c * 4 + dy * 2 + dx", "c * 4 + dx * 2 + dy"),
     "stride_ignored_rows": ("const int ih = stride * oh + kh - 1;", "const int ih = oh + kh - 1;"),
+    "two_pass_g_not_rounded": ("if (round_g) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));", ""),
+    "two_pass_tap_transposed": ("(i * 3 + j) * 12 + c];", "(j * 3 + i) * 12 + c];"),
+    "two_pass_bias_dropped": ("float acc = b ? b[c] : 0.0f;", "float acc = 0.0f;"),
 }
 
 
@@ -47,6 +50,9 @@ def _pins():
         ("identity", P.test_identity_and_delta_kernels),
         ("unpatchify", P.test_unpatchify_is_a_bijection),
         ("act_rounding", P.test_act_commutes_with_rounding),
+        ("head_split", P.test_head_split_identity),
+        ("head_exact", P.test_head_two_pass_exact_when_g_is_representable),
+        ("head_rounds_g", P.test_head_two_pass_rounds_g_before_the_spatial_sum),
     ]
     for case in P._golden_cases():
         pins.append((case["name"], lambda m, c=case: P.test_hand_worked_values(m, c)))

@@ -353,3 +353,46 @@ def test_act_commutes_with_rounding(oracle_mod):
         assert np.array_equal(np.maximum(r, 0), a)
         a, _ = oracle_mod.round_to(np.clip(v, -1, 1), dt)
         assert np.array_equal(np.clip(r, -1, 1), a)
+
+
+# ------------------------------------------------------------------ two-pass head (the page's split)
+
+def test_head_split_identity(oracle_mod):
+    """Without the early rounding, the temporal pass plus the nine shifted spatial sums equal the
+    direct 27-tap convolution (within the fp32 summation bound, against float64 brute force)."""
+    rng = np.random.default_rng(21)
+    x = rng.normal(0, 1, (1, 5, 3, 4, 6)).astype(np.float32)
+    c = rng.normal(0, 1, (1, 5, 2, 4, 6)).astype(np.float32)
+    w = rng.normal(0, 0.2, (12, 5, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-0.05, 0.05, 12).astype(np.float32)
+    y2 = oracle_mod.head_two_pass(x, w, b, carry=c, round_g=False)
+    ref, absref = brute_conv3d_f64(x.astype(np.float64), w.astype(np.float64), b.astype(np.float64),
+                                   c.astype(np.float64), "clamp")
+    assert within_fp32_sum_bound(y2, ref, absref, 27 * 5 + 10)
+
+
+def test_head_two_pass_exact_when_g_is_representable(oracle_mod):
+    """Integer data whose temporal partial sums fit bf16's 8-bit significand: the early rounding is
+    exact and both forms give the same values."""
+    rng = np.random.default_rng(22)
+    x = rng.integers(-1, 2, (1, 6, 2, 5, 7)).astype(np.float32)
+    c = rng.integers(-1, 2, (1, 6, 2, 5, 7)).astype(np.float32)
+    w = rng.choice([-1.0, 0.0, 1.0], size=(12, 6, 3, 3, 3), p=[0.1, 0.8, 0.1]).astype(np.float32)
+    y2 = oracle_mod.head_two_pass(x, w, np.zeros(12, np.float32), carry=c)
+    y1 = oracle_mod.conv3d_causal(x, w, np.zeros(12, np.float32), carry=c, act="clamp")
+    assert np.array_equal(y2, y1)
+
+
+def test_head_two_pass_rounds_g_before_the_spatial_sum(oracle_mod):
+    """Hand-worked: one pixel, one channel path; the temporal sum g = 257 is not a bf16 value and
+    rounds to 256 (ties to even), so with bias -256.5 the output is clamp(-0.5) = -0.5, where the
+    one-accumulator form gives clamp(0.5) = 0.5."""
+    x = np.zeros((1, 1, 1, 1, 1), np.float32)
+    x[0, 0, 0, 0, 0] = 257.0
+    w = np.zeros((12, 1, 3, 3, 3), np.float32)
+    w[0, 0, 2, 1, 1] = 1.0          # output channel 0, current frame, centre tap
+    b = np.zeros(12, np.float32)
+    b[0] = -256.5
+    assert oracle_mod.head_two_pass(x, w, b)[0, 0, 0, 0, 0] == -0.5
+    assert oracle_mod.head_two_pass(x, w, b, round_g=False)[0, 0, 0, 0, 0] == 0.5
+    assert oracle_mod.conv3d_causal(x, w, b, act="clamp")[0, 0, 0, 0, 0] == 0.5
