@@ -38,6 +38,7 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
             "(256->12 @4+2x352x624, clamp, 2x2 unpatchify)")
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
+AB_STAGES = ["head_two_pass"]
 TRAFFIC_DOMINANT_BYTES = 876.3e6
 
 
@@ -164,6 +165,10 @@ class Workload:
         self.head_x = hx.torch(dev)
         self.head_c = hc.torch(dev)
         self.head_y = torch.empty(self.head.out_shape(), dtype=torch.bfloat16, device=dev)
+        # A/B variant of the head, not part of the step: the two-pass (temporal, then spatial) form
+        self.head2 = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, D=FRAMES, act="clamp", unpatchify2x2=True,
+                                          kernel="head_two_pass"), HL.w.torch(dev), HL.b.torch(dev))
+        self.head2_y = torch.empty(self.head2.out_shape(), dtype=torch.bfloat16, device=dev)
         self.kernels_per_step = len(convs) + len(sc) + 2
         self.plans = {"taesd": [x3.conv_plan_describe(c.plan) for c in convs],
                       "stack": x3.conv_plan_describe(sc[0].plan),
@@ -273,7 +278,8 @@ def run_stage(wl, args, stream, fl, nb):
           "stack": lambda: wl.stack(wl.stack_x, carries=wl.stack_carries, carry_valid=True, out=wl.stack_y,
                                     stream=stream),
           "l3": lambda: wl.l3(wl.l3_x, wl.l3_c, out=wl.l3_y, stream=stream),
-          "head": lambda: wl.head(wl.head_x, wl.head_c, out=wl.head_y, stream=stream)}[args.stage]
+          "head": lambda: wl.head(wl.head_x, wl.head_c, out=wl.head_y, stream=stream),
+          "head_two_pass": lambda: wl.head2(wl.head_x, wl.head_c, out=wl.head2_y, stream=stream)}[args.stage]
     for _ in range(args.warmup):
         fn()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -285,8 +291,30 @@ def run_stage(wl, args, stream, fl, nb):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    print(json.dumps({"stage": args.stage, "ms": ms, "tflops": fl[args.stage] / (ms * 1e-3) / 1e12,
-                      "gbs": nb[args.stage] / (ms * 1e-3) / 1e9, "plan": wl.plans[args.stage]}), flush=True)
+    key = "head" if args.stage == "head_two_pass" else args.stage
+    print(json.dumps({"stage": args.stage, "ms": ms, "tflops": fl[key] / (ms * 1e-3) / 1e12,
+                      "gbs": nb[key] / (ms * 1e-3) / 1e9, "plan": wl.plans[key]}), flush=True)
+
+
+def head_ab(wl, stream, reps=10):
+    """The fused head and its two-pass variant, each timed alone (CUDA events, after warm-up), and
+    the largest difference between their outputs."""
+    import torch
+    out = {}
+    for name, conv, y in (("fused", wl.head, wl.head_y), ("two_pass", wl.head2, wl.head2_y)):
+        for _ in range(3):
+            conv(wl.head_x, wl.head_c, out=y, stream=stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            conv(wl.head_x, wl.head_c, out=y, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name + "_ms"] = e0.elapsed_time(e1) / reps
+    out["max_abs_diff"] = float((wl.head_y.float() - wl.head2_y.float()).abs().max())
+    return out
 
 
 def main():
@@ -297,7 +325,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--stage", choices=STAGES, default=None,
+    ap.add_argument("--stage", choices=STAGES + AB_STAGES, default=None,
                     help="run only this stage per step (for profiler captures); prints its per-launch time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -388,6 +416,7 @@ def main():
         e2e = {"value": world * total_flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
 
+    ab = head_ab(wl, stream)
     peaks = load_peaks()
     # dominant kernel: the causal 128->128 tcgen05 implicit GEMM, launched twice per step by the stack
     # stage; its per-launch time is the stage time over 2 (which also carries the two 2-frame carry copies)
@@ -415,7 +444,7 @@ def main():
                    "frames_per_pass": FRAMES},
         "decoder_ms_per_frame": (stage_ms["stack"] + stage_ms["l3"] + stage_ms["head"]) / FRAMES,
         "stages": stages, "roofline": roofline, "gpu_launches": wl.kernels_per_step * args.steps,
-        "clocks": clk, "e2e": e2e,
+        "clocks": clk, "e2e": e2e, "head_variants": ab,
         "plans": {k: (v if k != "taesd" else [p.get("kernel") for p in v]) for k, v in wl.plans.items()},
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -66,7 +66,12 @@ typedef enum { X3_ACT_NONE = 0, X3_ACT_RELU = 1, X3_ACT_CLAMP1 = 2 } x3_act;
 typedef enum {
     X3_KERNEL_AUTO = 0,   /* pick the fastest kernel that handles the descriptor */
     X3_KERNEL_IGEMM = 1,  /* tcgen05/TMEM implicit GEMM (fails with X3_ERR_UNSUPPORTED if it can't) */
-    X3_KERNEL_DIRECT = 2  /* plain SIMT direct convolution; handles every valid descriptor */
+    X3_KERNEL_DIRECT = 2, /* plain SIMT direct convolution; handles every valid descriptor */
+    X3_KERNEL_HEAD_TWO_PASS = 3 /* conv_out head as two passes (run with conv_head_two_pass): a temporal-
+                                   only 3x1x1 convolution into a 112-channel bf16 plane g, then the nine
+                                   spatial taps with bias and clamp (FastVideo wan22_vae_decode/solution/
+                                   head.cu, header comment and head_stencil_kernel); needs
+                                   unpatchify2x2, 3D, X3_NDHWC, bf16 */
 } x3_kernel;
 
 /* Descriptor of one convolution layer. */
@@ -138,6 +143,23 @@ x3_status conv_pack_weights(const x3_conv_plan* plan, const void* w, void* w_pac
  */
 x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carry,
                        const void* w_packed, const void* bias, void* y, x3_stream_t stream);
+
+/*
+ * The conv_out head computed as the head.cu page's two passes, for a plan made with
+ * kernel = X3_KERNEL_HEAD_TWO_PASS (weights packed by conv_pack_weights with that plan):
+ *   pass 1: g[n,t,h,w,(i*3+j)*12+c] = bf16( sum_{ci,kt} w[c,ci,kt,i,j] * xt[n,ci,t+kt,h,w] ), channels
+ *           108..111 zero: a temporal-only convolution on the tensor cores, one fp32 accumulator per
+ *           value, rounded once into the plane;
+ *   pass 2: y = bf16( clamp( b[c] + sum_{i,j} g[n,t,h+i-1,w+j-1,(i*3+j)*12+c] ) ) with the zero padding,
+ *           written as unpatchified RGB like conv_forward's head output.
+ * The early bf16 rounding of g is the page's value path; it differs from conv_forward's single
+ * accumulator over all 27 taps by a few bf16 ulps of the partial sums (max|d| moves, rms does not).
+ *   g: caller buffer of conv_head_g_bytes(plan) bytes, 16-byte aligned ([N][D][H][W][112] bf16).
+ * Errors: X3_ERR_INVALID (wrong plan kind, NULL or misaligned pointers), X3_ERR_CUDA.
+ */
+size_t conv_head_g_bytes(const x3_conv_plan* plan);
+x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void* carry, const void* w_packed,
+                             const void* bias, void* g, void* y, x3_stream_t stream);
 
 /*
  * Workspace bytes conv_stack_forward needs for these layers: two ping-pong buffers, each the size

@@ -137,6 +137,8 @@ WORKLOADS = {
     "ragged_3d": dict(dims=3, N=2, C_in=40, C_out=72, D=3, H=7, W=301),
     "ragged_3d_wide": dict(dims=3, N=2, C_in=40, C_out=136, D=3, H=7, W=301),
     "nhwc_2d_256": dict(dims=2, N=3, C_in=64, C_out=256, H=33, W=97, layout="NHWC"),
+    "head_two_pass_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True,
+                                  kernel="head_two_pass"),
 }
 
 
@@ -164,7 +166,7 @@ def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
-        if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head"):
+        if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head", "head_two_pass"):
             _check_sw128_plan(g)
             return
         assert g["kernel"] == "igemm_tcgen05"
@@ -188,3 +190,32 @@ def test_igemm_plans_cover_their_reads(lib, name):
         assert g["col_tiles"] * Wt >= g["W_out"] and g["row_tiles"] * Rt >= g["H_out"]
     finally:
         x3.conv_plan_destroy(p)
+
+
+def test_head_two_pass_plan(lib):
+    """The two-pass head is only offered for the conv_out head's shape, and its plan runs only
+    through conv_head_two_pass, with a caller-provided 112-channel bf16 g plane."""
+    good = dict(dims=3, N=2, C_in=256, C_out=12, D=3, H=20, W=30, unpatchify2x2=True, kernel="head_two_pass")
+    p = x3.conv_plan_create(x3.make_desc(**good))
+    try:
+        assert x3.conv_plan_kernel_name(p) == "head_two_pass"
+        assert x3.conv_head_g_bytes(p) == 2 * 3 * 20 * 30 * 112 * 2
+        assert x3.conv_packed_weight_bytes(p) == 3 * 4 * 128 * 64 * 2   # [kt][chunk] A tiles, centre tap only
+        g = x3.conv_plan_describe(p)
+        assert g["win_adv"] == 256 and not g["kwm"] and g["n_tiles"] == 1
+        st = lib.conv_forward(p, 16, None, 256, 32, 1 << 40, None)
+        assert st == x3.X3_ERR_INVALID and "conv_head_two_pass" in x3.conv_last_error()
+        assert lib.conv_head_two_pass(p, 16, None, 256, None, 1 << 40, 1 << 41, None) == x3.X3_ERR_INVALID  # bias
+        assert lib.conv_head_two_pass(p, 16, None, 256, 32, (1 << 40) + 4, 1 << 41, None) == x3.X3_ERR_INVALID   # g align
+    finally:
+        x3.conv_plan_destroy(p)
+    q = x3.conv_plan_create(x3.make_desc(3, 1, 64, 64, 8, 8, D=2))
+    try:
+        assert x3.conv_head_g_bytes(q) == 0
+        assert lib.conv_head_two_pass(q, 16, None, 256, 32, 4096, 8192, None) == x3.X3_ERR_INVALID
+    finally:
+        x3.conv_plan_destroy(q)
+    for bad in (dict(unpatchify2x2=False), dict(layout="NCDHW"), dict(dtype="f16")):
+        with pytest.raises(x3.X3Error) as e:
+            x3.conv_plan_create(x3.make_desc(**{**good, **bad}))
+        assert e.value.status == x3.X3_ERR_UNSUPPORTED

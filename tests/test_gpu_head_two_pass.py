@@ -1,0 +1,89 @@
+"""GPU parity of the two-pass conv_out head (the head.cu page's temporal-then-spatial split).
+
+Pass 1 is the swapped tcgen05 engine in its centre-tap form writing the 108 (112) channel bf16
+plane g; pass 2 is the stencil kernel (nine spatial taps in fp32, bias, clamp, one rounding,
+2x2 unpatchify). Both are compared with the oracle's two-pass restatement (g rounded to bf16):
+exactly on sparse {-1,0,1} data, where every g value and sum is representable; within the
+random-data tolerance otherwise. Against the exact single-pass head the rounding of g costs
+accuracy, so that comparison is by PSNR over the [-1,1] range.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import x3x3_convolution_gb300 as x3
+from x3x3_convolution_gb300 import synth
+from tests.gpu_helpers import (PSNR_MIN, assert_close, assert_exact, crops_3d, dev, host_values, psnr,
+                               sample_positions)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    x3.load()
+    yield
+    assert x3.conv_device_status(1) == x3.X3_OK
+
+
+def run_two_pass(x, carry, L):
+    N, D, H, W, C = x.shape
+    d = x3.make_desc(3, N, C, 12, H, W, D=D, layout="NDHWC", dtype="bf16", act="clamp", unpatchify2x2=True,
+                     kernel="head_two_pass")
+    conv = x3.Conv(d, dev(L.w), dev(L.b))
+    assert conv.kernel_name == "head_two_pass"
+    y = conv(dev(x), None if carry is None else dev(carry))
+    torch.cuda.synchronize()
+    return host_values(y, "bf16"), conv
+
+
+def to_rgb(y12_ndhwc):
+    """[N, D, H, W, 12] -> [N, D, 2H, 2W, 3] by the oracle's unpatchify."""
+    return oracle.unpatchify2x2(y12_ndhwc.transpose(0, 4, 1, 2, 3)).transpose(0, 2, 3, 4, 1)
+
+
+SHAPES = [(2, 9, 140), (3, 5, 300), (1, 17, 33), (4, 1, 7), (2, 12, 254)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=str)
+@pytest.mark.parametrize("variant", ["sparse1", "random"])
+def test_two_pass_head(variant, shape):
+    D, H, W = shape
+    x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3600 + H + W)
+    got, _ = run_two_pass(x, carry, L)
+    ref = to_rgb(oracle.head_two_pass(x.vals, L.w.vals, L.b.vals, carry=carry.vals, layout="NDHWC"))
+    assert got.shape == ref.shape == (1, D, 2 * H, 2 * W, 3)
+    if variant == "sparse1":
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+        exact = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp",
+                                            layout="NDHWC"))
+        assert psnr(got, exact) >= PSNR_MIN
+
+
+def test_two_pass_head_without_carry_and_batch():
+    x, _, L = synth.head(D=2, H=6, W=70, variant="random", seed=3690)
+    xs = np.concatenate([x.vals, x.vals[:, ::-1]], axis=0)          # N = 2, second sequence reversed
+    xt = synth.Tensor(*synth.to_storage(xs, "bf16"), "bf16")
+    got, _ = run_two_pass(xt, None, L)
+    ref = to_rgb(oracle.head_two_pass(xt.vals, L.w.vals, L.b.vals, layout="NDHWC"))
+    assert_close(got, ref)
+
+
+def test_two_pass_head_full_size_sampled():
+    """4 x 352 x 624 latent frames, 256 channels: outputs at sampled positions, each from the
+    oracle's two-pass head run on that position's own 3x3x3 window."""
+    x, carry, L = synth.head(seed=3950)
+    got, _ = run_two_pass(x, carry, L)
+    assert got.shape == (1, 4, 704, 1248, 3)
+    seq = np.concatenate([carry.vals, x.vals], axis=1)
+    pos = sample_positions(4, 352, 624, 300, seed=77)
+    cr = crops_3d(seq, pos)
+    y = oracle.head_two_pass(cr[:, 2:3], L.w.vals, L.b.vals, carry=cr[:, 0:2], layout="NDHWC")[:, 0, 1, 1, :]
+    ref = to_rgb(y[:, None, None, None, :])[:, 0]                   # [n, 2, 2, 3]
+    g = np.stack([got[0, t, 2 * h:2 * h + 2, 2 * w:2 * w + 2] for (t, h, w) in pos])
+    assert_close(g, ref)

@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "X3_OK", 1: "X3_ERR_INVALID", 2: "X3_ERR_UNSUPPORTED", 3: "X3
 LAYOUT = {"NCHW": 0, "NHWC": 1, "NCDHW": 2, "NDHWC": 3}
 DTYPE = {"f16": 0, "bf16": 1}
 ACT = {"none": 0, "relu": 1, "clamp": 2}
-KERNEL = {"auto": 0, "igemm": 1, "direct": 2}
+KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3}
 
 
 class ConvDesc(ctypes.Structure):
@@ -66,6 +66,8 @@ def load():
         "conv_stack_workspace_bytes": ([pp, i], sz),
         "conv_stack_forward": ([pp, i, vp, pp, i, pp, pp, vp, vp, sz, vp], i),
         "conv_device_status": ([i], i),
+        "conv_head_g_bytes": ([vp], sz),
+        "conv_head_two_pass": ([vp, vp, vp, vp, vp, vp, vp, vp], i),
         "conv_selftest_wait_timeout": ([i, vp], i),
         "conv_last_error": ([], ctypes.c_char_p),
         "conv_version": ([], ctypes.c_char_p),
@@ -141,6 +143,14 @@ def conv_stack_forward(plans, x: int, carries, carry_valid: int, w_packed, bias,
     b, k4 = _ptrs(bias)
     _check(load().conv_stack_forward(p, len(plans), x, c, int(carry_valid), w, b, y, workspace or None,
                                      workspace_bytes, stream))
+
+
+def conv_head_g_bytes(plan: int) -> int:
+    return load().conv_head_g_bytes(plan)
+
+
+def conv_head_two_pass(plan: int, x: int, carry, w_packed: int, bias, g: int, y: int, stream: int = 0) -> None:
+    _check(load().conv_head_two_pass(plan, x, carry or None, w_packed, bias or None, g, y, stream))
 
 
 def conv_device_status(reset: int = 0) -> int:
@@ -228,6 +238,14 @@ class Conv:
         torch = _torch()
         if out is None:
             out = torch.empty(self.out_shape(), dtype=x.dtype, device=x.device)
+        if self.kernel_name == "head_two_pass":
+            gb = conv_head_g_bytes(self.plan)
+            if getattr(self, "_g", None) is None or self._g.numel() * 2 < gb:
+                self._g = torch.empty(gb // 2, dtype=torch.int16, device=x.device)
+            conv_head_two_pass(self.plan, x.data_ptr(), None if carry is None else carry.data_ptr(), self._wp,
+                               None if self.bias is None else self.bias.data_ptr(), self._g.data_ptr(),
+                               out.data_ptr(), _stream(stream))
+            return out
         conv_forward(self.plan, x.data_ptr(), None if carry is None else carry.data_ptr(), self._wp,
                      None if self.bias is None else self.bias.data_ptr(), out.data_ptr(), _stream(stream))
         return out

@@ -62,7 +62,7 @@ static x3_status validate(const x3_conv_desc* d) {
     if (d->has_bias != 0 && d->has_bias != 1) return fail(X3_ERR_INVALID, "has_bias must be 0 or 1");
     if (d->unpatchify2x2 != 0 && d->unpatchify2x2 != 1) return fail(X3_ERR_INVALID, "unpatchify2x2 must be 0 or 1");
     if (d->unpatchify2x2 && d->C_out != 12) return fail(X3_ERR_INVALID, "unpatchify2x2 needs C_out == 12");
-    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_DIRECT) return fail(X3_ERR_INVALID, "bad kernel choice");
+    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_TWO_PASS) return fail(X3_ERR_INVALID, "bad kernel choice");
     // Every tensor must be indexable with 63-bit offsets and every per-image plane with 31 bits.
     const long long frames = (long long)d->N * (d->dims == 3 ? d->D + 2 : 1);
     const long long plane = (long long)d->H * d->W;
@@ -114,6 +114,16 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         else if (!strcmp(force, "igemm")) choice = X3_KERNEL_IGEMM;
     }
     bool cl_ok = false;
+    if (choice == X3_KERNEL_HEAD_TWO_PASS) {
+        if (!igemm_cl_plan(p, p->num_sms)) {
+            delete p;
+            return fail(X3_ERR_UNSUPPORTED, "the two-pass head needs unpatchify2x2, 3D, X3_NDHWC and bf16");
+        }
+        p->kind = K_HEAD_TWO_PASS;
+        p->packed_bytes = (size_t)p->cl.KT * p->cl.n_chunks * (128 * 64 * 2);
+        *plan = p;
+        return X3_OK;
+    }
     if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) cl_ok = igemm_cl_plan(p, p->num_sms);
     if (choice != X3_KERNEL_DIRECT && !cl_ok) igemm_ok = igemm_plan(p, p->num_sms);
     if (choice == X3_KERNEL_IGEMM && !igemm_ok && !cl_ok) {
@@ -139,6 +149,7 @@ void conv_plan_destroy(x3_conv_plan* plan) { delete plan; }
 
 const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
     if (!plan) return "";
+    if (plan->kind == K_HEAD_TWO_PASS) return "head_two_pass";
     if (plan->kind == K_IGEMM_CL && plan->cl.kwm) return "igemm_tcgen05_sw128_head";
     if (plan->kind == K_IGEMM_CL && plan->cl.nchw) return "igemm_tcgen05_sw128_nchw";
     return plan->kind == K_IGEMM_CL ? "igemm_tcgen05_sw128" : plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
@@ -149,7 +160,7 @@ int conv_plan_launches(const x3_conv_plan* plan) { return plan ? 1 : 0; }
 int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
     if (!plan) return snprintf(buf, len, "{}");
     const IgemmGeom& g = plan->g;
-    if (plan->kind == K_IGEMM_CL) {
+    if (plan->kind == K_IGEMM_CL || plan->kind == K_HEAD_TWO_PASS) {
         const ClGeom& c = plan->cl;
         return snprintf(buf, len,
                         "{\"kernel\": \"igemm_tcgen05_sw128\", \"mode\": \"channels_last_sw128_swapped\", "
@@ -200,10 +211,38 @@ x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carr
     const char* lo_x = (const char*)x;
     const char* hi_x = lo_x + in_elems(plan) * 2;
     if (lo_y < hi_x && lo_x < hi_y) return fail(X3_ERR_INVALID, "conv_forward: y overlaps x");
+    if (plan->kind == K_HEAD_TWO_PASS)
+        return fail(X3_ERR_INVALID, "conv_forward: a two-pass head plan runs with conv_head_two_pass");
     if (plan->kind == K_IGEMM_CL)
         return launch_igemm_cl(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
     if (plan->kind == K_IGEMM) return launch_igemm(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
     return launch_direct(plan, x, c, w_packed, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
+}
+
+size_t conv_head_g_bytes(const x3_conv_plan* plan) {
+    if (!plan || plan->kind != K_HEAD_TWO_PASS) return 0;
+    return (size_t)plan->d.N * plan->d.D * plan->d.H * plan->d.W * 112 * 2;
+}
+
+x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void* carry, const void* w_packed,
+                             const void* bias, void* g, void* y, x3_stream_t stream) {
+    clear_err();
+    if (!plan || plan->kind != K_HEAD_TWO_PASS) return fail(X3_ERR_INVALID, "conv_head_two_pass: needs a two-pass head plan");
+    if (!x || !w_packed || !g || !y || (plan->d.has_bias && !bias))
+        return fail(X3_ERR_INVALID, "conv_head_two_pass: NULL argument");
+    if (!aligned(x, 16) || !aligned(g, 16) || !aligned(y, 16) || !aligned(w_packed, 256) || (carry && !aligned(carry, 16)))
+        return fail(X3_ERR_INVALID, "conv_head_two_pass: x, g, y, carry need 16-byte alignment, w_packed 256-byte");
+    // pass 1: the temporal convolution into g (112 channels, no bias, no activation)
+    x3_conv_plan p1 = *plan;
+    p1.kind = K_IGEMM_CL;
+    p1.d.C_out = 112;
+    p1.d.unpatchify2x2 = 0;
+    p1.d.act = X3_ACT_NONE;
+    p1.d.has_bias = 0;
+    x3_status st = launch_igemm_cl(&p1, x, carry, w_packed, nullptr, g, (cudaStream_t)stream);
+    if (st != X3_OK) return st;
+    // pass 2: nine spatial taps, bias, clamp, one rounding, unpatchify
+    return launch_head_stencil(plan, g, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
 }
 
 size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers) {

@@ -179,7 +179,106 @@ __global__ void __launch_bounds__(256) pack_kwm_kernel(const uint16_t* __restric
     }
 }
 
+// Packed weights of the temporal pass of the two-pass head: blocks ordered [kt][chunk], each the
+// canonical A tile [8 planes][128 rows][8 channels] where row (i*3+j)*12 + c (< 108) carries
+// w[c][ci][kt][i][j] and rows 108..127 are zero.
+__global__ void __launch_bounds__(256) pack_ctr_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                       int C_in, int n_chunks, size_t total) {
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        size_t r = idx;
+        const int e = (int)(r % 8); r /= 8;
+        const int row = (int)(r % 128); r /= 128;
+        const int j8 = (int)(r % 8); r /= 8;
+        const int cc = (int)(r % n_chunks); r /= n_chunks;
+        const int kt = (int)r;
+        const int ci = cc * 64 + j8 * 8 + e;
+        uint16_t v = 0;
+        if (row < 108 && ci < C_in) {
+            const int i = row / 36, j = (row / 12) % 3, c = row % 12;
+            v = w[(((size_t)c * C_in + ci) * 3 + kt) * 9 + i * 3 + j];
+        }
+        out[idx] = v;
+    }
+}
+
+// The nine spatial taps of the two-pass head, one thread per output position: bias-initialised fp32
+// accumulators for the 12 channels, the (i, j) slice of g at each neighbour inside the plane added in
+// i, j order, clamp to [-1,1], one rounding to bf16, written as the 2x2-unpatchified RGB pixels
+// (channel c = rgb*4 + dy*2 + dx goes to pixel (2h+dy, 2w+dx)), channels-last.
+__global__ void __launch_bounds__(256) head_stencil_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ bias,
+                                                           uint16_t* __restrict__ rgb, int frames, int H, int W) {
+    const size_t total = (size_t)frames * H * W;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int w = (int)(idx % W);
+        const size_t fh = idx / W;
+        const int h = (int)(fh % H);
+        const size_t f = fh / H;
+        float acc[12];
+#pragma unroll
+        for (int c = 0; c < 12; ++c) acc[c] = bias ? __bfloat162float(__ushort_as_bfloat16(__ldg(bias + c))) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int hh = h + i - 1;
+            if (hh < 0 || hh >= H) continue;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int ww = w + j - 1;
+                if (ww < 0 || ww >= W) continue;
+                // 12 bf16 of tap (i, j): 24 bytes, 8-byte aligned
+                const uint2* p = reinterpret_cast<const uint2*>(g + ((f * H + hh) * W + ww) * 112 + (i * 3 + j) * 12);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    const uint2 v = __ldg(p + q);
+                    acc[4 * q + 0] += __uint_as_float(v.x << 16);
+                    acc[4 * q + 1] += __uint_as_float(v.x & 0xffff0000u);
+                    acc[4 * q + 2] += __uint_as_float(v.y << 16);
+                    acc[4 * q + 3] += __uint_as_float(v.y & 0xffff0000u);
+                }
+            }
+        }
+        uint16_t o[12];
+#pragma unroll
+        for (int c = 0; c < 12; ++c) {
+            const __nv_bfloat16 r = __float2bfloat16_rn(fminf(1.0f, fmaxf(-1.0f, acc[c])));
+            o[c] = *reinterpret_cast<const uint16_t*>(&r);
+        }
+        const size_t W2 = 2 * (size_t)W;
+#pragma unroll
+        for (int dy = 0; dy < 2; ++dy) {
+            uint32_t* row = reinterpret_cast<uint32_t*>(rgb + ((f * 2 * H + 2 * (size_t)h + dy) * W2 + 2 * (size_t)w) * 3);
+            // pixels dx = 0, 1 x rgb: channel rgb*4 + dy*2 + dx
+            const uint16_t px[6] = {o[dy * 2], o[4 + dy * 2], o[8 + dy * 2], o[dy * 2 + 1], o[4 + dy * 2 + 1], o[8 + dy * 2 + 1]};
+            row[0] = (uint32_t)px[0] | ((uint32_t)px[1] << 16);
+            row[1] = (uint32_t)px[2] | ((uint32_t)px[3] << 16);
+            row[2] = (uint32_t)px[4] | ((uint32_t)px[5] << 16);
+        }
+    }
+}
+
+x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* bias, void* y, cudaStream_t s) {
+    const int frames = p->d.N * p->d.D;
+    const size_t total = (size_t)frames * p->d.H * p->d.W;
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)p->num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    head_stencil_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)g, (const uint16_t*)bias, (uint16_t*)y,
+                                                         frames, p->d.H, p->d.W);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "head stencil launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
 x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s) {
+    if (p->kind == K_HEAD_TWO_PASS) {
+        const size_t total = p->packed_bytes / 2;
+        size_t blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        pack_ctr_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, p->d.C_in,
+                                                        p->cl.n_chunks, total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
     if (p->kind == K_IGEMM_CL && p->cl.kwm) {
         const size_t total = p->packed_bytes / 2;
         size_t blocks = (total + 255) / 256;

@@ -54,6 +54,7 @@ struct ClArgs {
     int win_adv;     // raster positions between consecutive windows (256, or 254 when kw is folded into M)
     int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW: raw tile columns, stage bytes, TMA bytes, stages
     int ngroups;     // kw folded into M: channel groups (10 channels x 3 kw per TMEM lane quarter)
+    int ctr;         // 1: centre spatial tap only (the temporal pass of the two-pass head)
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
-                        constexpr int kTaps = KWM ? 3 : 9;
+                        const int kTaps = KWM ? 3 : (a.ctr ? 1 : 9);
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTaps) * (size_t)kWBlock;
                         for (int tap = 0; tap < kTaps; ++tap) {
@@ -287,8 +288,9 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) { ok = false; break; }
                         ptx::tc_fence_after();
                         const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
-                        for (int kh = 0; kh < 3 && ok; ++kh) {
-                            for (int kw = 0; kw < (KWM ? 1 : 3); ++kw) {
+                        const int kh0 = a.ctr ? 1 : 0, kh1 = a.ctr ? 2 : 3;
+                        for (int kh = kh0; kh < kh1 && ok; ++kh) {
+                            for (int kw = (a.ctr ? 1 : 0); kw < (KWM ? 1 : (a.ctr ? 2 : 3)); ++kw) {
                                 const uint32_t sw = w_cnt % a.n_w;
                                 if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
                                 ptx::tc_fence_after();
@@ -598,13 +600,19 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     }
     // the conv_out head (12 channels to unpatchified RGB) runs in the kw-folded form
     g.kwm = d.unpatchify2x2 ? 1 : 0;
-    if (!g.kwm && !g.nchw && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
+    g.ctr = (d.kernel == X3_KERNEL_HEAD_TWO_PASS) ? 1 : 0;
+    if (g.ctr) {
+        // temporal pass of the two-pass head: 12 output channels x 9 spatial taps = 108 (112) channels
+        if (!d.unpatchify2x2 || d.dims != 3 || d.layout != X3_NDHWC || d.dtype != X3_BF16) return false;
+        g.kwm = 0;
+    }
+    if (!g.kwm && !g.nchw && !g.ctr && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
     g.win_adv = g.kwm ? kBNP - 2 : kBNP;
     g.ngroups = g.kwm ? (d.C_out + 9) / 10 : 0;
     if (g.kwm && g.ngroups > 4) return false;
     g.KT = d.dims == 3 ? 3 : 1;
     g.n_chunks = (d.C_in + kCK - 1) / kCK;
-    g.n_tiles = (d.C_out + kBM - 1) / kBM;
+    g.n_tiles = g.ctr ? 1 : (d.C_out + kBM - 1) / kBM;
     g.frames = d.N * (d.dims == 3 ? d.D : 1);
     const int H_out = p->H_out, W_out = p->W_out;
     const int fixed = 1024 + 4 * kStageWarpBytes + 512 + (g.nchw ? 4 * 32 * 16 : 0);
@@ -677,7 +685,7 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
-    a.win_adv = g.win_adv; a.ngroups = g.ngroups;
+    a.win_adv = g.win_adv; a.ngroups = g.ngroups; a.ctr = g.ctr;
     a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes; a.raw_tx_bytes = g.raw_tx_bytes; a.n_raw = g.n_raw;
     a.idesc = ptx::idesc_f16(kBM, kBNP, bf16);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;

@@ -9,7 +9,7 @@
 
 namespace x3 {
 
-enum KernelKind { K_DIRECT = 0, K_IGEMM = 1, K_IGEMM_CL = 2 };
+enum KernelKind { K_DIRECT = 0, K_IGEMM = 1, K_IGEMM_CL = 2, K_HEAD_TWO_PASS = 3 };
 
 // A-operand staging modes of the implicit-GEMM engine.
 enum StageMode {
@@ -68,6 +68,7 @@ struct ClGeom {
     int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW raw-slice staging
     int win_adv;                 // raster positions between consecutive windows (256, or 254 when kwm)
     int ngroups;                 // kwm: groups of 10 output channels (one TMEM lane quarter each)
+    int ctr;                     // 1: centre spatial tap only (temporal pass of the two-pass head)
     long long tiles;
     int smem_bytes, grid;
 };
@@ -106,6 +107,8 @@ bool igemm_plan(x3_conv_plan* p, int num_sms);  // fills p->g; false if the engi
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms);  // fills p->cl (+ packing fields of p->g)
 x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                           const void* bias, void* y, cudaStream_t s);
+// Two-pass head: temporal pass into the 112-channel g plane, then the spatial stencil.
+x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* bias, void* y, cudaStream_t s);
 x3_status read_device_status(int reset);
 x3_status selftest_wait_timeout(int limit_ms, cudaStream_t s);
 x3_status device_status_word(unsigned int** out);  // device address of the timeout status word
