@@ -219,3 +219,53 @@ def test_head_two_pass_plan(lib):
         with pytest.raises(x3.X3Error) as e:
             x3.conv_plan_create(x3.make_desc(**{**good, **bad}))
         assert e.value.status == x3.X3_ERR_UNSUPPORTED
+
+
+SHADOW_WORKLOADS = {
+    "taesd_3to64_256": dict(dims=2, N=4, C_in=3, C_out=64, H=256, W=256, dtype="f16"),
+    "taesd_64_256": dict(dims=2, N=4, C_in=64, C_out=64, H=256, W=256, dtype="f16"),
+    "taesd_64_256_s2": dict(dims=2, N=4, C_in=64, C_out=64, H=256, W=256, stride=2, dtype="f16"),
+    "taesd_64_128": dict(dims=2, N=4, C_in=64, C_out=64, H=128, W=128, dtype="f16"),
+    "odd_5to24": dict(dims=2, N=1, C_in=5, C_out=24, H=37, W=83),
+    "odd_72to136": dict(dims=2, N=1, C_in=72, C_out=136, H=19, W=42),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHADOW_WORKLOADS))
+def test_nchw_layers_have_channels_last_forms(lib, name):
+    """A 2D NCHW layer's channels-last form (used between the layers of a stack) stages every halo
+    row its windows read, covers the stride-1 raster of its input, and puts its weight blocks after
+    the layer's own packed weights unless the two share one format."""
+    cfg = SHADOW_WORKLOADS[name]
+    p = x3.conv_plan_create(x3.make_desc(**cfg))
+    try:
+        g = x3.conv_plan_describe(p)
+        s = g["shadow"]
+        P, HR, Wt = s["P"], s["HR"], s["Wt"]
+        assert P == Wt + 2 and P <= 256 and HR <= 256
+        for win in range(min(s["windows"], 4 * P)):
+            need = (256 * win) % P + 255 + 2 * P + 2 + 1
+            assert need <= HR * P
+        assert s["strips"] * Wt >= cfg["W"] and s["windows"] * 256 >= cfg["H"] * P
+        assert s["sub2"] == (cfg.get("stride", 1) == 2)
+        assert s["n_chunks"] == (cfg["C_in"] + 63) // 64
+        assert s["n_tiles"] == (cfg["C_out"] + (63 if s["m64"] else 127)) // (64 if s["m64"] else 128)
+        assert s["smem_bytes"] <= 232448 and s["w_off"] % 256 == 0
+        assert s["m64"] == (cfg["C_out"] <= 64)
+        shadow_bytes = s["n_tiles"] * s["n_chunks"] * 9 * (64 if s["m64"] else 128) * 64 * 2
+        assert x3.conv_packed_weight_bytes(p) == s["w_off"] + shadow_bytes or \
+            (s["w_off"] == 0 and x3.conv_packed_weight_bytes(p) == shadow_bytes)
+    finally:
+        x3.conv_plan_destroy(p)
+
+
+def test_stack_workspace_covers_the_channels_last_input(lib):
+    """A two-layer NCHW stack run channels-last holds the converted input and one intermediate."""
+    a = x3.conv_plan_create(x3.make_desc(2, 2, 64, 8, 16, 24))
+    b = x3.conv_plan_create(x3.make_desc(2, 2, 8, 8, 16, 24))
+    try:
+        need = x3.conv_stack_workspace_bytes([a, b])
+        assert need == 2 * ((2 * 16 * 24 * 64 * 2 + 255) // 256 * 256)
+    finally:
+        x3.conv_plan_destroy(a)
+        x3.conv_plan_destroy(b)

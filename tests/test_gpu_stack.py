@@ -122,12 +122,25 @@ def test_stack3d_single_frame_passes():
     assert_exact(np.concatenate(outs, axis=1), want, "bf16")
 
 
-@pytest.mark.parametrize("variant", ["int", "random"])
-def test_stack2d_taesd_like(variant):
-    """A shortened TAESD-like chain at reduced size, NCHW f16: 3->32, 32->32, 32->32 stride 2, 32->32."""
-    N, H, W = 2, 40, 72
+TAESD_LIKE = {
     # integer data: two layers stay inside f16's range (16*9*2*110 < 65504) with exact fp32 sums
-    spec = [(3, 16, 1), (16, 16, 2)] if variant == "int" else [(3, 32, 1), (32, 32, 1), (32, 32, 2), (32, 32, 1)]
+    "int": [(3, 16, 1), (16, 16, 2)],
+    # {-1,0,1} data, sparse weights: small exact sums through four layers, stride 2 inside the chain
+    "sparse1": [(3, 16, 1), (16, 16, 1), (16, 16, 2), (16, 8, 1)],
+    "random": [(3, 32, 1), (32, 32, 1), (32, 32, 2), (32, 32, 1)],
+}
+
+
+@pytest.mark.parametrize("layout", ["channels_last", "nchw"])
+@pytest.mark.parametrize("variant", ["int", "sparse1", "random"])
+def test_stack2d_taesd_like(variant, layout, monkeypatch):
+    """A shortened TAESD-like chain at reduced size, NCHW f16 in and out. channels_last: the driver
+    keeps the activations between layers channels-last (the default when every layer has that form
+    and the last one has stride 1); nchw: every layer runs its own NCHW form."""
+    if layout == "nchw":
+        monkeypatch.setenv("X3CONV_STACK_LAYOUT", "nchw")
+    N, H, W = 2, 40, 72
+    spec = TAESD_LIKE[variant]
     x = synth.activation([4400, 0], (N, 3, H, W), "f16", variant, ("uniform", -1.0, 1.0))
     layers = [synth.make_layer([4400, i], 2, ci, co, "f16", stride=s, act="relu", variant=variant)
               for i, (ci, co, s) in enumerate(spec)]
@@ -142,7 +155,7 @@ def test_stack2d_taesd_like(variant):
     y = x.vals
     for L in layers:
         y, _ = oracle.round_to(oracle.conv2d(y, L.w.vals, L.b.vals, stride=L.stride, act="relu"), "f16")
-    if variant == "int":
+    if variant != "random":
         assert np.array_equal(got, y)
     else:
         assert_close(got, y)
@@ -168,3 +181,29 @@ def test_stack3d_wide_channels():
     assert_close(got, want)
     assert np.array_equal(host_values(cdev[0], "bf16"), want_carries[0])
     assert_close(host_values(cdev[1], "bf16"), want_carries[1])
+
+
+def test_stack2d_layouts_agree_on_odd_shapes(monkeypatch):
+    """Channel counts that are not multiples of 64, odd sizes, stride 2 with odd input sizes, one
+    image: the channels-last stack against the per-layer NCHW stack and the oracle."""
+    N, H, W = 1, 37, 83
+    spec = [(5, 24, 1), (24, 40, 2), (40, 72, 1), (72, 136, 1), (136, 16, 1)]
+    x = synth.activation([4600, 0], (N, 5, H, W), "bf16", "random", ("uniform", -1.0, 1.0))
+    layers = [synth.make_layer([4600, i], 2, ci, co, "bf16", stride=s, act="relu" if i < 4 else "none")
+              for i, (ci, co, s) in enumerate(spec)]
+    convs, h, w = [], H, W
+    for L in layers:
+        convs.append(x3.Conv(x3.make_desc(2, N, L.C_in, L.C_out, h, w, stride=L.stride, dtype="bf16", act=L.act),
+                             dev(L.w), dev(L.b)))
+        h, w = convs[-1].H_out, convs[-1].W_out
+    assert all("shadow" in x3.conv_plan_describe(c.plan) for c in convs)
+    y_cl = host_values(x3.ConvStack(convs)(dev(x)), "bf16")
+    monkeypatch.setenv("X3CONV_STACK_LAYOUT", "nchw")
+    y_nc = host_values(x3.ConvStack(convs)(dev(x)), "bf16")
+    torch.cuda.synchronize()
+    assert y_cl.shape == y_nc.shape == (1, 16, 19, 42)
+    ref = x.vals
+    for L in layers:
+        ref, _ = oracle.round_to(oracle.conv2d(ref, L.w.vals, L.b.vals, stride=L.stride, act=L.act), "bf16")
+    assert_close(y_cl, ref)
+    assert_close(y_nc, ref)

@@ -14,7 +14,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libx3conv.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "direct.cu", "igemm.cu", "igemm_cl.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "direct.cu", "igemm.cu", "igemm_cl.cu", "layout.cu", "noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

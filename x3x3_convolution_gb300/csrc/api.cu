@@ -141,6 +141,32 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         p->kind = K_DIRECT;
         p->packed_bytes = direct_packed_bytes(p->d);
     }
+    // A 2D NCHW layer on the tensor-core engines also gets a channels-last form for the stack driver,
+    // which keeps the activations between layers channels-last; unless forced to one engine.
+    if (p->d.dims == 2 && p->d.layout == X3_NCHW && choice != X3_KERNEL_DIRECT && !force && p->d.stride <= 2 &&
+        p->d.C_out % 8 == 0) {
+        x3_conv_plan q = *p;
+        q.d.layout = X3_NHWC;
+        q.d.C_in = (q.d.C_in + 7) / 8 * 8;
+        q.d.stride = 1;
+        q.H_out = q.d.H;
+        q.W_out = q.d.W;
+        if (igemm_cl_plan(&q, p->num_sms, true)) {
+            p->has_shadow = 1;
+            p->cl_shadow = q.cl;
+            p->cl_shadow.sub2 = p->d.stride == 2 ? 1 : 0;
+            // the channels-last engine's weight blocks; the NCHW form of the same engine uses the
+            // same blocks (n_chunks agree: C_in and its round-up to 8 need the same 64-channel chunks)
+            if (p->kind == K_IGEMM_CL && !p->cl.kwm && !p->cl.ctr && !q.cl.m64 && p->cl.n_chunks == q.cl.n_chunks &&
+                p->cl.n_tiles == q.cl.n_tiles) {
+                p->shadow_w_off = 0;
+            } else {
+                p->shadow_w_off = (p->packed_bytes + 255) & ~(size_t)255;
+                p->packed_bytes = p->shadow_w_off +
+                                  (size_t)q.cl.n_tiles * q.cl.n_chunks * 9 * ((q.cl.m64 ? 64 : 128) * 64 * 2);
+            }
+        }
+    }
     *plan = p;
     return X3_OK;
 }
@@ -157,7 +183,7 @@ const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
 
 int conv_plan_launches(const x3_conv_plan* plan) { return plan ? 1 : 0; }
 
-int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
+static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
     if (!plan) return snprintf(buf, len, "{}");
     const IgemmGeom& g = plan->g;
     if (plan->kind == K_IGEMM_CL || plan->kind == K_HEAD_TWO_PASS) {
@@ -185,6 +211,23 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
                     g.n_chunks, g.KT, g.NSUB, g.Rt, g.Wt, g.P, g.spr, g.plane_stride, g.a_bytes, g.raw_bytes,
                     g.b_bytes, g.n_a, g.n_b, g.n_raw, g.acc_bufs, g.tmem_cols, g.col_tiles, g.row_tiles, g.frames,
                     g.tiles, g.smem_bytes, g.grid, plan->H_out, plan->W_out, plan->num_sms);
+}
+
+int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
+    char tmp[2048];
+    int n = describe_main(plan, tmp, sizeof tmp);
+    if (plan && plan->has_shadow && n > 0 && (size_t)n < sizeof tmp) {
+        // the channels-last form used inside stacks: appended as "shadow" before the closing brace
+        const ClGeom& c = plan->cl_shadow;
+        const int m = snprintf(tmp + n - 1, sizeof tmp - (size_t)(n - 1),
+                               ", \"shadow\": {\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, "
+                               "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"sub2\": %d, \"tiles\": %lld, "
+                               "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d}}",
+                               c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.sub2, c.tiles,
+                               c.smem_bytes, c.grid, plan->shadow_w_off, c.m64);
+        n = n - 1 + m;
+    }
+    return snprintf(buf, len, "%s", tmp);
 }
 
 size_t conv_packed_weight_bytes(const x3_conv_plan* plan) { return plan ? plan->packed_bytes : 0; }
@@ -245,6 +288,32 @@ x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void
     return launch_head_stencil(plan, g, plan->d.has_bias ? bias : nullptr, y, (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace x3 {
+
+// A stack of 2D NCHW layers that all have a channels-last form, the last one stride 1, runs with its
+// activations channels-last between the layers: the input is converted once, each layer reads and
+// writes NHWC, and the last layer's epilogue writes the NCHW result. X3CONV_STACK_LAYOUT=nchw turns
+// this off (each layer then runs its own NCHW form).
+static bool stack_channels_last(const x3_conv_plan* const* plans, int n_layers) {
+    if (n_layers < 2) return false;
+    const char* env = getenv("X3CONV_STACK_LAYOUT");
+    if (env && !strcmp(env, "nchw")) return false;
+    for (int i = 0; i < n_layers; ++i)
+        if (!plans[i] || plans[i]->d.dims != 2 || plans[i]->d.layout != X3_NCHW || !plans[i]->has_shadow) return false;
+    return plans[n_layers - 1]->d.stride == 1;
+}
+
+// Bytes of the channels-last copy of the first layer's input (C_in rounded up to 8).
+static size_t stack_input_cl_bytes(const x3_conv_plan* p) {
+    return (size_t)p->d.N * p->d.H * p->d.W * ((p->d.C_in + 7) / 8 * 8) * 2;
+}
+
+}  // namespace x3
+
+extern "C" {
+
 size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers) {
     if (!plans || n_layers < 1) return 0;
     size_t biggest = 0;
@@ -253,6 +322,12 @@ size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers
         size_t b = out_elems(plans[i]) * 2;
         b = (b + 255) & ~(size_t)255;
         if (b > biggest) biggest = b;
+    }
+    if (n_layers > 1 && plans[n_layers - 1] && stack_channels_last(plans, n_layers)) {
+        // two buffers: the converted input and the odd layers' outputs / the even layers' outputs
+        size_t b = (stack_input_cl_bytes(plans[0]) + 255) & ~(size_t)255;
+        if (b > biggest) biggest = b;
+        return 2 * biggest;
     }
     return n_layers > 1 ? (n_layers > 2 ? 2 * biggest : biggest) : 0;
 }
@@ -320,8 +395,25 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
     if (need && (!workspace || workspace_bytes < need))
         return fail(X3_ERR_OOM, "conv_stack_forward: workspace needs %zu bytes, got %zu", need, workspace_bytes);
     if (workspace && !aligned(workspace, 256)) return fail(X3_ERR_INVALID, "conv_stack_forward: workspace must be 256-byte aligned");
-    const size_t half = n_layers > 2 ? need / 2 : need;
     cudaStream_t s = (cudaStream_t)stream;
+    if (stack_channels_last(plans, n_layers)) {
+        const size_t half = need / 2;
+        void* buf[2] = {workspace, (char*)workspace + half};
+        const x3_conv_desc& d0 = plans[0]->d;
+        x3_status st = launch_nchw_to_nhwc(x, buf[0], d0.N, d0.C_in, (d0.C_in + 7) / 8 * 8, d0.H, d0.W, s);
+        if (st != X3_OK) return st;
+        const void* in = buf[0];
+        for (int i = 0; i < n_layers; ++i) {
+            const bool last = i == n_layers - 1;
+            void* out = last ? y : buf[(i + 1) % 2];
+            const x3_conv_plan* p = plans[i];
+            st = launch_igemm_cl_shadow(p, in, w_packed[i], p->d.has_bias ? bias[i] : nullptr, out, last ? 1 : 0, s);
+            if (st != X3_OK) return st;
+            in = out;
+        }
+        return X3_OK;
+    }
+    const size_t half = n_layers > 2 ? need / 2 : need;
     const void* in = x;
     for (int i = 0; i < n_layers; ++i) {
         void* out = (i == n_layers - 1) ? y : (char*)workspace + (size_t)(i % 2) * half;

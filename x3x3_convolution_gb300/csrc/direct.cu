@@ -268,7 +268,27 @@ x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* 
     return X3_OK;
 }
 
+static x3_status pack_primary(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s);
+
 x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s) {
+    x3_status st = pack_primary(p, w, w_packed, s);
+    if (st != X3_OK || !p->has_shadow || p->shadow_w_off == 0) return st;
+    // the channels-last form's weight blocks (128, or 64 in the M = 64 form, output channels x 64
+    // input channels per tap)
+    const ClGeom& g = p->cl_shadow;
+    const int rows = g.m64 ? 64 : 128;
+    PackArgs a{p->d.C_in, p->d.C_out, 1, rows, 64, g.n_chunks, g.n_tiles};
+    const size_t total = (size_t)g.n_tiles * g.n_chunks * 9 * rows * 64;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pack_igemm_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w,
+                                                      (uint16_t*)((uint8_t*)w_packed + p->shadow_w_off), a, total);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
+static x3_status pack_primary(const x3_conv_plan* p, const void* w, void* w_packed, cudaStream_t s) {
     if (p->kind == K_HEAD_TWO_PASS) {
         const size_t total = p->packed_bytes / 2;
         size_t blocks = (total + 255) / 256;
@@ -290,13 +310,14 @@ x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_pack
         return X3_OK;
     }
     if (p->kind == K_DIRECT) {
-        cudaError_t e = cudaMemcpyAsync(w_packed, w, p->packed_bytes, cudaMemcpyDeviceToDevice, s);
+        const size_t bytes = (size_t)p->d.C_out * p->d.C_in * (p->d.dims == 3 ? 27 : 9) * 2;
+        cudaError_t e = cudaMemcpyAsync(w_packed, w, bytes, cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return fail(X3_ERR_CUDA, "weight copy: %s", cudaGetErrorString(e));
         return X3_OK;
     }
     const IgemmGeom& g = p->g;
     PackArgs a{p->d.C_in, p->d.C_out, g.KT, g.BN, g.CK, g.n_chunks, g.n_tiles};
-    const size_t total = p->packed_bytes / 2;
+    const size_t total = (size_t)g.n_tiles * g.KT * g.n_chunks * 9 * g.BN * g.CK;
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     pack_igemm_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, a, total);

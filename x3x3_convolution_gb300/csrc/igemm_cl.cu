@@ -43,6 +43,7 @@ constexpr int kBM = 128;        // output channels per tile (MMA M)
 constexpr int kBNP = 256;       // positions per tile (MMA N)
 constexpr int kCK = 64;         // input channels per staged chunk (one 128-byte swizzle row)
 constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one tap, one chunk)
+constexpr int kWBlock64 = 64 * kCK * 2; // the same for the M = 64 form
 constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kStageWarpBytes = 32 * kSPitch * 4;  // per-warp staging block (covers both uses)
@@ -55,6 +56,10 @@ struct ClArgs {
     int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW: raw tile columns, stage bytes, TMA bytes, stages
     int ngroups;     // kw folded into M: channel groups (10 channels x 3 kw per TMEM lane quarter)
     int ctr;         // 1: centre spatial tap only (the temporal pass of the two-pass head)
+    int sub2;        // 1: stride 2 as the stride-1 raster with only even (oh, ow) stored at (oh/2, ow/2)
+    int out_nchw;    // 1: channels-last input, NCHW output (the NCHW epilogue)
+    int yH, yW;      // stored output plane (H_out x W_out, or halved when sub2)
+    int w_smem;      // bytes of shared memory for weight blocks (n_w stages, or all blocks when resident)
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -113,6 +118,18 @@ __device__ __forceinline__ uint16_t cl_round(float v) {
     }
 }
 
+// Two values rounded to the storage type and packed, the first in the low half.
+template <bool BF16>
+__device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
+    if (BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
 // KWM (the conv_out head form): the MMA's M rows are (kw, output channel) triples, quarter g of the
 // 128 TMEM lanes holding kw*10 + r for channel 10g + r, so one MMA covers the three horizontal taps
 // of a row of the window and the K loop runs over (kt, kh, channel) only; the epilogue adds the three
@@ -120,7 +137,12 @@ __device__ __forceinline__ uint16_t cl_round(float v) {
 // NC (NCHW 2D input and output): the producer loads raw [16 channels][HR rows][Wt+16 columns] tiles,
 // four transposer warps (6-9) turn them into the swizzled position rows with ldmatrix.trans /
 // stmatrix (shifting the halo by one column on the way), and the epilogue writes NCHW planes.
-template <bool BF16, bool KWM, bool NC>
+// CTR (the temporal pass of the two-pass head): only the centre spatial tap, one weight block per
+// (kt, chunk). Each form is its own instantiation so the MMA issuer's loops keep constant bounds.
+// M64 (layers with at most 64 output channels): MMAs of M = 64, whose accumulator rows 16q..16q+15
+// sit in TMEM lanes 32q..32q+15; every weight block of the layer stays resident in shared memory
+// (loaded once per CTA), so a tile only streams its halo.
+template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -130,7 +152,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     uint8_t* sbase = smem_raw + (base - raw_base);
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
-    const uint32_t sStage = sW + (uint32_t)(a.n_w * kWBlock);      // epilogue transpose tile
+    const uint32_t sStage = sW + (uint32_t)a.w_smem;               // epilogue transpose tile
     const uint32_t sRaw = sStage + 4u * (uint32_t)kStageWarpBytes;           // NCHW raw tiles (128-aligned)
     const uint32_t sJunk = sRaw + (uint32_t)(a.n_raw * a.raw_bytes);         // NCHW: 16 B per transposer lane
     const uint32_t sBar = sJunk + (NC ? 4u * 32u * 16u : 0u);
@@ -191,6 +213,13 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         if (lane == 0) {
             uint32_t h_cnt = 0, w_cnt = 0, r_cnt = 0;
             bool ok = true;
+            if (M64) {  // every weight block of the layer, once, on the first weight barrier
+                const int nblk = a.KT * a.n_chunks * 9;
+                ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)(nblk * kWBlock64));
+                for (int b = 0; b < nblk; ++b)
+                    ptx::bulk_load(sW + (uint32_t)(b * kWBlock64), a.w + (size_t)b * kWBlock64, (uint32_t)kWBlock64, bar_w_full);
+                w_cnt = 1;
+            }
             for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
                 const ClTile tc = cl_decode(a, tile);
                 const int n = tc.fr / a.dout, t = tc.fr % a.dout;
@@ -227,10 +256,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
-                        const int kTaps = KWM ? 3 : (a.ctr ? 1 : 9);
+                        constexpr int kTaps = KWM ? 3 : (CTR ? 1 : 9);
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTaps) * (size_t)kWBlock;
-                        for (int tap = 0; tap < kTaps; ++tap) {
+                        for (int tap = 0; tap < (M64 ? 0 : kTaps); ++tap) {
                             const uint32_t sw = w_cnt % a.n_w;
                             if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
@@ -265,8 +294,13 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             bool ok = true;
             // A (weights), no swizzle: SBO = 128 B between 8-row groups, LBO = 2 KB between the two
             // 8-channel halves of a 16-channel K step; version 1 in bits 46-47.
+            constexpr int kRows = M64 ? 64 : kBM;  // rows of a weight block (MMA M)
             const uint32_t a_hi = (128u >> 4) | (1u << 14);
-            const uint32_t a_lo0 = ((sW >> 4) & 0x3FFFu) | ((uint32_t)((kBM * 16) >> 4) << 16);
+            const uint32_t a_lo0 = ((sW >> 4) & 0x3FFFu) | ((uint32_t)((kRows * 16) >> 4) << 16);
+            if (M64) {  // resident weights
+                if (!cl_wait(bar_w_full, 0, abort_flag, a.status)) ok = false;
+                ptx::tc_fence_after();
+            }
             // B (halo), 128-byte swizzle: SBO = 1024 B between 8-row groups, LBO encoded 1 (unused by
             // the swizzled K-major layout), version 1, layout type 2 (128-byte swizzle) in bits 61-63,
             // base offset 0. The tensor core applies the swizzle to the absolute shared-memory address
@@ -288,28 +322,34 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) { ok = false; break; }
                         ptx::tc_fence_after();
                         const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
-                        const int kh0 = a.ctr ? 1 : 0, kh1 = a.ctr ? 2 : 3;
-                        for (int kh = kh0; kh < kh1 && ok; ++kh) {
-                            for (int kw = (a.ctr ? 1 : 0); kw < (KWM ? 1 : (a.ctr ? 2 : 3)); ++kw) {
+                        for (int kh = (CTR ? 1 : 0); kh < (CTR ? 2 : 3) && ok; ++kh) {
+                            for (int kw = (CTR ? 1 : 0); kw < (KWM ? 1 : (CTR ? 2 : 3)); ++kw) {
                                 const uint32_t sw = w_cnt % a.n_w;
-                                if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
-                                ptx::tc_fence_after();
-                                const uint32_t a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
+                                uint32_t a_lo;
+                                if (M64) {
+                                    a_lo = a_lo0 + (uint32_t)(((kt * a.n_chunks + cc) * 9 + kh * 3 + kw) * (kWBlock64 >> 4));
+                                } else {
+                                    if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
+                                    ptx::tc_fence_after();
+                                    a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
+                                }
                                 const uint32_t row_addr = hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
                                 const uint32_t b_hi = b_hi_fixed;
 #pragma unroll
                                 for (int ks = 0; ks < kCK / 16; ++ks) {
                                     if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
                                     const uint64_t adesc = ((uint64_t)a_hi << 32) |
-                                                           (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kBM * 16) >> 4));
+                                                           (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kRows * 16) >> 4));
                                     const uint32_t baddr = row_addr + (uint32_t)ks * 32u;
                                     const uint64_t bdesc = ((uint64_t)b_hi << 32) |
                                                            (uint64_t)(((baddr >> 4) & 0x3FFFu) | (1u << 16));
                                     ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
                                     acc = 1;
                                 }
-                                ptx::mma_commit(bar_w_empty + 8 * sw);
-                                ++w_cnt;
+                                if (!M64) {
+                                    ptx::mma_commit(bar_w_empty + 8 * sw);
+                                    ++w_cnt;
+                                }
                             }
                         }
                         if (!ok) break;
@@ -349,7 +389,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             ptx::tc_fence_after();
             const ClTile tc = cl_decode(a, tile);
             const int n = tc.fr / a.dout, t = tc.fr % a.dout;
-            const int co_lane = tc.nt * kBM + q * 32 + lane;
+            constexpr int kCpw = M64 ? 16 : 32;  // accumulator rows per TMEM lane quarter
+            const int co_lane = (M64 && lane >= 16) ? a.C_out : tc.nt * (M64 ? 64 : kBM) + q * kCpw + lane;
             if (tc.nt != cur_nt) {
                 bias_r = 0.0f;
                 if (a.bias && co_lane < a.C_out) {
@@ -402,11 +443,11 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     }
                 }
             } else {
-                if (NC) {
+                if (NC || a.out_nchw) {
                     // NCHW: this warp's 32 channels x 32 positions are transposed through its staging
                     // block so that each store instruction writes 32 consecutive positions of a channel.
                     uint16_t* T = reinterpret_cast<uint16_t*>(stage_ptr + ew * kStageWarpBytes);  // [32][34]
-                    const int co_base = tc.nt * kBM + q * 32;
+                    const int co_base = tc.nt * (M64 ? 64 : kBM) + q * kCpw;
                     if (co_base < a.C_out) {
                         for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
                             uint32_t v[32];
@@ -421,11 +462,72 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             const int m = m0 + chunk * 32 + lane;
                             const int oh = m / a.P, c = m % a.P;
                             const int ow = ow0 + c;
-                            if (c < a.Wt && ow < a.W_out && oh < a.H_out) {
-                                const size_t plane = (size_t)a.H_out * a.W_out;
-                                uint16_t* yp = y + ((size_t)n * a.C_out + co_base) * plane + (size_t)oh * a.W_out + ow;
-                                const int nco = min(32, a.C_out - co_base);
+                            const bool keep = c < a.Wt && ow < a.W_out && oh < a.H_out && !(a.sub2 && ((oh | ow) & 1));
+                            if (keep) {
+                                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
+                                const size_t plane = (size_t)a.yH * a.yW;
+                                uint16_t* yp = y + ((size_t)n * a.C_out + co_base) * plane + (size_t)yh * a.yW + yw;
+                                const int nco = min(kCpw, a.C_out - co_base);
                                 for (int r = 0; r < nco; ++r) yp[(size_t)r * plane] = T[r * 34 + lane];
+                            }
+                        }
+                    }
+                } else if (M64) {
+                    // M = 64: this quarter's 16 channels x 32 positions per chunk come in the MMA
+                    // fragment layout (16 lanes x 256 bits, four column groups); each thread rounds its
+                    // pairs of positions into packed 32-bit words, stmatrix.trans writes them as
+                    // [position][16 channels] rows of the warp's staging block, and each position's
+                    // 32 bytes go out as two 16-byte stores. The next chunk's TMEM load is in flight
+                    // while this one is processed.
+                    const uint32_t wst = sStage + (uint32_t)(ew * kStageWarpBytes);  // [32][16] x 2 B
+                    const uint8_t* wstp = stage_ptr + ew * kStageWarpBytes;
+                    const int g = lane >> 2;
+                    const int co0 = tc.nt * 64 + q * 16 + g, co1 = co0 + 8;
+                    float b0 = 0.0f, b1 = 0.0f;
+                    if (a.bias) {
+                        const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.bias);
+                        if (co0 < a.C_out) b0 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co0) << 16) : __half2float(__ushort_as_half(__ldg(bp + co0)));
+                        if (co1 < a.C_out) b1 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co1) << 16) : __half2float(__ushort_as_half(__ldg(bp + co1)));
+                    }
+                    const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
+                    // stmatrix row address of this thread: matrix mi = lane / 8 (column group i = mi / 2,
+                    // channel half mi % 2), row j = lane % 8 = position 8i + j of the pair of groups
+                    const int mi = lane >> 3, jr = lane & 7;
+                    const uint32_t st_addr = wst + (uint32_t)((8 * (mi >> 1) + jr) * 32 + (mi & 1) * 16);
+                    uint32_t r0[16], r1[16];
+                    ptx::tmem_ld16x256b_x4(tq, r0);
+#pragma unroll
+                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                        uint32_t (&v)[16] = (chunk & 1) ? r1 : r0;
+                        ptx::tmem_ld_wait();
+                        if (chunk + 1 < kBNP / 32) ptx::tmem_ld16x256b_x4(tq + (uint32_t)((chunk + 1) * 32), (chunk & 1) ? r0 : r1);
+                        uint32_t h[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            h[2 * i] = cl_pack2<BF16>(cl_act(__uint_as_float(v[4 * i]) + b0, a.act),
+                                                      cl_act(__uint_as_float(v[4 * i + 1]) + b0, a.act));
+                            h[2 * i + 1] = cl_pack2<BF16>(cl_act(__uint_as_float(v[4 * i + 2]) + b1, a.act),
+                                                          cl_act(__uint_as_float(v[4 * i + 3]) + b1, a.act));
+                        }
+                        __syncwarp();
+                        ptx::stsm_x4_trans(st_addr, h[0], h[1], h[2], h[3]);            // positions 0..15
+                        ptx::stsm_x4_trans(st_addr + 16u * 32u, h[4], h[5], h[6], h[7]);  // positions 16..31
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int piece = k * 32 + lane;
+                            const int pos = piece >> 1, half = piece & 1;
+                            const int m = m0 + chunk * 32 + pos;
+                            const int oh = m / a.P, c = m % a.P;
+                            const int ow = ow0 + c;
+                            const int co = tc.nt * 64 + q * 16 + half * 8;
+                            if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
+                                !(a.sub2 && ((oh | ow) & 1))) {
+                                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
+                                const uint4 val = *reinterpret_cast<const uint4*>(wstp + pos * 32 + half * 16);
+                                const size_t off =
+                                    ((((size_t)n * a.dout + t) * a.yH + yh) * a.yW + yw) * (size_t)a.C_out + co;
+                                *reinterpret_cast<uint4*>(y + off) = val;
                             }
                         }
                     }
@@ -444,17 +546,20 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
                         __syncwarp();
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int row = k * 8 + (lane >> 2);
-                            const int seg = lane & 3;
+                        for (int k = 0; k < (M64 ? 2 : 4); ++k) {
+                            // 32 positions x (kCpw / 8) 16-byte channel segments per chunk
+                            const int row = M64 ? k * 16 + (lane >> 1) : k * 8 + (lane >> 2);
+                            const int seg = M64 ? (lane & 1) : (lane & 3);
                             const int m = m0 + chunk * 32 + row;
                             const int oh = m / a.P, c = m % a.P;
                             const int ow = ow0 + c;
-                            const int co = tc.nt * kBM + q * 32 + seg * 8;
-                            if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out) {
+                            const int co = tc.nt * (M64 ? 64 : kBM) + q * kCpw + seg * 8;
+                            if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
+                                !(a.sub2 && ((oh | ow) & 1))) {
+                                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
                                 const uint4 val = *reinterpret_cast<const uint4*>(wst + row * kStagePitch + seg * 16);
                                 const size_t off =
-                                    ((((size_t)n * a.dout + t) * a.H_out + oh) * a.W_out + ow) * (size_t)a.C_out + co;
+                                    ((((size_t)n * a.dout + t) * a.yH + yh) * a.yW + yw) * (size_t)a.C_out + co;
                                 *reinterpret_cast<uint4*>(y + off) = val;
                             }
                         }
@@ -585,7 +690,7 @@ x3_status encode_nchw_raw(CUtensorMap* m, bool bf16, const void* ptr, uint64_t W
 
 }  // namespace
 
-bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
+bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     const x3_conv_desc& d = p->d;
     if (d.stride != 1) return false;
     ClGeom g;
@@ -606,7 +711,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
         if (!d.unpatchify2x2 || d.dims != 3 || d.layout != X3_NDHWC || d.dtype != X3_BF16) return false;
         g.kwm = 0;
     }
-    if (!g.kwm && !g.nchw && !g.ctr && (d.C_out % 8 != 0 || d.C_out < 96)) return false;
+    if (!g.kwm && !g.nchw && !g.ctr && (d.C_out % 8 != 0 || (d.C_out < 96 && !small_cout))) return false;
     g.win_adv = g.kwm ? kBNP - 2 : kBNP;
     g.ngroups = g.kwm ? (d.C_out + 9) / 10 : 0;
     if (g.kwm && g.ngroups > 4) return false;
@@ -621,6 +726,17 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     int cands[80], nc = 0;
     for (int k = 1; k <= 64; ++k) cands[nc++] = (W_out + k - 1) / k;
     cands[nc++] = 30; cands[nc++] = 62; cands[nc++] = 126; cands[nc++] = 254;  // P divides 256
+    // layers with at most 64 output channels (when asked for): the M = 64 form with every weight block
+    // resident in shared memory; if no tiling leaves room for them, the 128-row form
+    g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
+    if (g.m64) g.n_tiles = 1;
+  for (int attempt = 0; attempt < 2 && !found; ++attempt) {
+    if (attempt == 1) {
+        if (!g.m64) break;
+        g.m64 = 0;
+        g.n_tiles = (d.C_out + kBM - 1) / kBM;
+    }
+    const int wres = g.m64 ? g.KT * g.n_chunks * 9 * kWBlock64 : 0;
     for (int ci = 0; ci < nc; ++ci) {
         const int Wt = g.nchw ? (cands[ci] + 7) / 8 * 8 : cands[ci];  // NCHW: strips start 16-byte aligned
         const int P = Wt + 2;
@@ -644,6 +760,10 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
         }
         int n_w = (kSmemLimit - fixed - 2 * h_bytes - n_raw * raw_bytes) / kWBlock;
         if (n_w > 6) n_w = 6;
+        if (g.m64) {
+            if (fixed + 2 * h_bytes + wres > kSmemLimit) continue;
+            n_w = 6;  // no weight ring: rank as the deepest one
+        }
         if (n_w < 3) continue;
         const int strips = (W_out + Wt - 1) / Wt;
         const int windows = (int)(((long long)H_out * P + g.win_adv - 1) / g.win_adv);
@@ -656,12 +776,14 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
             found = true;
             best_cost = cost;
             g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
-            g.n_h = 2; g.n_w = n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
+            g.n_h = 2; g.n_w = g.m64 ? 1 : n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
             g.raw_w = g.nchw ? raw_w : 0; g.raw_bytes = raw_bytes; g.n_raw = n_raw;
             g.raw_tx_bytes = g.nchw ? 16 * HR * raw_w * 2 : 0;
-            g.smem_bytes = fixed + 2 * h_bytes + n_w * kWBlock + n_raw * raw_bytes;
+            g.w_smem = g.m64 ? wres : n_w * kWBlock;
+            g.smem_bytes = fixed + 2 * h_bytes + g.w_smem + n_raw * raw_bytes;
         }
     }
+  }
     if (!found) return false;
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
     p->cl = g;
@@ -672,22 +794,25 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms) {
     return true;
 }
 
-x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
-                          const void* bias, void* y, cudaStream_t s) {
-    const x3_conv_desc& d = p->d;
-    const ClGeom& g = p->cl;
+namespace {
+
+// One launch of the engine for descriptor d (its layout, C_in and stride as the kernel sees them)
+// with tiling g over an H_out x W_out raster; the stored plane is yH x yW.
+x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out, int yH, int yW, int out_nchw,
+                    const void* x, const void* carry, const void* w_packed, const void* bias, void* y, cudaStream_t s) {
     const bool bf16 = d.dtype == X3_BF16;
     ClArgs a;
     memset(&a, 0, sizeof a);
     a.C_in = d.C_in; a.C_out = d.C_out; a.N = d.N; a.D = d.D; a.H = d.H; a.W = d.W;
-    a.H_out = p->H_out; a.W_out = p->W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
+    a.H_out = H_out; a.W_out = W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
+    a.sub2 = g.sub2; a.out_nchw = out_nchw; a.yH = yH; a.yW = yW; a.w_smem = g.w_smem;
     a.has_carry = carry != nullptr;
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
     a.win_adv = g.win_adv; a.ngroups = g.ngroups; a.ctr = g.ctr;
     a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes; a.raw_tx_bytes = g.raw_tx_bytes; a.n_raw = g.n_raw;
-    a.idesc = ptx::idesc_f16(kBM, kBNP, bf16);
+    a.idesc = ptx::idesc_f16(g.m64 ? 64 : kBM, kBNP, bf16);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
     x3_status st0 = device_status_word(&a.status);
     if (st0 != X3_OK) return st0;
@@ -709,7 +834,9 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
         }
     }
     void (*k)(CUtensorMap, CUtensorMap, ClArgs);
-    if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
+    if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
+    else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
+    else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
     else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false> : igemm_cl_kernel<false, true, false>;
     else k = bf16 ? igemm_cl_kernel<true, false, false> : igemm_cl_kernel<false, false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
@@ -718,6 +845,24 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl launch: %s", cudaGetErrorString(e));
     return X3_OK;
+}
+
+}  // namespace
+
+x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
+                          const void* bias, void* y, cudaStream_t s) {
+    return launch_cl(p->d, p->cl, p->H_out, p->W_out, p->H_out, p->W_out, 0, x, carry, w_packed, bias, y, s);
+}
+
+x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const void* w_packed, const void* bias,
+                                 void* y, int out_nchw, cudaStream_t s) {
+    if (!p->has_shadow) return fail(X3_ERR_UNSUPPORTED, "layer has no channels-last form");
+    x3_conv_desc d = p->d;
+    d.layout = X3_NHWC;
+    d.C_in = (d.C_in + 7) / 8 * 8;
+    d.stride = 1;
+    return launch_cl(d, p->cl_shadow, d.H, d.W, p->H_out, p->W_out, out_nchw, x, nullptr,
+                     (const uint8_t*)w_packed + p->shadow_w_off, bias, y, s);
 }
 
 }  // namespace x3

@@ -69,6 +69,9 @@ struct ClGeom {
     int win_adv;                 // raster positions between consecutive windows (256, or 254 when kwm)
     int ngroups;                 // kwm: groups of 10 output channels (one TMEM lane quarter each)
     int ctr;                     // 1: centre spatial tap only (temporal pass of the two-pass head)
+    int sub2;                    // 1: stride 2 computed as the stride-1 raster, even positions kept
+    int m64;                     // 1: M = 64 MMAs (at most 64 output channels), weights resident
+    int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
     long long tiles;
     int smem_bytes, grid;
 };
@@ -83,6 +86,12 @@ struct x3_conv_plan {
     x3::ClGeom cl;
     size_t packed_bytes;
     int num_sms;
+    // Channels-last form of a 2D NCHW layer, used by the stack driver for the layers between the
+    // first input and the last output: input NHWC with C_in rounded up to 8, stride 1 (stride 2 as
+    // sub2). Its packed weights start at shadow_w_off bytes into the layer's packed buffer.
+    int has_shadow;
+    x3::ClGeom cl_shadow;
+    size_t shadow_w_off;
 };
 
 namespace x3 {
@@ -104,9 +113,17 @@ x3_status launch_direct(const x3_conv_plan* p, const void* x, const void* carry,
 x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                        const void* bias, void* y, cudaStream_t s);
 bool igemm_plan(x3_conv_plan* p, int num_sms);  // fills p->g; false if the engine can't run it
-bool igemm_cl_plan(x3_conv_plan* p, int num_sms);  // fills p->cl (+ packing fields of p->g)
+// Fills p->cl (+ packing fields of p->g); small_cout also accepts channels-last layers with fewer
+// than 96 output channels (the M tile is then partly empty).
+bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout = false);
 x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                           const void* bias, void* y, cudaStream_t s);
+// The channels-last form (cl_shadow) of a 2D NCHW layer: x is NHWC with C_in rounded up to 8
+// channels; y is NHWC, or NCHW when out_nchw. w_packed is the layer's packed buffer.
+x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const void* w_packed, const void* bias,
+                                 void* y, int out_nchw, cudaStream_t s);
+// NCHW [N][C][H][W] -> NHWC [N][H][W][C8], channels C..C8-1 zero.
+x3_status launch_nchw_to_nhwc(const void* x, void* y, int N, int C, int C8, int H, int W, cudaStream_t s);
 // Two-pass head: temporal pass into the 112-channel g plane, then the spatial stencil.
 x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* bias, void* y, cudaStream_t s);
 x3_status read_device_status(int reset);
