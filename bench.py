@@ -8,7 +8,9 @@ The step runs every stage of the path through the library's C ABI:
              (+2 carried) at 352x624 (conv_stack_forward with per-layer carries);
   * l3     - causal 256->128 over 4 frames (+2 carried) at 176x312 (conv_forward);
   * head   - conv_out head: causal 256->12 over 4 frames (+2 carried) at 352x624, bias, clamp to
-             [-1,1], 2x2 unpatchify to 4x704x1248 RGB (conv_forward).
+             [-1,1], 2x2 unpatchify to 4x704x1248 RGB, as the split form (conv_head_two_pass with an
+             fp32 G plane: the temporal pass on the tensor cores, then the nine spatial taps; exact on
+             integer data like the single-pass form, which is timed beside it with the bf16-G form).
 value = total convolution FLOP of the step / step time (TFLOP/s, whole job over all ranks).
 Also reported: decoder-stack ms per frame (stack + l3 + head over the 4 frames), per-stage times,
 the roofline fraction of the dominant kernel, an end-to-end number with host buffers, the SM
@@ -38,7 +40,7 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
             "(256->12 @4+2x352x624, clamp, 2x2 unpatchify)")
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
-AB_STAGES = ["head_two_pass"]
+AB_STAGES = ["head_fused", "head_two_pass"]
 TRAFFIC_DOMINANT_BYTES = 876.3e6
 
 
@@ -160,16 +162,22 @@ class Workload:
         self.l3_c = st["carry3"].torch(dev)
         self.l3_y = torch.empty(self.l3.out_shape(), dtype=torch.bfloat16, device=dev)
         hx, hc, HL = synth.head(seed=1005 + seed_base)
-        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, D=FRAMES, act="clamp", unpatchify2x2=True),
+        head_desc = dict(D=FRAMES, act="clamp", unpatchify2x2=True)
+        # the step's head: two passes with an fp32 G plane (buffer held by the Conv)
+        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_split", **head_desc),
                             HL.w.torch(dev), HL.b.torch(dev))
         self.head_x = hx.torch(dev)
         self.head_c = hc.torch(dev)
         self.head_y = torch.empty(self.head.out_shape(), dtype=torch.bfloat16, device=dev)
-        # A/B variant of the head, not part of the step: the two-pass (temporal, then spatial) form
-        self.head2 = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, D=FRAMES, act="clamp", unpatchify2x2=True,
-                                          kernel="head_two_pass"), HL.w.torch(dev), HL.b.torch(dev))
+        # A/B forms of the head, not part of the step: the single pass and the bf16-G two passes
+        self.head_fused = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, **head_desc), HL.w.torch(dev),
+                                  HL.b.torch(dev))
+        self.head_fused_y = torch.empty(self.head_fused.out_shape(), dtype=torch.bfloat16, device=dev)
+        self.head2 = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_two_pass", **head_desc),
+                             HL.w.torch(dev), HL.b.torch(dev))
         self.head2_y = torch.empty(self.head2.out_shape(), dtype=torch.bfloat16, device=dev)
-        self.kernels_per_step = len(convs) + len(sc) + 2
+        # kernels per step: layout conversion + 7 TAESD convs, 2 stack convs, l3, the head's two passes
+        self.kernels_per_step = 1 + len(convs) + len(sc) + 1 + 2
         self.plans = {"taesd": [x3.conv_plan_describe(c.plan) for c in convs],
                       "stack": x3.conv_plan_describe(sc[0].plan),
                       "l3": x3.conv_plan_describe(self.l3.plan),
@@ -279,6 +287,7 @@ def run_stage(wl, args, stream, fl, nb):
                                     stream=stream),
           "l3": lambda: wl.l3(wl.l3_x, wl.l3_c, out=wl.l3_y, stream=stream),
           "head": lambda: wl.head(wl.head_x, wl.head_c, out=wl.head_y, stream=stream),
+          "head_fused": lambda: wl.head_fused(wl.head_x, wl.head_c, out=wl.head_fused_y, stream=stream),
           "head_two_pass": lambda: wl.head2(wl.head_x, wl.head_c, out=wl.head2_y, stream=stream)}[args.stage]
     for _ in range(args.warmup):
         fn()
@@ -291,17 +300,18 @@ def run_stage(wl, args, stream, fl, nb):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    key = "head" if args.stage == "head_two_pass" else args.stage
+    key = "head" if args.stage.startswith("head") else args.stage
     print(json.dumps({"stage": args.stage, "ms": ms, "tflops": fl[key] / (ms * 1e-3) / 1e12,
                       "gbs": nb[key] / (ms * 1e-3) / 1e9, "plan": wl.plans[key]}), flush=True)
 
 
 def head_ab(wl, stream, reps=10):
-    """The fused head and its two-pass variant, each timed alone (CUDA events, after warm-up), and
-    the largest difference between their outputs."""
+    """The step's head (two passes, fp32 G), the single-pass head and the bf16-G two passes, each
+    timed alone (CUDA events, after warm-up), and the largest differences from the single pass."""
     import torch
     out = {}
-    for name, conv, y in (("fused", wl.head, wl.head_y), ("two_pass", wl.head2, wl.head2_y)):
+    for name, conv, y in (("split_f32", wl.head, wl.head_y), ("fused", wl.head_fused, wl.head_fused_y),
+                          ("two_pass_bf16", wl.head2, wl.head2_y)):
         for _ in range(3):
             conv(wl.head_x, wl.head_c, out=y, stream=stream)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -313,7 +323,8 @@ def head_ab(wl, stream, reps=10):
         e1.record(stream)
         torch.cuda.synchronize()
         out[name + "_ms"] = e0.elapsed_time(e1) / reps
-    out["max_abs_diff"] = float((wl.head_y.float() - wl.head2_y.float()).abs().max())
+    out["max_abs_diff_split_f32"] = float((wl.head_fused_y.float() - wl.head_y.float()).abs().max())
+    out["max_abs_diff_two_pass_bf16"] = float((wl.head_fused_y.float() - wl.head2_y.float()).abs().max())
     return out
 
 

@@ -67,11 +67,14 @@ typedef enum {
     X3_KERNEL_AUTO = 0,   /* pick the fastest kernel that handles the descriptor */
     X3_KERNEL_IGEMM = 1,  /* tcgen05/TMEM implicit GEMM (fails with X3_ERR_UNSUPPORTED if it can't) */
     X3_KERNEL_DIRECT = 2, /* plain SIMT direct convolution; handles every valid descriptor */
-    X3_KERNEL_HEAD_TWO_PASS = 3 /* conv_out head as two passes (run with conv_head_two_pass): a temporal-
-                                   only 3x1x1 convolution into a 112-channel bf16 plane g, then the nine
-                                   spatial taps with bias and clamp (FastVideo wan22_vae_decode/solution/
-                                   head.cu, header comment and head_stencil_kernel); needs
-                                   unpatchify2x2, 3D, X3_NDHWC, bf16 */
+    X3_KERNEL_HEAD_TWO_PASS = 3, /* conv_out head as two passes (run with conv_head_two_pass): a temporal-
+                                    only 3x1x1 convolution into a 108-channel bf16 plane g, then the nine
+                                    spatial taps with bias and clamp (FastVideo wan22_vae_decode/solution/
+                                    head.cu, header comment and head_stencil_kernel); needs
+                                    unpatchify2x2, 3D, X3_NDHWC, bf16 */
+    X3_KERNEL_HEAD_SPLIT = 4     /* the same two passes with g kept in fp32: every product and partial sum
+                                    is carried in fp32 as in the single-pass head, so integer-valued data
+                                    give the exact result; same requirements */
 } x3_kernel;
 
 /* Descriptor of one convolution layer. */
@@ -146,15 +149,18 @@ x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carr
 
 /*
  * The conv_out head computed as the head.cu page's two passes, for a plan made with
- * kernel = X3_KERNEL_HEAD_TWO_PASS (weights packed by conv_pack_weights with that plan):
- *   pass 1: g[n,t,h,w,(i*3+j)*12+c] = bf16( sum_{ci,kt} w[c,ci,kt,i,j] * xt[n,ci,t+kt,h,w] ), channels
- *           108..111 zero: a temporal-only convolution on the tensor cores, one fp32 accumulator per
- *           value, rounded once into the plane;
- *   pass 2: y = bf16( clamp( b[c] + sum_{i,j} g[n,t,h+i-1,w+j-1,(i*3+j)*12+c] ) ) with the zero padding,
- *           written as unpatchified RGB like conv_forward's head output.
- * The early bf16 rounding of g is the page's value path; it differs from conv_forward's single
+ * kernel = X3_KERNEL_HEAD_TWO_PASS or X3_KERNEL_HEAD_SPLIT (weights packed by conv_pack_weights with
+ * that plan):
+ *   pass 1: G[n,t,p,h,w,c] = sum_{ci,kt} w[c,ci,kt,i,j] * xt[n,ci,t+kt,h,w] for the nine spatial taps
+ *           p = i*3+j: a temporal-only convolution on the tensor cores, one fp32 accumulator per value,
+ *           stored as bf16 (HEAD_TWO_PASS, rounded once) or fp32 (HEAD_SPLIT);
+ *   pass 2: y = bf16( clamp( b[c] + sum_{i,j} G[n,t,i*3+j,h+i-1,w+j-1,c] ) ) with the zero padding,
+ *           summed in fp32 in (i, j) order, written as unpatchified RGB like conv_forward's head output.
+ * The early bf16 rounding of G is the page's value path; it differs from conv_forward's single
  * accumulator over all 27 taps by a few bf16 ulps of the partial sums (max|d| moves, rms does not).
- *   g: caller buffer of conv_head_g_bytes(plan) bytes, 16-byte aligned ([N][D][H][W][112] bf16).
+ * With fp32 G the two passes differ from the single pass only in the order of the fp32 additions.
+ *   g: caller buffer of conv_head_g_bytes(plan) bytes, 16-byte aligned, layout [N][D][9][H][W][12] of
+ *      bf16 or fp32 (each tap's 12 channels contiguous per position, one plane per tap).
  * Errors: X3_ERR_INVALID (wrong plan kind, NULL or misaligned pointers), X3_ERR_CUDA.
  */
 size_t conv_head_g_bytes(const x3_conv_plan* plan);

@@ -166,7 +166,13 @@ def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
-        if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head", "head_two_pass"):
+        if WORKLOADS[name].get("kernel") == "head_two_pass":
+            # the temporal pass stages no halo: windows of 256 consecutive positions of a frame
+            assert g["P"] == g["Wt"] == g["W_out"] and g["strips"] == 1
+            assert g["windows"] * 256 >= g["H_out"] * g["W_out"] and g["h_bytes"] == 256 * 128
+            assert g["tiles"] == g["windows"] * g["frames"] and g["smem_bytes"] <= 232448
+            return
+        if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head"):
             _check_sw128_plan(g)
             return
         assert g["kernel"] == "igemm_tcgen05"
@@ -199,7 +205,7 @@ def test_head_two_pass_plan(lib):
     p = x3.conv_plan_create(x3.make_desc(**good))
     try:
         assert x3.conv_plan_kernel_name(p) == "head_two_pass"
-        assert x3.conv_head_g_bytes(p) == 2 * 3 * 20 * 30 * 112 * 2
+        assert x3.conv_head_g_bytes(p) == 2 * 3 * 9 * 20 * 30 * 12 * 2      # [N][D][9][H][W][12] bf16
         assert x3.conv_packed_weight_bytes(p) == 3 * 4 * 128 * 64 * 2   # [kt][chunk] A tiles, centre tap only
         g = x3.conv_plan_describe(p)
         assert g["win_adv"] == 256 and not g["kwm"] and g["n_tiles"] == 1
@@ -215,6 +221,12 @@ def test_head_two_pass_plan(lib):
         assert lib.conv_head_two_pass(q, 16, None, 256, 32, 4096, 8192, None) == x3.X3_ERR_INVALID
     finally:
         x3.conv_plan_destroy(q)
+    s = x3.conv_plan_create(x3.make_desc(**{**good, "kernel": "head_split"}))
+    try:
+        assert x3.conv_plan_kernel_name(s) == "head_split"
+        assert x3.conv_head_g_bytes(s) == 2 * 3 * 9 * 20 * 30 * 12 * 4    # fp32 G
+    finally:
+        x3.conv_plan_destroy(s)
     for bad in (dict(unpatchify2x2=False), dict(layout="NCDHW"), dict(dtype="f16")):
         with pytest.raises(x3.X3Error) as e:
             x3.conv_plan_create(x3.make_desc(**{**good, **bad}))

@@ -1,11 +1,14 @@
 """GPU parity of the two-pass conv_out head (the head.cu page's temporal-then-spatial split).
 
-Pass 1 is the swapped tcgen05 engine in its centre-tap form writing the 108 (112) channel bf16
-plane g; pass 2 is the stencil kernel (nine spatial taps in fp32, bias, clamp, one rounding,
-2x2 unpatchify). Both are compared with the oracle's two-pass restatement (g rounded to bf16):
-exactly on sparse {-1,0,1} data, where every g value and sum is representable; within the
-random-data tolerance otherwise. Against the exact single-pass head the rounding of g costs
-accuracy, so that comparison is by PSNR over the [-1,1] range.
+Pass 1 is the swapped tcgen05 engine in its centre-tap form writing one plane of G per spatial tap
+(12 channels each); pass 2 is the stencil kernel (nine spatial taps in fp32, bias, clamp, one
+rounding, 2x2 unpatchify).
+
+* head_two_pass (G in bf16, the page's value path) against the oracle's two-pass restatement with
+  G rounded to bf16: exactly on sparse {-1,0,1} data, where every G value and sum is representable;
+  within the random-data tolerance otherwise; against the exact single-pass head by PSNR.
+* head_split (G in fp32) against the oracle's single-pass head: exactly on {-2..2} integer data
+  (every partial sum is an integer below 2^24), within the tolerance and PSNR on random data.
 """
 import numpy as np
 import pytest
@@ -29,12 +32,12 @@ def _lib():
     assert x3.conv_device_status(1) == x3.X3_OK
 
 
-def run_two_pass(x, carry, L):
+def run_two_pass(x, carry, L, kernel="head_two_pass"):
     N, D, H, W, C = x.shape
     d = x3.make_desc(3, N, C, 12, H, W, D=D, layout="NDHWC", dtype="bf16", act="clamp", unpatchify2x2=True,
-                     kernel="head_two_pass")
+                     kernel=kernel)
     conv = x3.Conv(d, dev(L.w), dev(L.b))
-    assert conv.kernel_name == "head_two_pass"
+    assert conv.kernel_name == kernel
     y = conv(dev(x), None if carry is None else dev(carry))
     torch.cuda.synchronize()
     return host_values(y, "bf16"), conv
@@ -85,5 +88,37 @@ def test_two_pass_head_full_size_sampled():
     cr = crops_3d(seq, pos)
     y = oracle.head_two_pass(cr[:, 2:3], L.w.vals, L.b.vals, carry=cr[:, 0:2], layout="NDHWC")[:, 0, 1, 1, :]
     ref = to_rgb(y[:, None, None, None, :])[:, 0]                   # [n, 2, 2, 3]
+    g = np.stack([got[0, t, 2 * h:2 * h + 2, 2 * w:2 * w + 2] for (t, h, w) in pos])
+    assert_close(g, ref)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=str)
+@pytest.mark.parametrize("variant", ["int", "sparse1", "random"])
+def test_split_head(variant, shape):
+    D, H, W = shape
+    x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3700 + H + W)
+    got, _ = run_two_pass(x, carry, L, kernel="head_split")
+    ref = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp", layout="NDHWC"))
+    assert got.shape == ref.shape
+    if variant != "random":   # int: mostly clamped values; sparse1: small unclamped sums
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+        assert psnr(got, ref) >= PSNR_MIN
+        split = to_rgb(oracle.head_two_pass(x.vals, L.w.vals, L.b.vals, carry=carry.vals, round_g=False,
+                                            layout="NDHWC"))
+        assert_close(got, split)
+
+
+def test_split_head_full_size_sampled():
+    x, carry, L = synth.head(seed=3960)
+    got, _ = run_two_pass(x, carry, L, kernel="head_split")
+    assert got.shape == (1, 4, 704, 1248, 3)
+    seq = np.concatenate([carry.vals, x.vals], axis=1)
+    pos = sample_positions(4, 352, 624, 300, seed=78)
+    cr = crops_3d(seq, pos)
+    y = oracle.conv3d_causal(cr[:, 2:3], L.w.vals, L.b.vals, carry=cr[:, 0:2], act="clamp",
+                             layout="NDHWC")[:, 0, 1, 1, :]
+    ref = to_rgb(y[:, None, None, None, :])[:, 0]
     g = np.stack([got[0, t, 2 * h:2 * h + 2, 2 * w:2 * w + 2] for (t, h, w) in pos])
     assert_close(g, ref)

@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "X3_OK", 1: "X3_ERR_INVALID", 2: "X3_ERR_UNSUPPORTED", 3: "X3
 LAYOUT = {"NCHW": 0, "NHWC": 1, "NCDHW": 2, "NDHWC": 3}
 DTYPE = {"f16": 0, "bf16": 1}
 ACT = {"none": 0, "relu": 1, "clamp": 2}
-KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3}
+KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3, "head_split": 4}
 
 
 class ConvDesc(ctypes.Structure):
@@ -238,7 +238,7 @@ class Conv:
         torch = _torch()
         if out is None:
             out = torch.empty(self.out_shape(), dtype=x.dtype, device=x.device)
-        if self.kernel_name == "head_two_pass":
+        if self.kernel_name in ("head_two_pass", "head_split"):
             gb = conv_head_g_bytes(self.plan)
             if getattr(self, "_g", None) is None or self._g.numel() * 2 < gb:
                 self._g = torch.empty(gb // 2, dtype=torch.int16, device=x.device)

@@ -62,7 +62,7 @@ static x3_status validate(const x3_conv_desc* d) {
     if (d->has_bias != 0 && d->has_bias != 1) return fail(X3_ERR_INVALID, "has_bias must be 0 or 1");
     if (d->unpatchify2x2 != 0 && d->unpatchify2x2 != 1) return fail(X3_ERR_INVALID, "unpatchify2x2 must be 0 or 1");
     if (d->unpatchify2x2 && d->C_out != 12) return fail(X3_ERR_INVALID, "unpatchify2x2 needs C_out == 12");
-    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_TWO_PASS) return fail(X3_ERR_INVALID, "bad kernel choice");
+    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_SPLIT) return fail(X3_ERR_INVALID, "bad kernel choice");
     // Every tensor must be indexable with 63-bit offsets and every per-image plane with 31 bits.
     const long long frames = (long long)d->N * (d->dims == 3 ? d->D + 2 : 1);
     const long long plane = (long long)d->H * d->W;
@@ -114,7 +114,7 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         else if (!strcmp(force, "igemm")) choice = X3_KERNEL_IGEMM;
     }
     bool cl_ok = false;
-    if (choice == X3_KERNEL_HEAD_TWO_PASS) {
+    if (choice == X3_KERNEL_HEAD_TWO_PASS || choice == X3_KERNEL_HEAD_SPLIT) {
         if (!igemm_cl_plan(p, p->num_sms)) {
             delete p;
             return fail(X3_ERR_UNSUPPORTED, "the two-pass head needs unpatchify2x2, 3D, X3_NDHWC and bf16");
@@ -175,7 +175,7 @@ void conv_plan_destroy(x3_conv_plan* plan) { delete plan; }
 
 const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
     if (!plan) return "";
-    if (plan->kind == K_HEAD_TWO_PASS) return "head_two_pass";
+    if (plan->kind == K_HEAD_TWO_PASS) return plan->d.kernel == X3_KERNEL_HEAD_SPLIT ? "head_split" : "head_two_pass";
     if (plan->kind == K_IGEMM_CL && plan->cl.kwm) return "igemm_tcgen05_sw128_head";
     if (plan->kind == K_IGEMM_CL && plan->cl.nchw) return "igemm_tcgen05_sw128_nchw";
     return plan->kind == K_IGEMM_CL ? "igemm_tcgen05_sw128" : plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
@@ -264,7 +264,8 @@ x3_status conv_forward(const x3_conv_plan* plan, const void* x, const void* carr
 
 size_t conv_head_g_bytes(const x3_conv_plan* plan) {
     if (!plan || plan->kind != K_HEAD_TWO_PASS) return 0;
-    return (size_t)plan->d.N * plan->d.D * plan->d.H * plan->d.W * 112 * 2;
+    // [N][D][9][H][W][12] of bf16 or fp32
+    return (size_t)plan->d.N * plan->d.D * 9 * plan->d.H * plan->d.W * 12 * (plan->d.kernel == X3_KERNEL_HEAD_SPLIT ? 4 : 2);
 }
 
 x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void* carry, const void* w_packed,
@@ -275,7 +276,8 @@ x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void
         return fail(X3_ERR_INVALID, "conv_head_two_pass: NULL argument");
     if (!aligned(x, 16) || !aligned(g, 16) || !aligned(y, 16) || !aligned(w_packed, 256) || (carry && !aligned(carry, 16)))
         return fail(X3_ERR_INVALID, "conv_head_two_pass: x, g, y, carry need 16-byte alignment, w_packed 256-byte");
-    // pass 1: the temporal convolution into g (112 channels, no bias, no activation)
+    // pass 1: the temporal convolution into g (108 accumulator rows, no bias, no activation), written
+    // one plane per spatial tap
     x3_conv_plan p1 = *plan;
     p1.kind = K_IGEMM_CL;
     p1.d.C_out = 112;

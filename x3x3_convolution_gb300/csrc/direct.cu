@@ -202,12 +202,35 @@ __global__ void __launch_bounds__(256) pack_ctr_kernel(const uint16_t* __restric
 }
 
 // The nine spatial taps of the two-pass head, one thread per output position: bias-initialised fp32
-// accumulators for the 12 channels, the (i, j) slice of g at each neighbour inside the plane added in
-// i, j order, clamp to [-1,1], one rounding to bf16, written as the 2x2-unpatchified RGB pixels
-// (channel c = rgb*4 + dy*2 + dx goes to pixel (2h+dy, 2w+dx)), channels-last.
-__global__ void __launch_bounds__(256) head_stencil_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ bias,
+// accumulators for the 12 channels, the 12 values of tap plane i*3+j at each neighbour inside the
+// image added in (i, j) order, clamp to [-1,1], one rounding to bf16, written as the 2x2-unpatchified
+// RGB pixels (channel c = rgb*4 + dy*2 + dx goes to pixel (2h+dy, 2w+dx)), channels-last. Consecutive
+// threads read consecutive positions of a plane, so every tap's loads are contiguous across a warp.
+__device__ __forceinline__ void head_add12(float (&acc)[12], const float* p) {
+    const float4* v = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const float4 f = __ldg(v + q);
+        acc[4 * q + 0] += f.x; acc[4 * q + 1] += f.y; acc[4 * q + 2] += f.z; acc[4 * q + 3] += f.w;
+    }
+}
+__device__ __forceinline__ void head_add12(float (&acc)[12], const uint16_t* p) {
+    const uint2* v = reinterpret_cast<const uint2*>(p);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const uint2 u = __ldg(v + q);
+        acc[4 * q + 0] += __uint_as_float(u.x << 16);
+        acc[4 * q + 1] += __uint_as_float(u.x & 0xffff0000u);
+        acc[4 * q + 2] += __uint_as_float(u.y << 16);
+        acc[4 * q + 3] += __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) head_stencil_kernel(const T* __restrict__ g, const uint16_t* __restrict__ bias,
                                                            uint16_t* __restrict__ rgb, int frames, int H, int W) {
-    const size_t total = (size_t)frames * H * W;
+    const size_t hw = (size_t)H * W;
+    const size_t total = (size_t)frames * hw;
     for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
         const int w = (int)(idx % W);
         const size_t fh = idx / W;
@@ -224,16 +247,7 @@ __global__ void __launch_bounds__(256) head_stencil_kernel(const uint16_t* __res
             for (int j = 0; j < 3; ++j) {
                 const int ww = w + j - 1;
                 if (ww < 0 || ww >= W) continue;
-                // 12 bf16 of tap (i, j): 24 bytes, 8-byte aligned
-                const uint2* p = reinterpret_cast<const uint2*>(g + ((f * H + hh) * W + ww) * 112 + (i * 3 + j) * 12);
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    const uint2 v = __ldg(p + q);
-                    acc[4 * q + 0] += __uint_as_float(v.x << 16);
-                    acc[4 * q + 1] += __uint_as_float(v.x & 0xffff0000u);
-                    acc[4 * q + 2] += __uint_as_float(v.y << 16);
-                    acc[4 * q + 3] += __uint_as_float(v.y & 0xffff0000u);
-                }
+                head_add12(acc, g + ((f * 9 + (size_t)(i * 3 + j)) * hw + (size_t)hh * W + ww) * 12);
             }
         }
         uint16_t o[12];
@@ -261,8 +275,12 @@ x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* 
     size_t blocks = (total + 255) / 256;
     const size_t cap = (size_t)p->num_sms * 16;
     if (blocks > cap) blocks = cap;
-    head_stencil_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)g, (const uint16_t*)bias, (uint16_t*)y,
-                                                         frames, p->d.H, p->d.W);
+    if (p->d.kernel == X3_KERNEL_HEAD_SPLIT)
+        head_stencil_kernel<float><<<(unsigned)blocks, 256, 0, s>>>((const float*)g, (const uint16_t*)bias,
+                                                                   (uint16_t*)y, frames, p->d.H, p->d.W);
+    else
+        head_stencil_kernel<uint16_t><<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)g, (const uint16_t*)bias,
+                                                                      (uint16_t*)y, frames, p->d.H, p->d.W);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "head stencil launch: %s", cudaGetErrorString(e));
     return X3_OK;

@@ -46,7 +46,8 @@ constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one
 constexpr int kWBlock64 = 64 * kCK * 2; // the same for the M = 64 form
 constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
-constexpr int kStageWarpBytes = 32 * kSPitch * 4;  // per-warp staging block (covers both uses)
+constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
+constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (covers every use)
 
 struct ClArgs {
     int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
@@ -60,6 +61,8 @@ struct ClArgs {
     int out_nchw;    // 1: channels-last input, NCHW output (the NCHW epilogue)
     int yH, yW;      // stored output plane (H_out x W_out, or halved when sub2)
     int w_smem;      // bytes of shared memory for weight blocks (n_w stages, or all blocks when resident)
+    int frame_inner; // tile order with the output frame varying fastest
+    int g_f32;       // centre-tap form: the tap planes of G in fp32 (else bf16)
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -74,6 +77,17 @@ struct ClTile {
 
 __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long t) {
     ClTile c;
+    if (a.frame_inner) {
+        // frames fastest: the output frames of one window are in flight together, so the input frames
+        // they share (three temporal taps each) are read from DRAM once and then hit in L2
+        c.fr = (int)(t % a.frames);
+        t /= a.frames;
+        c.nt = (int)(t % a.n_tiles);
+        t /= a.n_tiles;
+        c.win = (int)(t % a.windows);
+        c.strip = (int)(t / a.windows);
+        return c;
+    }
     c.nt = (int)(t % a.n_tiles);
     t /= a.n_tiles;
     c.win = (int)(t % a.windows);
@@ -253,7 +267,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             const uint32_t sh = h_cnt % a.n_h;
                             if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
-                            ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
+                            if (CTR)  // 256 consecutive positions of the frame's flattened plane
+                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
+                            else
+                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
                         constexpr int kTaps = KWM ? 3 : (CTR ? 1 : 9);
@@ -333,7 +350,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                     ptx::tc_fence_after();
                                     a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
                                 }
-                                const uint32_t row_addr = hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
+                                const uint32_t row_addr = CTR ? hbase : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
                                 const uint32_t b_hi = b_hi_fixed;
 #pragma unroll
                                 for (int ks = 0; ks < kCK / 16; ++ks) {
@@ -383,6 +400,18 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             }
         }
         uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
+        // M = 64 form: one output tile, so this thread's two bias values are loaded once; the
+        // activation as a clamp to [act_lo, act_hi]
+        float m64_b0 = 0.0f, m64_b1 = 0.0f;
+        if (M64 && a.bias) {
+            const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.bias);
+            const int co0 = q * 16 + (lane >> 2), co1 = co0 + 8;
+            if (co0 < a.C_out) m64_b0 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co0) << 16) : __half2float(__ushort_as_half(__ldg(bp + co0)));
+            if (co1 < a.C_out) m64_b1 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co1) << 16) : __half2float(__ushort_as_half(__ldg(bp + co1)));
+        }
+        const float act_lo = a.act == X3_ACT_RELU ? 0.0f : (a.act == X3_ACT_CLAMP1 ? -1.0f : -INFINITY);
+        const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
+        const float inv_p = 1.0f / (float)a.P;
         for (long long tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++it) {
             const uint32_t ab = it & 1u;
             if (!cl_wait(bar_acc_full + 8 * ab, (it >> 1) & 1u, abort_flag, a.status)) break;
@@ -481,33 +510,24 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // while this one is processed.
                     const uint32_t wst = sStage + (uint32_t)(ew * kStageWarpBytes);  // [32][16] x 2 B
                     const uint8_t* wstp = stage_ptr + ew * kStageWarpBytes;
-                    const int g = lane >> 2;
-                    const int co0 = tc.nt * 64 + q * 16 + g, co1 = co0 + 8;
-                    float b0 = 0.0f, b1 = 0.0f;
-                    if (a.bias) {
-                        const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.bias);
-                        if (co0 < a.C_out) b0 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co0) << 16) : __half2float(__ushort_as_half(__ldg(bp + co0)));
-                        if (co1 < a.C_out) b1 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co1) << 16) : __half2float(__ushort_as_half(__ldg(bp + co1)));
-                    }
+                    const float b0 = m64_b0, b1 = m64_b1;
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
                     // stmatrix row address of this thread: matrix mi = lane / 8 (column group i = mi / 2,
                     // channel half mi % 2), row j = lane % 8 = position 8i + j of the pair of groups
                     const int mi = lane >> 3, jr = lane & 7;
                     const uint32_t st_addr = wst + (uint32_t)((8 * (mi >> 1) + jr) * 32 + (mi & 1) * 16);
-                    uint32_t r0[16], r1[16];
-                    ptx::tmem_ld16x256b_x4(tq, r0);
-#pragma unroll
-                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
-                        uint32_t (&v)[16] = (chunk & 1) ? r1 : r0;
-                        ptx::tmem_ld_wait();
-                        if (chunk + 1 < kBNP / 32) ptx::tmem_ld16x256b_x4(tq + (uint32_t)((chunk + 1) * 32), (chunk & 1) ? r0 : r1);
+                    // the window's first raster row and column; a position's row and column follow from
+                    // its offset by a float reciprocal (exact: offsets < 512, pitch <= 256)
+                    const int oh0 = m0 / a.P, c00 = m0 - oh0 * a.P;
+                    uint16_t* yf = y + ((size_t)n * a.dout + t) * (size_t)a.yH * a.yW * a.C_out;
+                    auto process = [&](int chunk, const uint32_t (&v)[16]) {
                         uint32_t h[8];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            h[2 * i] = cl_pack2<BF16>(cl_act(__uint_as_float(v[4 * i]) + b0, a.act),
-                                                      cl_act(__uint_as_float(v[4 * i + 1]) + b0, a.act));
-                            h[2 * i + 1] = cl_pack2<BF16>(cl_act(__uint_as_float(v[4 * i + 2]) + b1, a.act),
-                                                          cl_act(__uint_as_float(v[4 * i + 3]) + b1, a.act));
+                            h[2 * i] = cl_pack2<BF16>(fminf(fmaxf(__uint_as_float(v[4 * i]) + b0, act_lo), act_hi),
+                                                      fminf(fmaxf(__uint_as_float(v[4 * i + 1]) + b0, act_lo), act_hi));
+                            h[2 * i + 1] = cl_pack2<BF16>(fminf(fmaxf(__uint_as_float(v[4 * i + 2]) + b1, act_lo), act_hi),
+                                                          fminf(fmaxf(__uint_as_float(v[4 * i + 3]) + b1, act_lo), act_hi));
                         }
                         __syncwarp();
                         ptx::stsm_x4_trans(st_addr, h[0], h[1], h[2], h[3]);            // positions 0..15
@@ -517,17 +537,60 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         for (int k = 0; k < 2; ++k) {
                             const int piece = k * 32 + lane;
                             const int pos = piece >> 1, half = piece & 1;
-                            const int m = m0 + chunk * 32 + pos;
-                            const int oh = m / a.P, c = m % a.P;
+                            const int cc = c00 + chunk * 32 + pos;
+                            const int dr = __float2int_rz(((float)cc + 0.5f) * inv_p);
+                            const int oh = oh0 + dr, c = cc - dr * a.P;
                             const int ow = ow0 + c;
-                            const int co = tc.nt * 64 + q * 16 + half * 8;
+                            const int co = q * 16 + half * 8;
                             if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
                                 !(a.sub2 && ((oh | ow) & 1))) {
                                 const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
                                 const uint4 val = *reinterpret_cast<const uint4*>(wstp + pos * 32 + half * 16);
-                                const size_t off =
-                                    ((((size_t)n * a.dout + t) * a.yH + yh) * a.yW + yw) * (size_t)a.C_out + co;
-                                *reinterpret_cast<uint4*>(y + off) = val;
+                                *reinterpret_cast<uint4*>(yf + ((size_t)yh * a.yW + yw) * a.C_out + co) = val;
+                            }
+                        }
+                    };
+                    uint32_t ra[4][16], rb[4][16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ptx::tmem_ld16x256b_x4(tq + (uint32_t)(c * 32), ra[c]);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ptx::tmem_ld16x256b_x4(tq + (uint32_t)((4 + c) * 32), rb[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) process(c, ra[c]);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) process(4 + c, rb[c]);
+                } else if (CTR) {
+                    // Temporal pass of the split head: accumulator row r = (i*3+j)*12 + c goes to plane
+                    // p = i*3+j of G at channel c. Each warp stages its 32 rows x 32 positions as
+                    // [position][row] fp32, then writes 4-row groups (16 bytes of fp32 or 8 of bf16;
+                    // quarter boundaries fall on 4-channel steps of a plane) for 32 positions at a time.
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * kStageWarpBytes);  // [32][kGPitch]
+                    const long long hw = (long long)a.H_out * a.W_out;
+                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
+                        ptx::tmem_ld_wait();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) S[j * kGPitch + lane] = __uint_as_float(v[j]);
+                        __syncwarp();
+                        const long long pos = (long long)m0 + chunk * 32 + lane;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int r0 = q * 32 + 4 * k;
+                            if (r0 < 108 && pos < hw) {
+                                const float4 f = *reinterpret_cast<const float4*>(S + lane * kGPitch + 4 * k);
+                                const long long e = (((long long)tc.fr * 9 + r0 / 12) * hw + pos) * 12 + r0 % 12;
+                                if (a.g_f32) {
+                                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + e) = f;
+                                } else {
+                                    uint2 b;
+                                    b.x = cl_pack2<true>(f.x, f.y);
+                                    b.y = cl_pack2<true>(f.z, f.w);
+                                    *reinterpret_cast<uint2*>(y + e) = b;
+                                }
                             }
                         }
                     }
@@ -705,7 +768,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     }
     // the conv_out head (12 channels to unpatchified RGB) runs in the kw-folded form
     g.kwm = d.unpatchify2x2 ? 1 : 0;
-    g.ctr = (d.kernel == X3_KERNEL_HEAD_TWO_PASS) ? 1 : 0;
+    g.ctr = (d.kernel == X3_KERNEL_HEAD_TWO_PASS || d.kernel == X3_KERNEL_HEAD_SPLIT) ? 1 : 0;
     if (g.ctr) {
         // temporal pass of the two-pass head: 12 output channels x 9 spatial taps = 108 (112) channels
         if (!d.unpatchify2x2 || d.dims != 3 || d.layout != X3_NDHWC || d.dtype != X3_BF16) return false;
@@ -730,7 +793,20 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // resident in shared memory; if no tiling leaves room for them, the 128-row form
     g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
     if (g.m64) g.n_tiles = 1;
-  for (int attempt = 0; attempt < 2 && !found; ++attempt) {
+    if (g.ctr) {
+        // the centre tap needs no halo: a window is 256 consecutive positions of a frame's flattened
+        // H x W plane (one strip as wide as the image, rows of pitch W), staged by one 32 KB box
+        g.Wt = g.P = W_out; g.HR = 1; g.strips = 1;
+        g.windows = (int)(((long long)H_out * W_out + kBNP - 1) / kBNP);
+        g.h_bytes = g.h_tx_bytes = kBNP * kCK * 2;
+        g.n_h = 4; g.n_w = 4;
+        g.w_smem = g.n_w * kWBlock;
+        g.smem_bytes = fixed + g.n_h * g.h_bytes + g.w_smem;
+        if (g.smem_bytes > kSmemLimit) return false;
+        g.tiles = (long long)g.windows * g.frames;
+        found = true;
+    }
+  for (int attempt = 0; attempt < 2 && !found && !g.ctr; ++attempt) {
     if (attempt == 1) {
         if (!g.m64) break;
         g.m64 = 0;
@@ -806,6 +882,8 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.C_in = d.C_in; a.C_out = d.C_out; a.N = d.N; a.D = d.D; a.H = d.H; a.W = d.W;
     a.H_out = H_out; a.W_out = W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
     a.sub2 = g.sub2; a.out_nchw = out_nchw; a.yH = yH; a.yW = yW; a.w_smem = g.w_smem;
+    a.frame_inner = g.ctr;
+    a.g_f32 = d.kernel == X3_KERNEL_HEAD_SPLIT ? 1 : 0;
     a.has_carry = carry != nullptr;
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
@@ -824,10 +902,13 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         mc = mx;
     } else {
         const uint64_t frames_x = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
-        st = encode_sw128(&mx, bf16, x, d.C_in, d.W, d.H, frames_x, (uint32_t)g.P, (uint32_t)g.HR);
+        // the flat form views each frame as one row of H*W positions
+        const uint64_t mw = g.ctr ? (uint64_t)d.H * d.W : (uint64_t)d.W, mh = g.ctr ? 1 : (uint64_t)d.H;
+        const uint32_t bw = g.ctr ? (uint32_t)kBNP : (uint32_t)g.P, bh = g.ctr ? 1u : (uint32_t)g.HR;
+        st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh);
         if (st != X3_OK) return st;
         if (carry) {
-            st = encode_sw128(&mc, bf16, carry, d.C_in, d.W, d.H, (uint64_t)d.N * 2, (uint32_t)g.P, (uint32_t)g.HR);
+            st = encode_sw128(&mc, bf16, carry, d.C_in, mw, mh, (uint64_t)d.N * 2, bw, bh);
             if (st != X3_OK) return st;
         } else {
             mc = mx;
