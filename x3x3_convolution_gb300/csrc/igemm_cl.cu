@@ -28,7 +28,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stdlib.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -98,6 +101,14 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long t) {
     return c;
 }
 
+// Tile of this CTA at iteration k. With weight multicast (MC) the two CTAs of a cluster take the two
+// tiles of a pair, so both walk the same number of iterations and stream the same weight blocks; the
+// second tile of the last pair can lie past the end (a phantom iteration: weight blocks only).
+__device__ __forceinline__ long long cl_tile_of(long long k, bool mc, uint32_t rank) {
+    if (!mc) return (long long)blockIdx.x + k * gridDim.x;
+    return 2 * ((long long)(blockIdx.x >> 1) + k * (gridDim.x >> 1)) + rank;
+}
+
 __device__ __forceinline__ bool cl_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
@@ -156,7 +167,11 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // M64 (layers with at most 64 output channels): MMAs of M = 64, whose accumulator rows 16q..16q+15
 // sit in TMEM lanes 32q..32q+15; every weight block of the layer stays resident in shared memory
 // (loaded once per CTA), so a tile only streams its halo.
-template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false>
+// MC (one 128-channel output tile): the kernel runs as clusters of two CTAs that stream the same
+// weight blocks; each block is fetched once from L2 by one of the two (alternating) and multicast into
+// both CTAs' ring stage, and a stage is refilled only after the MMAs of both CTAs have read it (each
+// MMA issuer's commit arrives on the stage's empty barrier in both CTAs).
+template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -199,7 +214,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         }
         for (int i = 0; i < a.n_w; ++i) {
             ptx::mbar_init(bar_w_full + 8 * i, 1);
-            ptx::mbar_init(bar_w_empty + 8 * i, 1);
+            ptx::mbar_init(bar_w_empty + 8 * i, MC ? 2 : 1);  // MC: the MMAs of both CTAs
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_acc_full + 8 * i, 1);
@@ -220,7 +235,19 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if (MC) ptx::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
     const uint32_t tmem_base = *tmem_slot;
+    const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
+    // K order of this CTA. In the head form (kw folded into M: few, small weight blocks per tile) each
+    // CTA walks its (kt, chunk) groups and the kh taps inside a group from a CTA-dependent starting
+    // point, so the CTAs, which run in near lockstep, fetch different weight blocks at any moment
+    // instead of all asking L2 for the same one (measured: 15 % faster there; the other forms run
+    // slower with it, so they keep the natural order). Both CTAs of a cluster share one order. Only
+    // the fp32 summation order depends on it.
+    constexpr int kTapsK = KWM ? 3 : (CTR ? 1 : 9);
+    const int n_groups = a.KT * a.n_chunks;
+    const int k_id = KWM ? (int)(MC ? blockIdx.x >> 1 : blockIdx.x) : 0;
+    const int rot_g = k_id % n_groups, rot_t = (k_id / n_groups) % kTapsK;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -234,12 +261,24 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     ptx::bulk_load(sW + (uint32_t)(b * kWBlock64), a.w + (size_t)b * kWBlock64, (uint32_t)kWBlock64, bar_w_full);
                 w_cnt = 1;
             }
-            for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
-                const ClTile tc = cl_decode(a, tile);
+            for (long long k = 0; ok; ++k) {
+                const long long tile = cl_tile_of(k, MC, rank);
+                if (tile - (long long)rank >= a.tiles) break;
+                const bool real = tile < a.tiles;
+                const ClTile tc = cl_decode(a, real ? tile : 0);
                 const int n = tc.fr / a.dout, t = tc.fr % a.dout;
                 const int r0 = (tc.win * a.win_adv) / a.P;
                 const int ow0 = tc.strip * a.Wt;
-                for (int kt = 0; kt < a.KT && ok; ++kt) {
+                for (int gi = 0; gi < n_groups && ok; ++gi) {
+                    int kt, cc;
+                    if (KWM) {
+                        const int gg = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
+                        kt = gg / a.n_chunks;
+                        cc = gg - kt * a.n_chunks;
+                    } else {
+                        kt = gi / a.n_chunks;
+                        cc = gi - kt * a.n_chunks;
+                    }
                     const void* map = &tm_x;
                     int fcoord;
                     if (a.KT == 3) {
@@ -250,7 +289,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     } else {
                         fcoord = n;
                     }
-                    for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                    {
                         if (NC) {
                             // raw NCHW slices of 16 channels for the transposers (aligned 8 columns left)
                             const int nsc = (min(a.C_in - cc * kCK, kCK) + 15) / 16;
@@ -263,7 +302,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 ++r_cnt;
                             }
                             if (!ok) break;
-                        } else {
+                        } else if (real) {
                             const uint32_t sh = h_cnt % a.n_h;
                             if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
@@ -273,15 +312,19 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
-                        constexpr int kTaps = KWM ? 3 : (CTR ? 1 : 9);
                         const uint8_t* wblk =
-                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTaps) * (size_t)kWBlock;
-                        for (int tap = 0; tap < (M64 ? 0 : kTaps); ++tap) {
+                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
+                        for (int ti = 0; ti < (M64 ? 0 : kTapsK); ++ti) {
+                            const int tap = KWM ? (ti + rot_t < kTapsK ? ti + rot_t : ti + rot_t - kTapsK) : ti;
                             const uint32_t sw = w_cnt % a.n_w;
                             if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
-                            ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
-                                           bar_w_full + 8 * sw);
+                            if (!MC)
+                                ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
+                                               bar_w_full + 8 * sw);
+                            else if ((w_cnt & 1u) == rank)  // alternate blocks, into both CTAs
+                                ptx::bulk_load_multicast(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock,
+                                                         (uint32_t)kWBlock, bar_w_full + 8 * sw, (uint16_t)3);
                             ++w_cnt;
                         }
                     }
@@ -325,7 +368,21 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             // 128-byte rows (a spatial tap) or by 32-byte K steps needs no base-offset correction;
             // the integer-exact parity tests pin this.
             const uint32_t b_hi_fixed = (1024u >> 4) | (1u << 14) | (2u << 29);
-            for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x, ++it) {
+            for (long long k = 0; ok; ++k) {
+                const long long tile = cl_tile_of(k, MC, rank);
+                if (tile - (long long)rank >= a.tiles) break;
+                if (MC && tile >= a.tiles) {
+                    // phantom iteration: take the pair's weight blocks through the ring (the peer's
+                    // producer waits for this CTA's arrivals on every stage it refills)
+                    for (int b = 0; b < n_groups * kTapsK && ok; ++b) {
+                        const uint32_t sw = w_cnt % a.n_w;
+                        if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
+                        ++w_cnt;
+                    }
+                    continue;
+                }
                 const ClTile tc = cl_decode(a, tile);
                 const int pos_off = (tc.win * a.win_adv) % a.P;
                 const uint32_t ab = it & 1u;
@@ -333,49 +390,78 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + ab * (uint32_t)kBNP;
                 uint32_t acc = 0;
-                for (int kt = 0; kt < a.KT && ok; ++kt) {
-                    for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
-                        const uint32_t sh = h_cnt % a.n_h;
-                        if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) { ok = false; break; }
+                // the MMAs of one tap: four K steps of 16 channels into the tile's accumulator
+                auto tap_mmas = [&](int cc, int kt, int kh, int kw, uint32_t hbase) -> bool {
+                    const uint32_t sw = w_cnt % a.n_w;
+                    uint32_t a_lo;
+                    if (M64) {
+                        a_lo = a_lo0 + (uint32_t)(((kt * a.n_chunks + cc) * 9 + kh * 3 + kw) * (kWBlock64 >> 4));
+                    } else {
+                        if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) return false;
                         ptx::tc_fence_after();
-                        const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
-                        for (int kh = (CTR ? 1 : 0); kh < (CTR ? 2 : 3) && ok; ++kh) {
-                            for (int kw = (CTR ? 1 : 0); kw < (KWM ? 1 : (CTR ? 2 : 3)); ++kw) {
-                                const uint32_t sw = w_cnt % a.n_w;
-                                uint32_t a_lo;
-                                if (M64) {
-                                    a_lo = a_lo0 + (uint32_t)(((kt * a.n_chunks + cc) * 9 + kh * 3 + kw) * (kWBlock64 >> 4));
-                                } else {
-                                    if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
-                                    ptx::tc_fence_after();
-                                    a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
-                                }
-                                const uint32_t row_addr = CTR ? hbase : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
-                                const uint32_t b_hi = b_hi_fixed;
+                        a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
+                    }
+                    const uint32_t row_addr = CTR ? hbase : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
 #pragma unroll
-                                for (int ks = 0; ks < kCK / 16; ++ks) {
-                                    if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
-                                    const uint64_t adesc = ((uint64_t)a_hi << 32) |
-                                                           (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kRows * 16) >> 4));
-                                    const uint32_t baddr = row_addr + (uint32_t)ks * 32u;
-                                    const uint64_t bdesc = ((uint64_t)b_hi << 32) |
-                                                           (uint64_t)(((baddr >> 4) & 0x3FFFu) | (1u << 16));
-                                    ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
-                                    acc = 1;
-                                }
-                                if (!M64) {
-                                    ptx::mma_commit(bar_w_empty + 8 * sw);
-                                    ++w_cnt;
-                                }
-                            }
+                    for (int ks = 0; ks < kCK / 16; ++ks) {
+                        if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
+                        const uint64_t adesc = ((uint64_t)a_hi << 32) |
+                                               (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kRows * 16) >> 4));
+                        const uint32_t baddr = row_addr + (uint32_t)ks * 32u;
+                        const uint64_t bdesc = ((uint64_t)b_hi_fixed << 32) |
+                                               (uint64_t)(((baddr >> 4) & 0x3FFFu) | (1u << 16));
+                        ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
+                        acc = 1;
+                    }
+                    if (!M64) {
+                        if (MC) ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
+                        else ptx::mma_commit(bar_w_empty + 8 * sw);
+                        ++w_cnt;
+                    }
+                    return true;
+                };
+                auto group_begin = [&](uint32_t& sh, uint32_t& hbase) -> bool {
+                    sh = h_cnt % a.n_h;
+                    if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) return false;
+                    ptx::tc_fence_after();
+                    hbase = sH + sh * (uint32_t)a.h_bytes;
+                    return true;
+                };
+                if constexpr (KWM) {
+                    // head form: rotated (kt, chunk) groups, rotated kh taps (kw is folded into M)
+                    for (int gi = 0; gi < n_groups && ok; ++gi) {
+                        const int gg = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
+                        const int kt = gg / a.n_chunks, cc = gg - kt * a.n_chunks;
+                        uint32_t sh, hbase;
+                        if (!group_begin(sh, hbase)) { ok = false; break; }
+#pragma unroll
+                        for (int ti = 0; ti < 3; ++ti) {
+                            const int kh = ti + rot_t < 3 ? ti + rot_t : ti + rot_t - 3;
+                            if (ok && !tap_mmas(cc, kt, kh, 0, hbase)) ok = false;
                         }
                         if (!ok) break;
                         ptx::mma_commit(bar_h_empty + 8 * sh);
                         ++h_cnt;
                     }
+                } else {
+                    for (int kt = 0; kt < a.KT && ok; ++kt) {
+                        for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                            uint32_t sh, hbase;
+                            if (!group_begin(sh, hbase)) { ok = false; break; }
+                            for (int kh = (CTR ? 1 : 0); kh < (CTR ? 2 : 3) && ok; ++kh) {
+                                for (int kw = (CTR ? 1 : 0); kw < (CTR ? 2 : 3); ++kw) {
+                                    if (!tap_mmas(cc, kt, kh, kw, hbase)) { ok = false; break; }
+                                }
+                            }
+                            if (!ok) break;
+                            ptx::mma_commit(bar_h_empty + 8 * sh);
+                            ++h_cnt;
+                        }
+                    }
                 }
                 if (!ok) break;
                 ptx::mma_commit(bar_acc_full + 8 * ab);
+                ++it;
             }
             ptx::mma_commit(bar_drain);
             volatile int dummy = 0;
@@ -412,7 +498,9 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         const float act_lo = a.act == X3_ACT_RELU ? 0.0f : (a.act == X3_ACT_CLAMP1 ? -1.0f : -INFINITY);
         const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
         const float inv_p = 1.0f / (float)a.P;
-        for (long long tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++it) {
+        for (long long k = 0;; ++k, ++it) {
+            const long long tile = cl_tile_of(k, MC, rank);
+            if (tile >= a.tiles) break;
             const uint32_t ab = it & 1u;
             if (!cl_wait(bar_acc_full + 8 * ab, (it >> 1) & 1u, abort_flag, a.status)) break;
             ptx::tc_fence_after();
@@ -641,7 +729,9 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         uint32_t h_cnt = 0, r_cnt = 0;
         bool ok = true;
         for (long long tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
-            for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+            for (int gi = 0; gi < n_groups && ok; ++gi) {
+                // the producer's chunk order (2D: one temporal tap, so a group is a chunk)
+                const int cc = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
                 const uint32_t sh = h_cnt % a.n_h;
                 if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                 const uint32_t hst = sH + sh * (uint32_t)a.h_bytes;
@@ -694,6 +784,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem_base, 512u);
+    if (MC) ptx::cluster_sync();  // no multicast copy or commit still targets this CTA's shared memory
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -862,6 +953,11 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
   }
     if (!found) return false;
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
+    // one output tile and streamed weights: pairs of CTAs can share the weight stream (the launcher
+    // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
+    // the weights measured no faster on any layer of the decoder (each SM still receives every block).
+    const char* cl_env = getenv("X3CONV_CLUSTER");
+    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
@@ -871,6 +967,44 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
 }
 
 namespace {
+
+// Clusters of two CTAs of kernel `func` (with `smem` bytes of dynamic shared memory each) that can be
+// resident at once on the current device; cached per kernel, size and device.
+x3_status active_pairs(const void* func, int smem, int* out) {
+    struct Entry { const void* f; int smem, dev, n; };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int n_cache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return fail(X3_ERR_CUDA, "cudaGetDevice failed"); }
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cache; ++i)
+            if (cache[i].f == func && cache[i].smem == smem && cache[i].dev == dev) { *out = cache[i].n; return X3_OK; }
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
+    if (e != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return fail(X3_ERR_CUDA, "no cluster of two CTAs fits (%s)", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (n_cache < 32) cache[n_cache++] = Entry{func, smem, dev, n};
+    *out = n;
+    return X3_OK;
+}
 
 // One launch of the engine for descriptor d (its layout, C_in and stride as the kernel sees them)
 // with tiling g over an H_out x W_out raster; the stored plane is yH x yW.
@@ -915,6 +1049,34 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         }
     }
     void (*k)(CUtensorMap, CUtensorMap, ClArgs);
+    if (g.mc) {
+        if (g.ctr) k = igemm_cl_kernel<true, false, false, true, false, true>;
+        else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false, false, false, true> : igemm_cl_kernel<false, true, false, false, false, true>;
+        else k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true> : igemm_cl_kernel<false, false, false, false, false, true>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
+        int clusters = 0;
+        x3_status st2 = active_pairs((const void*)k, g.smem_bytes, &clusters);
+        if (st2 != X3_OK) return st2;
+        const long long pairs = (g.tiles + 1) / 2;
+        if (clusters > pairs) clusters = (int)pairs;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3((unsigned)(2 * clusters));
+        cfg.blockDim = dim3(192);
+        cfg.dynamicSmemBytes = (size_t)g.smem_bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k, mx, mc, a);
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl cluster launch: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
     if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
     else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
     else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;

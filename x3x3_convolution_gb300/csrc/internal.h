@@ -72,6 +72,7 @@ struct ClGeom {
     int sub2;                    // 1: stride 2 computed as the stride-1 raster, even positions kept
     int m64;                     // 1: M = 64 MMAs (at most 64 output channels), weights resident
     int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
+    int mc;                      // 1: clusters of two CTAs sharing each weight block by multicast
     long long tiles;
     int smem_bytes, grid;
 };
