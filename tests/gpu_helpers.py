@@ -2,7 +2,8 @@
 
 Tolerances on random data: max|d| <= 1.5e-2 * max|ref| and rms(d) <= 4e-3 * rms(ref) against the
 oracle's fp32 result; on integer-valued data the result must equal the oracle's value rounded
-once to the storage type. Decoded outputs of the head: PSNR >= 55 dB over the [-1,1] range.
+once to the storage type. Decoded outputs of the head: PSNR >= 55 dB over the [-1,1] range and
+SSIM >= 0.998 (tests/ssim.py).
 """
 import numpy as np
 import torch
@@ -12,6 +13,7 @@ import oracle
 MAX_TOL = 1.5e-2
 RMS_TOL = 4e-3
 PSNR_MIN = 55.0
+SSIM_MIN = 0.998
 
 
 def dev(t):

@@ -17,7 +17,8 @@ import torch
 import oracle
 import x3x3_convolution_gb300 as x3
 from x3x3_convolution_gb300 import synth
-from tests.gpu_helpers import (PSNR_MIN, assert_close, assert_exact, crops_3d, dev, host_values, psnr,
+from tests.ssim import ssim_rgb
+from tests.gpu_helpers import (PSNR_MIN, SSIM_MIN, assert_close, assert_exact, crops_3d, dev, host_values, psnr,
                                sample_positions)
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +67,8 @@ def test_two_pass_head(variant, shape):
         exact = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp",
                                             layout="NDHWC"))
         assert psnr(got, exact) >= PSNR_MIN
+        if min(2 * H, 2 * W) >= 11:
+            assert ssim_rgb(got, exact) >= SSIM_MIN
 
 
 def test_two_pass_head_without_carry_and_batch():
@@ -105,6 +108,8 @@ def test_split_head(variant, shape):
     else:
         assert_close(got, ref)
         assert psnr(got, ref) >= PSNR_MIN
+        if min(2 * H, 2 * W) >= 11:
+            assert ssim_rgb(got, ref) >= SSIM_MIN
         split = to_rgb(oracle.head_two_pass(x.vals, L.w.vals, L.b.vals, carry=carry.vals, round_g=False,
                                             layout="NDHWC"))
         assert_close(got, split)
@@ -122,3 +127,20 @@ def test_split_head_full_size_sampled():
     ref = to_rgb(y[:, None, None, None, :])[:, 0]
     g = np.stack([got[0, t, 2 * h:2 * h + 2, 2 * w:2 * w + 2] for (t, h, w) in pos])
     assert_close(g, ref)
+
+
+@pytest.mark.parametrize("kernel", ["head_split", "auto"])
+def test_head_full_size_decoded_quality(kernel):
+    """All 4 decoded 704x1248 RGB frames of the full-size head against the oracle's head computed in
+    full: PSNR and SSIM (the second quality metric) of the decoded output, plus the tolerance."""
+    x, carry, L = synth.head(seed=3970)
+    N, D, H, W, C = x.shape
+    d = x3.make_desc(3, N, C, 12, H, W, D=D, act="clamp", unpatchify2x2=True, kernel=kernel)
+    conv = x3.Conv(d, dev(L.w), dev(L.b))
+    got = host_values(conv(dev(x), dev(carry)), "bf16")
+    torch.cuda.synchronize()
+    ref = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp", layout="NDHWC"))
+    assert got.shape == ref.shape == (1, 4, 704, 1248, 3)
+    assert_close(got, ref)
+    assert psnr(got, ref) >= PSNR_MIN
+    assert ssim_rgb(got, ref) >= SSIM_MIN

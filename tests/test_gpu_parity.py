@@ -12,8 +12,9 @@ import torch
 import oracle
 import x3x3_convolution_gb300 as x3
 from x3x3_convolution_gb300 import synth
+from tests.ssim import ssim_rgb
 from tests.gpu_helpers import (assert_close, assert_exact, dev, host_values, oracle_sampled_3d, psnr,
-                               sample_positions, PSNR_MIN)
+                               sample_positions, PSNR_MIN, SSIM_MIN)
 
 pytestmark = pytest.mark.gpu
 
@@ -79,18 +80,24 @@ def test_conv2d_nchw(case, variant, kernel):
 
 
 @pytest.mark.parametrize("variant", ["int", "random"])
-@pytest.mark.parametrize("case", [(2, 16, 32, 20, 150, "relu"), (1, 64, 64, 9, 300, "none"),
-                                  (1, 8, 16, 3, 5, "none")], ids=str)
-def test_conv2d_nhwc_bf16(case, variant):
-    N, Ci, Co, H, W, act = case
-    key = 2100 + sum(case[:5])
-    x = synth.activation([key, 0], (N, H, W, Ci), "bf16", variant, ("uniform", -1.0, 1.0))
-    L = synth.make_layer([key], 2, Ci, Co, "bf16", act=act, variant=variant)
+@pytest.mark.parametrize("case", [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"),
+                                  (1, 8, 16, 3, 5, 1, "none"), (2, 64, 64, 34, 72, 2, "relu"),
+                                  (1, 40, 24, 17, 33, 2, "none"), (2, 64, 128, 33, 97, 1, "relu"),
+                                  (1, 128, 64, 12, 130, 1, "relu")], ids=str)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_conv2d_nhwc(case, variant, dtype):
+    """Channels-last 2D layers on the swapped engine: the M = 64 form (C_out <= 64, weights resident
+    when they fit), the 128-row form, and stride 2 as the stride-1 raster with even positions kept."""
+    N, Ci, Co, H, W, s, act = case
+    key = 2100 + sum(case[:6])
+    x = synth.activation([key, 0], (N, H, W, Ci), dtype, variant, ("uniform", -1.0, 1.0))
+    L = synth.make_layer([key], 2, Ci, Co, dtype, stride=s, act=act, variant=variant)
     got, conv = run2d(x, L, layout="NHWC")
-    assert conv.kernel_name.startswith("igemm_tcgen05")
+    g = x3.conv_plan_describe(conv.plan)
+    assert g["kernel"] == "igemm_tcgen05_sw128" and g["sub2"] == (s == 2) and g["m64"] == (Co <= 64 and Ci <= 64)
     ref = oracle2d(x, L, layout="NHWC")
     if variant == "int":
-        assert_exact(got, ref, "bf16")
+        assert_exact(got, ref, dtype)
     else:
         assert_close(got, ref)
 
@@ -168,6 +175,8 @@ def test_head_clamp_unpatchify(variant, shape):
     else:
         assert_close(got, ref)
         assert psnr(got, ref) >= PSNR_MIN
+        if min(2 * H, 2 * W) >= 11:
+            assert ssim_rgb(got, ref) >= SSIM_MIN
 
 
 # ------------------------------------------------------------------ full sizes, sampled

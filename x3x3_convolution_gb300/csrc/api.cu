@@ -124,7 +124,25 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         *plan = p;
         return X3_OK;
     }
-    if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) cl_ok = igemm_cl_plan(p, p->num_sms);
+    if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) {
+        // 2D channels-last layers of any width run on the swapped engine (the M = 64 form for at most
+        // 64 output channels); stride 2 as the stride-1 raster with even positions kept
+        const bool nhwc2d = p->d.dims == 2 && p->d.layout == X3_NHWC;
+        if (nhwc2d && p->d.stride == 2) {
+            x3_conv_plan q = *p;
+            q.d.stride = 1;
+            q.H_out = q.d.H;
+            q.W_out = q.d.W;
+            if (igemm_cl_plan(&q, p->num_sms, true)) {
+                p->cl = q.cl;
+                p->cl.sub2 = 1;
+                p->g = q.g;
+                cl_ok = true;
+            }
+        } else {
+            cl_ok = igemm_cl_plan(p, p->num_sms, nhwc2d);
+        }
+    }
     if (choice != X3_KERNEL_DIRECT && !cl_ok) igemm_ok = igemm_plan(p, p->num_sms);
     if (choice == X3_KERNEL_IGEMM && !igemm_ok && !cl_ok) {
         delete p;
@@ -132,7 +150,8 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
     }
     if (cl_ok) {
         p->kind = K_IGEMM_CL;
-        p->packed_bytes = (size_t)p->cl.n_tiles * p->cl.KT * p->cl.n_chunks * (p->cl.kwm ? 3 : 9) * (128 * 64 * 2);
+        p->packed_bytes = (size_t)p->cl.n_tiles * p->cl.KT * p->cl.n_chunks * (p->cl.kwm ? 3 : 9) *
+                          ((p->cl.m64 ? 64 : 128) * 64 * 2);
     } else if (igemm_ok) {
         p->kind = K_IGEMM;
         const IgemmGeom& g = p->g;
@@ -193,10 +212,11 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"BM\": 128, \"BN\": 256, \"CK\": 64, \"n_tiles\": %d, \"n_chunks\": %d, \"KT\": %d, "
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
-                        "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, \"mc\": %d}",
+                        "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, \"mc\": %d, "
+                        "\"m64\": %d, \"sub2\": %d, \"ctr\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.mc);
+                        c.mc, c.m64, c.sub2, c.ctr);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",

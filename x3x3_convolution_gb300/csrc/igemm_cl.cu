@@ -961,8 +961,8 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
-    p->g.BN = kBM; p->g.CK = kCK; p->g.n_chunks = g.n_chunks; p->g.n_tiles = g.n_tiles; p->g.KT = g.KT;
-    p->g.b_bytes = kWBlock;
+    p->g.BN = g.m64 ? 64 : kBM; p->g.CK = kCK; p->g.n_chunks = g.n_chunks; p->g.n_tiles = g.n_tiles; p->g.KT = g.KT;
+    p->g.b_bytes = g.m64 ? kWBlock64 : kWBlock;
     return true;
 }
 
@@ -1094,7 +1094,9 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
 
 x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                           const void* bias, void* y, cudaStream_t s) {
-    return launch_cl(p->d, p->cl, p->H_out, p->W_out, p->H_out, p->W_out, 0, x, carry, w_packed, bias, y, s);
+    // stride 2 as sub2: the raster covers the input plane, the stored plane is the output
+    const int rh = p->cl.sub2 ? p->d.H : p->H_out, rw = p->cl.sub2 ? p->d.W : p->W_out;
+    return launch_cl(p->d, p->cl, rh, rw, p->H_out, p->W_out, 0, x, carry, w_packed, bias, y, s);
 }
 
 x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const void* w_packed, const void* bias,
