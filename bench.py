@@ -190,6 +190,19 @@ class Workload:
     def outputs(self):
         return [self.taesd_y, self.stack_y, self.l3_y, self.head_y]
 
+    def stage(self, i, stream):
+        """Stage i of the step alone (0 taesd, 1 stack, 2 l3, 3 head)."""
+        if i == 0:
+            self.taesd(self.taesd_x, out=self.taesd_y, stream=stream)
+        elif i == 1:
+            self.stack(self.stack_x, carries=self.stack_carries, carry_valid=self.carry_valid, out=self.stack_y,
+                       stream=stream)
+            self.carry_valid = True
+        elif i == 2:
+            self.l3(self.l3_x, self.l3_c, out=self.l3_y, stream=stream)
+        else:
+            self.head(self.head_x, self.head_c, out=self.head_y, stream=stream)
+
     def step(self, stream, ev=None):
         """One decoder pass; ev: optional 5 CUDA events recorded between the stages."""
         if ev:
@@ -403,24 +416,53 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        # end to end through host buffers: H2D of the step's inputs from pinned memory, the step,
-        # D2H of its outputs, all inside the timed region
+        # end to end through host buffers: every step copies each stage's input in from pinned host
+        # memory and its output back out, inside the timed region. The copies run on their own
+        # streams (one per direction) so that a stage's input transfer overlaps the previous stage's
+        # kernels; events order each stage after its input and each buffer's reuse after its last
+        # reader.
         hin = [t.cpu().pin_memory() for t in wl.inputs()]
         hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in wl.outputs()]
         h2d = sum(t.numel() * t.element_size() for t in hin)
         d2h = sum(t.numel() * t.element_size() for t in hout)
+        din, dout = wl.inputs(), wl.outputs()
+        copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         n_e2e = max(3, min(args.steps, 10))
+        done_prev, out_prev = [None] * 4, [None] * 4
         barrier(world)
         e0.record(stream)
+        copy_in.wait_stream(stream)
+        copy_out.wait_stream(stream)
         for _ in range(n_e2e):
-            for h, d in zip(hin, wl.inputs()):
-                d.copy_(h, non_blocking=True)
-            wl.step(stream)
-            for h, d in zip(hout, wl.outputs()):
-                h.copy_(d, non_blocking=True)
+            ev_in = []
+            for i in range(4):
+                if done_prev[i] is not None:
+                    copy_in.wait_event(done_prev[i])       # the previous step's stage i has read its input
+                with torch.cuda.stream(copy_in):
+                    din[i].copy_(hin[i], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_in)
+                ev_in.append(ev)
+            for i in range(4):
+                stream.wait_event(ev_in[i])
+                if out_prev[i] is not None:
+                    stream.wait_event(out_prev[i])         # the previous step's output i is copied out
+                wl.stage(i, stream)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                done_prev[i] = ev
+            for i in range(4):
+                copy_out.wait_event(done_prev[i])
+                with torch.cuda.stream(copy_out):
+                    hout[i].copy_(dout[i], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_out)
+                out_prev[i] = ev
+        stream.wait_stream(copy_in)
+        stream.wait_stream(copy_out)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max(world, e0.elapsed_time(e1)) / n_e2e

@@ -47,6 +47,7 @@ constexpr int kBNP = 256;       // positions per tile (MMA N)
 constexpr int kCK = 64;         // input channels per staged chunk (one 128-byte swizzle row)
 constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one tap, one chunk)
 constexpr int kWBlock64 = 64 * kCK * 2; // the same for the M = 64 form
+constexpr int kCtrW = kBNP * kCK * 2;    // centre-tap form: offset of the weight block in a stage
 constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
@@ -306,15 +307,20 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             const uint32_t sh = h_cnt % a.n_h;
                             if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
-                            if (CTR)  // 256 consecutive positions of the frame's flattened plane
+                            if (CTR) {
+                                // 256 consecutive positions of the frame's flattened plane and the
+                                // (kt, chunk) weight block, one stage and one barrier for both
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
-                            else
+                                ptx::bulk_load(sH + sh * a.h_bytes + (uint32_t)kCtrW,
+                                               a.w + ((size_t)kt * a.n_chunks + cc) * (size_t)kWBlock, (uint32_t)kWBlock,
+                                               bar_h_full + 8 * sh);
+                            } else
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
-                        for (int ti = 0; ti < (M64 ? 0 : kTapsK); ++ti) {
+                        for (int ti = 0; ti < ((M64 || CTR) ? 0 : kTapsK); ++ti) {
                             const int tap = KWM ? (ti + rot_t < kTapsK ? ti + rot_t : ti + rot_t - kTapsK) : ti;
                             const uint32_t sw = w_cnt % a.n_w;
                             if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
@@ -396,6 +402,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     uint32_t a_lo;
                     if (M64) {
                         a_lo = a_lo0 + (uint32_t)(((kt * a.n_chunks + cc) * 9 + kh * 3 + kw) * (kWBlock64 >> 4));
+                    } else if (CTR) {  // the weight block shares the stage (and its barrier) with the window
+                        a_lo = (((hbase + (uint32_t)kCtrW) >> 4) & 0x3FFFu) | ((uint32_t)((kBM * 16) >> 4) << 16);
                     } else {
                         if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) return false;
                         ptx::tc_fence_after();
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
                         acc = 1;
                     }
-                    if (!M64) {
+                    if (!M64 && !CTR) {
                         if (MC) ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
                         else ptx::mma_commit(bar_w_empty + 8 * sw);
                         ++w_cnt;
@@ -889,9 +897,10 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         // H x W plane (one strip as wide as the image, rows of pitch W), staged by one 32 KB box
         g.Wt = g.P = W_out; g.HR = 1; g.strips = 1;
         g.windows = (int)(((long long)H_out * W_out + kBNP - 1) / kBNP);
-        g.h_bytes = g.h_tx_bytes = kBNP * kCK * 2;
-        g.n_h = 4; g.n_w = 4;
-        g.w_smem = g.n_w * kWBlock;
+        // each stage holds the window (32 KB) and the (kt, chunk) weight block (16 KB) behind one barrier
+        g.h_bytes = g.h_tx_bytes = kCtrW + kWBlock;
+        g.n_h = 4; g.n_w = 1;
+        g.w_smem = 0;
         g.smem_bytes = fixed + g.n_h * g.h_bytes + g.w_smem;
         if (g.smem_bytes > kSmemLimit) return false;
         g.tiles = (long long)g.windows * g.frames;
@@ -957,7 +966,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
     // the weights measured no faster on any layer of the decoder (each SM still receives every block).
     const char* cl_env = getenv("X3CONV_CLUSTER");
-    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
+    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
