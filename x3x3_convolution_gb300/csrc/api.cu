@@ -242,9 +242,9 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
         const ClGeom& c = plan->cl_shadow;
         const int m = snprintf(tmp + n - 1, sizeof tmp - (size_t)(n - 1),
                                ", \"shadow\": {\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, "
-                               "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"sub2\": %d, \"tiles\": %lld, "
+                               "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"n_h\": %d, \"sub2\": %d, \"tiles\": %lld, "
                                "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d}}",
-                               c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.sub2, c.tiles,
+                               c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.n_h, c.sub2, c.tiles,
                                c.smem_bytes, c.grid, plan->shadow_w_off, c.m64);
         n = n - 1 + m;
     }

@@ -913,6 +913,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         g.n_tiles = (d.C_out + kBM - 1) / kBM;
     }
     const int wres = g.m64 ? g.KT * g.n_chunks * 9 * kWBlock64 : 0;
+    const bool light = g.m64 && d.C_in <= 16;
     for (int ci = 0; ci < nc; ++ci) {
         const int Wt = g.nchw ? (cands[ci] + 7) / 8 * 8 : cands[ci];  // NCHW: strips start 16-byte aligned
         const int P = Wt + 2;
@@ -936,9 +937,13 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         }
         int n_w = (kSmemLimit - fixed - 2 * h_bytes - n_raw * raw_bytes) / kWBlock;
         if (n_w > 6) n_w = 6;
+        int n_h = 2;
         if (g.m64) {
             if (fixed + 2 * h_bytes + wres > kSmemLimit) continue;
             n_w = 6;  // no weight ring: rank as the deepest one
+            // at most 16 input channels: one K step per tap, so a tile's MMAs take less time than a
+            // halo load's latency; stage as many halos ahead as fit
+            if (light) n_h = (int)((kSmemLimit - fixed - wres) / h_bytes) < 4 ? (int)((kSmemLimit - fixed - wres) / h_bytes) : 4;
         }
         if (n_w < 3) continue;
         const int strips = (W_out + Wt - 1) / Wt;
@@ -946,17 +951,18 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         const long long tiles = (long long)strips * windows * g.frames * g.n_tiles;
         const long long waves = (tiles + num_sms - 1) / num_sms;
         // every tile costs the same MMA work: rank by waves, then by weight-ring depth and halo size
-        const long long cost = waves * 100000 + (6 - n_w) * 10000 + (g.nchw ? (4 - n_raw) * 20000 : 0) +
-                               (long long)HR * P;
+        // (light M = 64 layers: by halo pipeline depth first)
+        const long long cost = (light ? (4 - n_h) * 10000000LL : 0) + waves * 100000 + (6 - n_w) * 10000 +
+                               (g.nchw ? (4 - n_raw) * 20000 : 0) + (long long)HR * P;
         if (!found || cost < best_cost) {
             found = true;
             best_cost = cost;
             g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
-            g.n_h = 2; g.n_w = g.m64 ? 1 : n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
+            g.n_h = n_h; g.n_w = g.m64 ? 1 : n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
             g.raw_w = g.nchw ? raw_w : 0; g.raw_bytes = raw_bytes; g.n_raw = n_raw;
             g.raw_tx_bytes = g.nchw ? 16 * HR * raw_w * 2 : 0;
             g.w_smem = g.m64 ? wres : n_w * kWBlock;
-            g.smem_bytes = fixed + 2 * h_bytes + g.w_smem + n_raw * raw_bytes;
+            g.smem_bytes = fixed + n_h * h_bytes + g.w_smem + n_raw * raw_bytes;
         }
     }
   }
