@@ -149,12 +149,14 @@ def _check_sw128_plan(g):
     # the furthest halo row read: a window starting at offset P-1 of a row (or 0 when P divides
     # 256), its last position, tap (kh=2, kw=2)
     adv = g["win_adv"]
-    assert adv == (254 if g["kwm"] else 256)
-    # furthest halo row read by a window: its start offset in the first row, its last column,
+    # a tile is one window of 256 positions (254 in the head form), or two (512) in the W2 form
+    assert adv == (254 if g["kwm"] else (512 if g["w2"] else 256))
+    span = 512 if g["w2"] else 256
+    # furthest halo row read by a tile: its start offset in the first row, its last column,
     # kh = 2 (+2P) and, unless kw is folded into M, kw = 2 (+2); every such row is staged by the box
     for win in range(min(g["windows"], 4 * P)):
         pos_off = (adv * win) % P
-        need = pos_off + 255 + 2 * P + (0 if g["kwm"] else 2) + 1
+        need = pos_off + span - 1 + 2 * P + (0 if g["kwm"] else 2) + 1
         assert need <= HR * P and need * 128 <= g["h_bytes"]
     assert g["h_bytes"] % 1024 == 0 and g["smem_bytes"] <= 232448
     assert g["strips"] * Wt >= g["W_out"] and g["windows"] * adv >= g["H_out"] * P

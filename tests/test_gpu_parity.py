@@ -179,6 +179,33 @@ def test_head_clamp_unpatchify(variant, shape):
             assert ssim_rgb(got, ref) >= SSIM_MIN
 
 
+W2_CASES = [
+    # (N, C_in, C_out, D, H, W, act, with_carry)
+    (1, 128, 128, 2, 10, 300, "relu", True),
+    (1, 128, 128, 3, 9, 140, "relu", False),
+    (2, 64, 96, 2, 7, 41, "none", True),       # ragged: the pair's second window past the end
+    (1, 256, 128, 2, 13, 77, "none", True),    # four channel chunks
+]
+
+
+@pytest.mark.parametrize("variant", ["int", "random"])
+@pytest.mark.parametrize("case", W2_CASES, ids=lambda c: "x".join(map(str, c[:6])) + ("c" if c[7] else "z"))
+def test_conv3d_two_window_form(case, variant, monkeypatch):
+    """The two-window form (X3CONV_W2=1 takes it on these small shapes; the planner picks it for the
+    352x624 128->128 layers): a tile is two consecutive windows sharing each weight K slice."""
+    monkeypatch.setenv("X3CONV_W2", "1")
+    N, Ci, Co, D, H, W, act, with_carry = case
+    x, carry, L = synth.conv3d_single(C_in=Ci, C_out=Co, D=D, H=H, W=W, N=N, variant=variant, act=act,
+                                      seed=3300 + sum(case[:6]), with_carry=with_carry)
+    got, conv = run3d(x, carry, L)
+    assert x3.conv_plan_describe(conv.plan)["w2"] == 1
+    ref = oracle3d(x, carry, L)
+    if variant == "int":
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+
+
 # ------------------------------------------------------------------ full sizes, sampled
 
 FULL_3D = {

@@ -172,7 +172,11 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // weight blocks; each block is fetched once from L2 by one of the two (alternating) and multicast into
 // both CTAs' ring stage, and a stage is refilled only after the MMAs of both CTAs have read it (each
 // MMA issuer's commit arrives on the stage's empty barrier in both CTAs).
-template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false>
+// W2 (channels-last, one output tile; opt-in): a tile is two consecutive 256-position windows whose
+// halo is staged by one box; each weight K slice feeds an MMA for the first window and then one for
+// the second, which re-uses the A operand it just fetched, the two accumulators filling all 512 TMEM
+// columns (so the epilogue no longer overlaps the MMAs).
+template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false, bool W2 = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -391,8 +395,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 }
                 const ClTile tc = cl_decode(a, tile);
                 const int pos_off = (tc.win * a.win_adv) % a.P;
-                const uint32_t ab = it & 1u;
-                if (!cl_wait(bar_acc_empty + 8 * ab, ((it >> 1) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                // two accumulator buffers used alternately, or (W2) one pair of them per tile
+                const uint32_t ab = W2 ? 0u : (it & 1u);
+                const uint32_t use = W2 ? it : (it >> 1);
+                if (!cl_wait(bar_acc_empty + 8 * ab, (use & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + ab * (uint32_t)kBNP;
                 uint32_t acc = 0;
@@ -419,6 +425,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         const uint64_t bdesc = ((uint64_t)b_hi_fixed << 32) |
                                                (uint64_t)(((baddr >> 4) & 0x3FFFu) | (1u << 16));
                         ptx::mma_f16(d, adesc, bdesc, a.idesc, acc);
+                        if (W2)  // the second window: 256 positions further on in the same staged halo
+                            ptx::mma_f16(d + (uint32_t)kBNP, adesc, bdesc + (uint64_t)((kBNP * 128u) >> 4), a.idesc, acc);
                         acc = 1;
                     }
                     if (!M64 && !CTR) {
@@ -509,8 +517,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         for (long long k = 0;; ++k, ++it) {
             const long long tile = cl_tile_of(k, MC, rank);
             if (tile >= a.tiles) break;
-            const uint32_t ab = it & 1u;
-            if (!cl_wait(bar_acc_full + 8 * ab, (it >> 1) & 1u, abort_flag, a.status)) break;
+            const uint32_t ab = W2 ? 0u : (it & 1u);
+            if (!cl_wait(bar_acc_full + 8 * ab, (W2 ? it : (it >> 1)) & 1u, abort_flag, a.status)) break;
             ptx::tc_fence_after();
             const ClTile tc = cl_decode(a, tile);
             const int n = tc.fr / a.dout, t = tc.fr % a.dout;
@@ -694,7 +702,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // Each warp transposes its own 32 channels x 32 positions through a private staging
                     // block (no barrier across warps), then writes 64 contiguous bytes per position row.
                     uint8_t* wst = stage_ptr + ew * kStageWarpBytes;
-                    for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
+                    // W2: the two windows of the tile, accumulators in TMEM columns 0-255 and 256-511
+                    for (int chunk = 0; chunk < (W2 ? 2 : 1) * (kBNP / 32); ++chunk) {
                         uint32_t v[32];
                         ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
                         ptx::tmem_ld_wait();
@@ -967,12 +976,48 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     }
   }
     if (!found) return false;
+    // Causal channels-last layers with one output tile can run in the two-window form (W2), taken
+    // only with X3CONV_W2=1. A probe had put a second MMA on the same A operand at ~104 cycles
+    // against ~200, but the form measured slower on the 352x624 128->128 layer (1.151 against 1.089
+    // ms per two launches): its weight ring is three blocks deep, a tile is twice as long, and the
+    // epilogue no longer overlaps the MMAs.
+    const char* w2_env = getenv("X3CONV_W2");
+    if (!g.kwm && !g.nchw && !g.ctr && !g.m64 && g.n_tiles == 1 && d.dims == 3 && !small_cout &&
+        w2_env && !strcmp(w2_env, "1")) {
+        double best = 1e30;
+        for (int ci = 0; ci < nc; ++ci) {
+            const int Wt = cands[ci];
+            const int P = Wt + 2;
+            if (P > 256) continue;
+            const int pos_off_max = (512 % P) == 0 ? 0 : P - 1;
+            const int need_pos = pos_off_max + 511 + 2 * P + 2 + 1;
+            const int HR = (need_pos + P - 1) / P;
+            if (HR > 256) continue;
+            const int pos = HR * P > need_pos ? HR * P : need_pos;
+            const int h_bytes = (pos * 128 + 1023) / 1024 * 1024;
+            int n_w = (kSmemLimit - fixed - 2 * h_bytes) / kWBlock;
+            if (n_w > 6) n_w = 6;
+            if (n_w < 3) continue;
+            const int strips = (W_out + Wt - 1) / Wt;
+            const int windows = (int)(((long long)H_out * P + 511) / 512);
+            const long long tiles = (long long)strips * windows * g.frames;
+            const double est = (double)((tiles + num_sms - 1) / num_sms) + 0.001 * (6 - n_w);
+            if (est < best) {
+                best = est;
+                g.w2 = 1; g.win_adv = 512;
+                g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
+                g.n_h = 2; g.n_w = n_w; g.strips = strips; g.windows = windows; g.tiles = tiles;
+                g.w_smem = n_w * kWBlock;
+                g.smem_bytes = fixed + 2 * h_bytes + g.w_smem;
+            }
+        }
+    }
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
     // one output tile and streamed weights: pairs of CTAs can share the weight stream (the launcher
     // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
     // the weights measured no faster on any layer of the decoder (each SM still receives every block).
     const char* cl_env = getenv("X3CONV_CLUSTER");
-    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
+    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && !g.w2 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
@@ -1092,7 +1137,9 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl cluster launch: %s", cudaGetErrorString(e));
         return X3_OK;
     }
-    if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
+    if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, true>
+                       : igemm_cl_kernel<false, false, false, false, false, false, true>;
+    else if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
     else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
     else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
     else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false> : igemm_cl_kernel<false, true, false>;

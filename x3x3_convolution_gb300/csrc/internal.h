@@ -73,6 +73,7 @@ struct ClGeom {
     int m64;                     // 1: M = 64 MMAs (at most 64 output channels), weights resident
     int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
     int mc;                      // 1: clusters of two CTAs sharing each weight block by multicast
+    int w2;                      // 1: a tile is two consecutive windows sharing every weight K slice
     long long tiles;
     int smem_bytes, grid;
 };
