@@ -82,16 +82,63 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """SM clocks and clock-event (throttle) reasons sampled during the timed region: NVML read through
+    ctypes every millisecond from a background thread (the timed region of a short run lasts only tens
+    of milliseconds), else nvidia-smi every 200 ms. Read-only: no setting of the GPU is touched."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h): SwPowerCap, HwSlowdown, SwThermalSlowdown, HwThermalSlowdown
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.nvml = None
+        self.handle = None
+        self.samples = []
+        self.stop_flag = None
+        self.thread = None
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(gpu_index)
+                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.nvml, self.handle = lib, h
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except Exception:
+            self.nvml = None
+
+    def _poll(self):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                    self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0 and \
+                    self.reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.001)
 
     def start(self):
+        if self.nvml is not None:
+            import threading
+            self.samples = []
+            self.stop_flag = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -100,6 +147,15 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            if not self.samples:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": "nvml"}
+            reasons = sorted({name for _, _, r in self.samples for bit, name in self.REASON_BITS.items() if r & bit})
+            return {"sm_mhz": statistics.median(c for c, _, _ in self.samples),
+                    "sm_max_mhz": max(m for _, m, _ in self.samples), "reasons": reasons,
+                    "samples": len(self.samples), "source": "nvml, 1 ms"}
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -126,7 +182,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 class Workload:
@@ -449,7 +505,8 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    if clocks.nvml is None:
+        time.sleep(0.3)  # nvidia-smi needs a moment to start its 200 ms loop
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
