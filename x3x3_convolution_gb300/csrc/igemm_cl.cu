@@ -1,14 +1,18 @@
 // Channels-last tcgen05 implicit-GEMM engine with output channels as M and positions as N.
 //
 // The causal 3x3x3 convolution of FastVideo wan22_vae_decode/solution/head.cu (bf16 storage, fp32
-// accumulation of all 27 taps, bias, one rounding at the store) for channels-last layers with at
-// least 128 output channels. Each MMA is tcgen05.mma kind::f16 with
-//   A = packed weights  (M = 128 output channels x K = 16 input channels, K-major, no swizzle),
+// accumulation of all 27 taps, bias, one rounding at the store) and the 2D 3x3 convolution of the
+// TAESD conv page, for channels-last layers (and, in the NCHW form, NCHW 2D layers). Each MMA is
+// tcgen05.mma kind::f16 with
+//   A = packed weights  (M = 128 output channels x K = 16 input channels, K-major, no swizzle;
+//                        M = 64 in the form for at most 64 output channels),
 //   B = input halo      (N = 256 output positions x K = 16 input channels, K-major, 128-byte swizzle),
 //   D = fp32 accumulator in TMEM (128 lanes = channels x 256 columns = positions).
 // Why this arrangement: with N = 256 each MMA reads 12 KB of operands for 1 MFLOP instead of the
 // 8 KB per 0.5 MFLOP of a 128x128 tile, which keeps the tensor core's shared-memory operand reads
 // below the SM's shared-memory bandwidth and leaves room for the TMA writes of the next stages.
+// Measured on GB300: ~165 cycles per MMA when consecutive taps re-read shifted rows of one staged
+// halo, ~270 when both operands are fresh (the centre-tap form), ~104 for a second MMA on the same A.
 //
 // Tiling. The output plane is cut into vertical strips Wt columns wide; each strip is walked as a
 // raster of pitch P = Wt + 2 (two junk columns per row), and a tile is a window of 256 consecutive
@@ -22,8 +26,10 @@
 // Roles (one persistent CTA per SM): warp 0 issues the TMA loads (halo) and bulk copies (weights),
 // warp 1 owns TMEM and one thread issues the MMAs, warps 2-5 drain TMEM (two accumulator buffers,
 // so the epilogue of one tile overlaps the MMAs of the next), add the bias, apply the activation,
-// round once and write channels-last rows through a shared-memory transpose. Every wait is bounded
-// (1 s); a wait that runs out sets the device status word and every role gives up cleanly.
+// round once and write channels-last rows through a shared-memory transpose (the NCHW form adds
+// four transposer warps). Every wait is bounded (1 s); a wait that runs out sets the device status
+// word and every role gives up cleanly. The forms (head, NCHW, centre tap, M = 64, cluster, two
+// windows) are described at the kernel template below.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
