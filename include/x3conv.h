@@ -21,7 +21,8 @@
  * Conventions shared by every entry point:
  *   - Device pointers are plain CUDA device (or managed) addresses owned by the caller. The
  *     library never allocates, frees or retains device memory, except for one internal 4-byte
- *     device status word per device.
+ *     device status word per device and the scratch array built in for
+ *     conv_stack_forward_noalloc (X3_NOALLOC_SCRATCH_BYTES per device).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All work is enqueued on it;
  *     nothing synchronises. Pointers must stay valid until the enqueued work has finished.
  *   - Functions return x3_status. On failure nothing was enqueued (for X3_ERR_INVALID and
@@ -109,7 +110,10 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan);
 /* Release a plan (NULL is ignored). */
 void conv_plan_destroy(x3_conv_plan* plan);
 
-/* Name of the kernel the plan runs ("igemm_tcgen05", "direct_simt"), for logs and tests. */
+/* Name of the kernel the plan runs, for logs and tests: "igemm_tcgen05_sw128" (swapped-operand
+ * tcgen05 engine, channels-last), "igemm_tcgen05_sw128_head" (its conv_out head form),
+ * "igemm_tcgen05_sw128_nchw" (its NCHW form), "igemm_tcgen05" (positions-as-M tcgen05 engine),
+ * "direct_simt", "head_two_pass" / "head_split" (run with conv_head_two_pass). */
 const char* conv_plan_kernel_name(const x3_conv_plan* plan);
 
 /*
@@ -119,7 +123,8 @@ const char* conv_plan_kernel_name(const x3_conv_plan* plan);
  */
 int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len);
 
-/* Number of kernel launches one conv_forward with this plan enqueues. */
+/* Number of kernel launches one conv_forward with this plan enqueues (a two-pass head plan runs
+ * with conv_head_two_pass, which enqueues two). */
 int conv_plan_launches(const x3_conv_plan* plan);
 
 /* Bytes of the packed-weight buffer conv_pack_weights fills for this plan. */
@@ -170,14 +175,19 @@ x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void
 /*
  * Workspace bytes conv_stack_forward needs for these layers: two ping-pong buffers, each the size
  * of the largest intermediate activation (every intermediate is dead as soon as the next layer
- * has read it). Returns 0 for an invalid stack.
+ * has read it), or, for a stack of 2D NCHW layers run channels-last between the layers, of the
+ * largest of those and of the first layer's input converted to channels-last (C_in rounded up to
+ * a multiple of 8). Returns 0 for an invalid stack.
  */
 size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers);
 
 /*
  * Run n_layers chained layers: layer i reads layer i-1's output (layer 0 reads x), the last layer
  * writes y. Consecutive plans must agree: C_out[i] == C_in[i+1], output size of i == input size of
- * i+1, same dims, N, D, layout and dtype, and no unpatchify except on the last layer.
+ * i+1, same dims, N, D, layout and dtype, and no unpatchify except on the last layer. A stack of
+ * 2D NCHW layers (each with C_out a multiple of 8, the last of stride 1) keeps its activations
+ * channels-last between the layers (x and y stay NCHW; X3CONV_STACK_LAYOUT=nchw in the environment
+ * runs every layer in NCHW instead); the values are the same.
  *   carries:     3D only; carries[i] is layer i's two-frame history buffer (layout of its input,
  *                2 frames). It is read as the frames preceding this pass (as zeros when
  *                carry_valid is 0) and then overwritten with the last two frames of the layer's
