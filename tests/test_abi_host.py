@@ -216,6 +216,9 @@ def test_head_two_pass_plan(lib):
         assert st == x3.X3_ERR_INVALID and "conv_head_two_pass" in x3.conv_last_error()
         assert lib.conv_head_two_pass(p, 16, None, 256, None, 1 << 40, 1 << 41, None) == x3.X3_ERR_INVALID  # bias
         assert lib.conv_head_two_pass(p, 16, None, 256, 32, (1 << 40) + 4, 1 << 41, None) == x3.X3_ERR_INVALID   # g align
+        assert lib.conv_head_two_pass(p, 16, None, 256, 32, 4096, 1 << 41, None) == x3.X3_ERR_INVALID  # g overlaps x
+        assert "overlap" in x3.conv_last_error()
+        assert lib.conv_head_two_pass(p, 1 << 42, None, 256, 32, 1 << 40, (1 << 40) + 4096, None) == x3.X3_ERR_INVALID
     finally:
         x3.conv_plan_destroy(p)
     q = x3.conv_plan_create(x3.make_desc(3, 1, 64, 64, 8, 8, D=2))

@@ -297,6 +297,17 @@ x3_status conv_head_two_pass(const x3_conv_plan* plan, const void* x, const void
         return fail(X3_ERR_INVALID, "conv_head_two_pass: NULL argument");
     if (!aligned(x, 16) || !aligned(g, 16) || !aligned(y, 16) || !aligned(w_packed, 256) || (carry && !aligned(carry, 16)))
         return fail(X3_ERR_INVALID, "conv_head_two_pass: x, g, y, carry need 16-byte alignment, w_packed 256-byte");
+    {
+        // g is written by pass 1 while x is read, and read by pass 2 while y is written
+        const char* lo_x = (const char*)x;
+        const char* hi_x = lo_x + in_elems(plan) * 2;
+        const char* lo_g = (const char*)g;
+        const char* hi_g = lo_g + conv_head_g_bytes(plan);
+        const char* lo_y = (const char*)y;
+        const char* hi_y = lo_y + out_elems(plan) * 2;
+        if ((lo_g < hi_x && lo_x < hi_g) || (lo_g < hi_y && lo_y < hi_g) || (lo_y < hi_x && lo_x < hi_y))
+            return fail(X3_ERR_INVALID, "conv_head_two_pass: x, g and y must not overlap");
+    }
     // pass 1: the temporal convolution into g (108 accumulator rows, no bias, no activation), written
     // one plane per spatial tap
     x3_conv_plan p1 = *plan;
