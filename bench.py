@@ -8,9 +8,9 @@ The step runs every stage of the path through the library's C ABI:
              (+2 carried) at 352x624 (conv_stack_forward with per-layer carries);
   * l3     - causal 256->128 over 4 frames (+2 carried) at 176x312 (conv_forward);
   * head   - conv_out head: causal 256->12 over 4 frames (+2 carried) at 352x624, bias, clamp to
-             [-1,1], 2x2 unpatchify to 4x704x1248 RGB, as the split form (conv_head_two_pass with an
-             fp32 G plane: the temporal pass on the tensor cores, then the nine spatial taps; exact on
-             integer data like the single-pass form, which is timed beside it with the bf16-G form).
+             [-1,1], 2x2 unpatchify to 4x704x1248 RGB (conv_forward: the stencil head, the temporal
+             sums of the nine taps on the tensor cores and the nine spatial taps in the epilogue;
+             the single-pass form and the two-pass forms are timed beside it).
 value = total convolution FLOP of the step / step time (TFLOP/s, whole job over all ranks).
 Also reported: decoder-stack ms per frame (stack + l3 + head over the 4 frames), per-stage times,
 the roofline fraction of the dominant kernel, an end-to-end number with host buffers, the SM
@@ -40,7 +40,7 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
             "(256->12 @4+2x352x624, clamp, 2x2 unpatchify)")
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
-AB_STAGES = ["head_fused", "head_two_pass"]
+AB_STAGES = ["head_fused", "head_two_pass", "head_split"]
 TRAFFIC_DOMINANT_BYTES = 876.3e6
 
 
@@ -219,21 +219,24 @@ class Workload:
         self.l3_y = torch.empty(self.l3.out_shape(), dtype=torch.bfloat16, device=dev)
         hx, hc, HL = synth.head(seed=1005 + seed_base)
         head_desc = dict(D=FRAMES, act="clamp", unpatchify2x2=True)
-        # the step's head: two passes with an fp32 G plane (buffer held by the Conv)
-        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_split", **head_desc),
-                            HL.w.torch(dev), HL.b.torch(dev))
+        # the step's head: the library's default (the stencil head: one kernel, G kept in fp32 on chip)
+        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, **head_desc), HL.w.torch(dev), HL.b.torch(dev))
         self.head_x = hx.torch(dev)
         self.head_c = hc.torch(dev)
         self.head_y = torch.empty(self.head.out_shape(), dtype=torch.bfloat16, device=dev)
-        # A/B forms of the head, not part of the step: the single pass and the bf16-G two passes
-        self.head_fused = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, **head_desc), HL.w.torch(dev),
-                                  HL.b.torch(dev))
+        # A/B forms of the head, not part of the step: the single pass (kw folded into M), the two
+        # passes with an fp32 G plane and with a bf16 one (the page's value path)
+        self.head_fused = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="igemm", **head_desc),
+                                  HL.w.torch(dev), HL.b.torch(dev))
         self.head_fused_y = torch.empty(self.head_fused.out_shape(), dtype=torch.bfloat16, device=dev)
         self.head2 = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_two_pass", **head_desc),
                              HL.w.torch(dev), HL.b.torch(dev))
         self.head2_y = torch.empty(self.head2.out_shape(), dtype=torch.bfloat16, device=dev)
-        # kernels per step: layout conversion + 7 TAESD convs, 2 stack convs, l3, the head's two passes
-        self.kernels_per_step = 1 + len(convs) + len(sc) + 1 + 2
+        self.head_split = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_split", **head_desc),
+                                  HL.w.torch(dev), HL.b.torch(dev))
+        self.head_split_y = torch.empty(self.head_split.out_shape(), dtype=torch.bfloat16, device=dev)
+        # kernels per step: layout conversion + 7 TAESD convs, 2 stack convs, l3, the head
+        self.kernels_per_step = 1 + len(convs) + len(sc) + 1 + 1
         self.plans = {"taesd": [x3.conv_plan_describe(c.plan) for c in convs],
                       "stack": x3.conv_plan_describe(sc[0].plan),
                       "l3": x3.conv_plan_describe(self.l3.plan),
@@ -408,7 +411,8 @@ def run_stage(wl, args, stream, fl, nb):
           "l3": lambda: wl.l3(wl.l3_x, wl.l3_c, out=wl.l3_y, stream=stream),
           "head": lambda: wl.head(wl.head_x, wl.head_c, out=wl.head_y, stream=stream),
           "head_fused": lambda: wl.head_fused(wl.head_x, wl.head_c, out=wl.head_fused_y, stream=stream),
-          "head_two_pass": lambda: wl.head2(wl.head_x, wl.head_c, out=wl.head2_y, stream=stream)}[args.stage]
+          "head_two_pass": lambda: wl.head2(wl.head_x, wl.head_c, out=wl.head2_y, stream=stream),
+          "head_split": lambda: wl.head_split(wl.head_x, wl.head_c, out=wl.head_split_y, stream=stream)}[args.stage]
     for _ in range(args.warmup):
         fn()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -426,12 +430,13 @@ def run_stage(wl, args, stream, fl, nb):
 
 
 def head_ab(wl, stream, reps=10):
-    """The step's head (two passes, fp32 G), the single-pass head and the bf16-G two passes, each
-    timed alone (CUDA events, after warm-up), and the largest differences from the single pass."""
+    """The step's head (the stencil head), the single-pass head, the two passes with fp32 and with
+    bf16 G, each timed alone (CUDA events, after warm-up), and the largest differences from the
+    single pass."""
     import torch
     out = {}
-    for name, conv, y in (("split_f32", wl.head, wl.head_y), ("fused", wl.head_fused, wl.head_fused_y),
-                          ("two_pass_bf16", wl.head2, wl.head2_y)):
+    for name, conv, y in (("stencil", wl.head, wl.head_y), ("fused", wl.head_fused, wl.head_fused_y),
+                          ("split_f32", wl.head_split, wl.head_split_y), ("two_pass_bf16", wl.head2, wl.head2_y)):
         for _ in range(3):
             conv(wl.head_x, wl.head_c, out=y, stream=stream)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -443,7 +448,8 @@ def head_ab(wl, stream, reps=10):
         e1.record(stream)
         torch.cuda.synchronize()
         out[name + "_ms"] = e0.elapsed_time(e1) / reps
-    out["max_abs_diff_split_f32"] = float((wl.head_fused_y.float() - wl.head_y.float()).abs().max())
+    out["max_abs_diff_stencil"] = float((wl.head_fused_y.float() - wl.head_y.float()).abs().max())
+    out["max_abs_diff_split_f32"] = float((wl.head_fused_y.float() - wl.head_split_y.float()).abs().max())
     out["max_abs_diff_two_pass_bf16"] = float((wl.head_fused_y.float() - wl.head2_y.float()).abs().max())
     return out
 

@@ -73,9 +73,14 @@ typedef enum {
                                     spatial taps with bias and clamp (FastVideo wan22_vae_decode/solution/
                                     head.cu, header comment and head_stencil_kernel); needs
                                     unpatchify2x2, 3D, X3_NDHWC, bf16 */
-    X3_KERNEL_HEAD_SPLIT = 4     /* the same two passes with g kept in fp32: every product and partial sum
+    X3_KERNEL_HEAD_SPLIT = 4,    /* the same two passes with g kept in fp32: every product and partial sum
                                     is carried in fp32 as in the single-pass head, so integer-valued data
                                     give the exact result; same requirements */
+    X3_KERNEL_HEAD_STENCIL = 5   /* the same arithmetic as HEAD_SPLIT in one kernel run by conv_forward:
+                                    the temporal sums of all nine taps stay in fp32 in TMEM and the
+                                    epilogue adds the nine spatial taps; same requirements. AUTO picks it
+                                    for such heads; X3_KERNEL_IGEMM gives the single-pass form (kw
+                                    folded into M, one accumulator over all 27 taps) */
 } x3_kernel;
 
 /* Descriptor of one convolution layer. */

@@ -133,7 +133,8 @@ WORKLOADS = {
     "causal_256_88x156": dict(dims=3, N=1, C_in=256, C_out=256, D=4, H=88, W=156),
     "causal_128_352x624": dict(dims=3, N=1, C_in=128, C_out=128, D=4, H=352, W=624),
     "causal_256to128_176x312": dict(dims=3, N=1, C_in=256, C_out=128, D=4, H=176, W=312),
-    "head_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True),
+    "head_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True, kernel="igemm"),
+    "head_stencil_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True),
     "ragged_3d": dict(dims=3, N=2, C_in=40, C_out=72, D=3, H=7, W=301),
     "ragged_3d_wide": dict(dims=3, N=2, C_in=40, C_out=136, D=3, H=7, W=301),
     "nhwc_2d_256": dict(dims=2, N=3, C_in=64, C_out=256, H=33, W=97, layout="NHWC"),
@@ -168,6 +169,14 @@ def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
+        if g.get("stn"):
+            # stencil head: 16 x 16 raster windows, 14 x 14 outputs each, one stage per (kt, chunk)
+            # holding the window (32 KB) and its weight block (16 KB)
+            assert g["P"] == 16 and g["Wt"] == 14 and g["HR"] == 16 and g["win_adv"] == 14 * 16
+            assert g["strips"] * 14 >= g["W_out"] and g["windows"] * 14 >= g["H_out"]
+            assert g["h_bytes"] == 16 * 16 * 128 + 128 * 64 * 2 and g["smem_bytes"] <= 232448
+            assert g["tiles"] == g["strips"] * g["windows"] * g["frames"]
+            return
         if WORKLOADS[name].get("kernel") == "head_two_pass":
             # the temporal pass stages no halo: windows of 256 consecutive positions of a frame, each
             # stage holding the window (32 KB) and its (kt, chunk) weight block (16 KB)

@@ -129,7 +129,7 @@ def test_split_head_full_size_sampled():
     assert_close(g, ref)
 
 
-@pytest.mark.parametrize("kernel", ["head_split", "auto"])
+@pytest.mark.parametrize("kernel", ["head_split", "head_stencil", "auto"])
 def test_head_full_size_decoded_quality(kernel):
     """All 4 decoded 704x1248 RGB frames of the full-size head against the oracle's head computed in
     full: PSNR and SSIM (the second quality metric) of the decoded output, plus the tolerance."""
@@ -144,3 +144,41 @@ def test_head_full_size_decoded_quality(kernel):
     assert_close(got, ref)
     assert psnr(got, ref) >= PSNR_MIN
     assert ssim_rgb(got, ref) >= SSIM_MIN
+
+
+def run_head(x, carry, L, kernel):
+    N, D, H, W, C = x.shape
+    d = x3.make_desc(3, N, C, 12, H, W, D=D, layout="NDHWC", dtype="bf16", act="clamp", unpatchify2x2=True,
+                     kernel=kernel)
+    conv = x3.Conv(d, dev(L.w), dev(L.b))
+    y = conv(dev(x), None if carry is None else dev(carry))
+    torch.cuda.synchronize()
+    return host_values(y, "bf16"), conv
+
+
+@pytest.mark.parametrize("shape", SHAPES + [(2, 15, 29), (1, 28, 14)], ids=str)
+@pytest.mark.parametrize("variant", ["int", "sparse1", "random"])
+def test_stencil_head(variant, shape):
+    """The head in one kernel with the spatial stencil in the epilogue: exact on integer data against
+    the oracle's single-pass head, and bit for bit the split form's values (same fp32 sums in the same
+    order) on random data; shapes around the 14 x 14 window interiors."""
+    D, H, W = shape
+    x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3800 + H + W)
+    got, conv = run_head(x, carry, L, "head_stencil")
+    assert conv.kernel_name == "igemm_tcgen05_sw128_head_stencil"
+    ref = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp", layout="NDHWC"))
+    assert got.shape == ref.shape
+    if variant != "random":
+        assert_exact(got, ref, "bf16")
+    else:
+        assert_close(got, ref)
+        assert psnr(got, ref) >= PSNR_MIN
+        split, _ = run_head(x, carry, L, "head_split")
+        assert np.array_equal(got, split)
+
+
+def test_stencil_head_without_carry():
+    x, _, L = synth.head(D=2, H=20, W=45, variant="int", seed=3890)
+    got, _ = run_head(x, None, L, "head_stencil")
+    ref = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, act="clamp", layout="NDHWC"))
+    assert_exact(got, ref, "bf16")

@@ -160,11 +160,14 @@ def test_conv3d_causal(case, variant, kernel, monkeypatch):
 
 @pytest.mark.parametrize("shape", [(2, 9, 140), (3, 5, 300), (1, 17, 33)], ids=str)
 @pytest.mark.parametrize("variant", ["sparse1", "random"])
-def test_head_clamp_unpatchify(variant, shape):
+@pytest.mark.parametrize("kernel", ["auto", "igemm"])
+def test_head_clamp_unpatchify(variant, shape, kernel):
+    """auto: the stencil head (one kernel, nine spatial taps in the epilogue); igemm: the single-pass
+    form with kw folded into M."""
     D, H, W = shape
     x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3500 + H)
-    got, conv = run3d(x, carry, L, unpatch=True)
-    assert conv.kernel_name == "igemm_tcgen05_sw128_head"
+    got, conv = run3d(x, carry, L, kernel=kernel, unpatch=True)
+    assert conv.kernel_name == ("igemm_tcgen05_sw128_head" if kernel == "igemm" else "igemm_tcgen05_sw128_head_stencil")
     ref12 = oracle3d(x, carry, L)                                   # [1, D, H, W, 12]
     ref = oracle.unpatchify2x2(ref12.transpose(0, 4, 1, 2, 3))      # [1, 3, D, 2H, 2W]
     ref = ref.transpose(0, 2, 3, 4, 1)                              # [1, D, 2H, 2W, 3]
@@ -230,7 +233,7 @@ def test_full_size_sampled(name):
 
 def test_full_size_head_sampled():
     x, carry, L = synth.head(seed=3950)
-    got, conv = run3d(x, carry, L, unpatch=True)
+    got, conv = run3d(x, carry, L, kernel="igemm", unpatch=True)
     assert conv.kernel_name == "igemm_tcgen05_sw128_head"
     assert got.shape == (1, 4, 704, 1248, 3)
     seq = np.concatenate([carry.vals, x.vals], axis=1)
@@ -256,7 +259,7 @@ def test_cluster_weight_multicast(form, monkeypatch):
     else:
         x, carry, L = synth.head(D=3, H=7, W=150, variant="sparse1", seed=3802)
         N, D, H, W, C = x.shape
-        d = x3.make_desc(3, N, C, 12, H, W, D=D, act="clamp", unpatchify2x2=True)
+        d = x3.make_desc(3, N, C, 12, H, W, D=D, act="clamp", unpatchify2x2=True, kernel="igemm")
         conv = x3.Conv(d, dev(L.w), dev(L.b))
         got = host_values(conv(dev(x), dev(carry)), "bf16")
         torch.cuda.synchronize()

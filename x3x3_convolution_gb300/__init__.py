@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "X3_OK", 1: "X3_ERR_INVALID", 2: "X3_ERR_UNSUPPORTED", 3: "X3
 LAYOUT = {"NCHW": 0, "NHWC": 1, "NCDHW": 2, "NDHWC": 3}
 DTYPE = {"f16": 0, "bf16": 1}
 ACT = {"none": 0, "relu": 1, "clamp": 2}
-KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3, "head_split": 4}
+KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3, "head_split": 4, "head_stencil": 5}
 
 
 class ConvDesc(ctypes.Structure):

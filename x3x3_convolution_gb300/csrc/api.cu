@@ -62,7 +62,7 @@ static x3_status validate(const x3_conv_desc* d) {
     if (d->has_bias != 0 && d->has_bias != 1) return fail(X3_ERR_INVALID, "has_bias must be 0 or 1");
     if (d->unpatchify2x2 != 0 && d->unpatchify2x2 != 1) return fail(X3_ERR_INVALID, "unpatchify2x2 must be 0 or 1");
     if (d->unpatchify2x2 && d->C_out != 12) return fail(X3_ERR_INVALID, "unpatchify2x2 needs C_out == 12");
-    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_SPLIT) return fail(X3_ERR_INVALID, "bad kernel choice");
+    if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_STENCIL) return fail(X3_ERR_INVALID, "bad kernel choice");
     // Every tensor must be indexable with 63-bit offsets and every per-image plane with 31 bits.
     const long long frames = (long long)d->N * (d->dims == 3 ? d->D + 2 : 1);
     const long long plane = (long long)d->H * d->W;
@@ -123,6 +123,23 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         p->packed_bytes = (size_t)p->cl.KT * p->cl.n_chunks * (128 * 64 * 2);
         *plan = p;
         return X3_OK;
+    }
+    // the conv_out head (bf16 channels-last, unpatchified) runs by default as the stencil head
+    const bool auto_head = choice == X3_KERNEL_AUTO && !force && p->d.unpatchify2x2 && p->d.dims == 3 &&
+                           p->d.layout == X3_NDHWC && p->d.dtype == X3_BF16;
+    if (choice == X3_KERNEL_HEAD_STENCIL || auto_head) {
+        p->d.kernel = X3_KERNEL_HEAD_STENCIL;
+        if (igemm_cl_plan(p, p->num_sms)) {
+            p->kind = K_IGEMM_CL;
+            p->packed_bytes = (size_t)p->cl.KT * p->cl.n_chunks * (128 * 64 * 2);
+            *plan = p;
+            return X3_OK;
+        }
+        if (!auto_head) {
+            delete p;
+            return fail(X3_ERR_UNSUPPORTED, "the stencil head needs unpatchify2x2, 3D, X3_NDHWC and bf16");
+        }
+        p->d.kernel = X3_KERNEL_AUTO;  // no stencil plan: the other forms below
     }
     if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) {
         // 2D channels-last layers of any width run on the swapped engine (the M = 64 form for at most
@@ -196,6 +213,7 @@ const char* conv_plan_kernel_name(const x3_conv_plan* plan) {
     if (!plan) return "";
     if (plan->kind == K_HEAD_TWO_PASS) return plan->d.kernel == X3_KERNEL_HEAD_SPLIT ? "head_split" : "head_two_pass";
     if (plan->kind == K_IGEMM_CL && plan->cl.kwm) return "igemm_tcgen05_sw128_head";
+    if (plan->kind == K_IGEMM_CL && plan->cl.stn) return "igemm_tcgen05_sw128_head_stencil";
     if (plan->kind == K_IGEMM_CL && plan->cl.nchw) return "igemm_tcgen05_sw128_nchw";
     return plan->kind == K_IGEMM_CL ? "igemm_tcgen05_sw128" : plan->kind == K_IGEMM ? "igemm_tcgen05" : "direct_simt";
 }
@@ -213,10 +231,10 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, \"mc\": %d, "
-                        "\"m64\": %d, \"sub2\": %d, \"ctr\": %d, \"w2\": %d}",
+                        "\"m64\": %d, \"sub2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.mc, c.m64, c.sub2, c.ctr, c.w2);
+                        c.mc, c.m64, c.sub2, c.ctr, c.w2, c.stn);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",

@@ -201,6 +201,29 @@ __global__ void __launch_bounds__(256) pack_ctr_kernel(const uint16_t* __restric
     }
 }
 
+// Packed weights of the stencil head: blocks ordered [kt][chunk] like the centre-tap form, but row
+// 32q + 9*cl + (i*3+j) (the last 5 rows of each 32-row quarter zero) carries w[c][ci][kt][i][j] for
+// channel c = 3q + cl, so that each epilogue warp holds all nine taps of its three channels.
+__global__ void __launch_bounds__(256) pack_stn_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                       int C_in, int n_chunks, size_t total) {
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        size_t r = idx;
+        const int e = (int)(r % 8); r /= 8;
+        const int row = (int)(r % 128); r /= 128;
+        const int j8 = (int)(r % 8); r /= 8;
+        const int cc = (int)(r % n_chunks); r /= n_chunks;
+        const int kt = (int)r;
+        const int ci = cc * 64 + j8 * 8 + e;
+        const int q = row / 32, rr = row % 32;
+        uint16_t v = 0;
+        if (rr < 27 && ci < C_in) {
+            const int c = 3 * q + rr / 9, tap = rr % 9;
+            v = w[(((size_t)c * C_in + ci) * 3 + kt) * 9 + tap];
+        }
+        out[idx] = v;
+    }
+}
+
 // The nine spatial taps of the two-pass head, one thread per output position: bias-initialised fp32
 // accumulators for the 12 channels, the 12 values of tap plane i*3+j at each neighbour inside the
 // image added in (i, j) order, clamp to [-1,1], one rounding to bf16, written as the 2x2-unpatchified
@@ -312,6 +335,16 @@ static x3_status pack_primary(const x3_conv_plan* p, const void* w, void* w_pack
         size_t blocks = (total + 255) / 256;
         if (blocks > 4096) blocks = 4096;
         pack_ctr_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, p->d.C_in,
+                                                        p->cl.n_chunks, total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
+    if (p->kind == K_IGEMM_CL && p->cl.stn) {
+        const size_t total = p->packed_bytes / 2;
+        size_t blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        pack_stn_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)w_packed, p->d.C_in,
                                                         p->cl.n_chunks, total);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));

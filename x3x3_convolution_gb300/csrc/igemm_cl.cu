@@ -57,7 +57,9 @@ constexpr int kCtrW = kBNP * kCK * 2;    // centre-tap form: offset of the weigh
 constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
-constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (covers every use)
+constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
+constexpr int kStnPitch = 97;     // STN: fp32 staging row (96 TMEM columns + pad) per lane
+constexpr int kStnStageBytes = 32 * kStnPitch * 4;
 
 struct ClArgs {
     int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
@@ -73,6 +75,7 @@ struct ClArgs {
     int w_smem;      // bytes of shared memory for weight blocks (n_w stages, or all blocks when resident)
     int frame_inner; // tile order with the output frame varying fastest
     int g_f32;       // centre-tap form: the tap planes of G in fp32 (else bf16)
+    int stage_warp;  // epilogue staging bytes per warp
     long long tiles;
     uint32_t idesc;
     const uint8_t* w;
@@ -182,7 +185,13 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // halo is staged by one box; each weight K slice feeds an MMA for the first window and then one for
 // the second, which re-uses the A operand it just fetched, the two accumulators filling all 512 TMEM
 // columns (so the epilogue no longer overlaps the MMAs).
-template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false, bool W2 = false>
+// STN (with CTR; the conv_out head in one pass): the centre-tap MMAs over a 16 x 16 raster window
+// (one halo column and row on each side of 14 x 14 outputs; windows overlap by two rows), M rows
+// 32q + 9cl + tap for channel 3q + cl, so each epilogue warp holds all nine taps of its three channels;
+// the epilogue adds, in fp32, the bias and the nine taps' values at the shifted window positions
+// (staged through shared memory), clamps, rounds once and writes the unpatchified RGB pixels.
+template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false, bool W2 = false,
+          bool STN = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
     const uint32_t sStage = sW + (uint32_t)a.w_smem;               // epilogue transpose tile
-    const uint32_t sRaw = sStage + 4u * (uint32_t)kStageWarpBytes;           // NCHW raw tiles (128-aligned)
+    const uint32_t sRaw = sStage + 4u * (uint32_t)a.stage_warp;              // NCHW raw tiles (128-aligned)
     const uint32_t sJunk = sRaw + (uint32_t)(a.n_raw * a.raw_bytes);         // NCHW: 16 B per transposer lane
     const uint32_t sBar = sJunk + (NC ? 4u * 32u * 16u : 0u);
     const uint32_t bar_h_full = sBar;
@@ -318,9 +327,14 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
                             if (CTR) {
-                                // 256 consecutive positions of the frame's flattened plane and the
-                                // (kt, chunk) weight block, one stage and one barrier for both
-                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
+                                // 256 consecutive positions of the frame's flattened plane (STN: the
+                                // 16 x 16 raster window) and the (kt, chunk) weight block, one stage
+                                // and one barrier for both
+                                if (STN)
+                                    ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1,
+                                                     tc.win * (a.HR - 2) - 1, fcoord);
+                                else
+                                    ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
                                 ptx::bulk_load(sH + sh * a.h_bytes + (uint32_t)kCtrW,
                                                a.w + ((size_t)kt * a.n_chunks + cc) * (size_t)kWBlock, (uint32_t)kWBlock,
                                                bar_h_full + 8 * sh);
@@ -517,6 +531,13 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             if (co0 < a.C_out) m64_b0 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co0) << 16) : __half2float(__ushort_as_half(__ldg(bp + co0)));
             if (co1 < a.C_out) m64_b1 = BF16 ? __uint_as_float((uint32_t)__ldg(bp + co1) << 16) : __half2float(__ushort_as_half(__ldg(bp + co1)));
         }
+        float stn_bias[3] = {0.0f, 0.0f, 0.0f};  // STN: this warp's three channels 3q..3q+2
+        if (STN && a.bias) {
+            const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.bias);
+#pragma unroll
+            for (int cl = 0; cl < 3; ++cl)
+                if (3 * q + cl < a.C_out) stn_bias[cl] = __uint_as_float((uint32_t)__ldg(bp + 3 * q + cl) << 16);
+        }
         const float act_lo = a.act == X3_ACT_RELU ? 0.0f : (a.act == X3_ACT_CLAMP1 ? -1.0f : -INFINITY);
         const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
         const float inv_p = 1.0f / (float)a.P;
@@ -545,7 +566,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 // with that kw, at every window column; output column j adds kw = 0, 1, 2 at columns
                 // j, j+1, j+2 (its left, centre and right input columns).
                 if (q < a.ngroups) {
-                    float* S = reinterpret_cast<float*>(stage_ptr + ew * kStageWarpBytes);
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);
                     for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
                         uint32_t v[32], e2[2] = {0u, 0u};
                         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP +
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 if (NC || a.out_nchw) {
                     // NCHW: this warp's 32 channels x 32 positions are transposed through its staging
                     // block so that each store instruction writes 32 consecutive positions of a channel.
-                    uint16_t* T = reinterpret_cast<uint16_t*>(stage_ptr + ew * kStageWarpBytes);  // [32][34]
+                    uint16_t* T = reinterpret_cast<uint16_t*>(stage_ptr + ew * a.stage_warp);  // [32][34]
                     const int co_base = tc.nt * (M64 ? 64 : kBM) + q * kCpw;
                     if (co_base < a.C_out) {
                         for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
@@ -618,8 +639,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // [position][16 channels] rows of the warp's staging block, and each position's
                     // 32 bytes go out as two 16-byte stores. The next chunk's TMEM load is in flight
                     // while this one is processed.
-                    const uint32_t wst = sStage + (uint32_t)(ew * kStageWarpBytes);  // [32][16] x 2 B
-                    const uint8_t* wstp = stage_ptr + ew * kStageWarpBytes;
+                    const uint32_t wst = sStage + (uint32_t)(ew * a.stage_warp);  // [32][16] x 2 B
+                    const uint8_t* wstp = stage_ptr + ew * a.stage_warp;
                     const float b0 = m64_b0, b1 = m64_b1;
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
                     // stmatrix row address of this thread: matrix mi = lane / 8 (column group i = mi / 2,
@@ -671,12 +692,55 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) process(4 + c, rb[c]);
+                } else if (STN) {
+                    // Window position m = 16a + c holds G at plane row a, column c (row 0 and 15, column 0
+                    // and 15 are halo). Per chunk of 32 output positions, the warp stages TMEM columns
+                    // [32k - 32, 32k + 64) of its rows (9 taps x 3 channels) as S[lane][0..95]; thread
+                    // t then sums, for output m = 32k + t, bias + the nine taps in (i, j) order at
+                    // m + (i-1)*16 + (j-1), all inside the staged range since |offset| <= 17.
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [32][kStnPitch]
+                    const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
+                    const int oh_base = tc.win * (a.HR - 2) - 1, ow_base = ow0 - 1;
+                    const size_t W2o = 2 * (size_t)a.W_out;
+                    const size_t row0 = ((size_t)n * a.dout + t) * 2 * (size_t)a.H_out;
+                    for (int k = 0; k < kBNP / 32; ++k) {
+#pragma unroll
+                        for (int part = 0; part < 3; ++part) {
+                            const int col = 32 * (k - 1 + part);
+                            if (col < 0 || col >= kBNP) continue;  // only invalid outputs would read it
+                            uint32_t v[32];
+                            ptx::tmem_ld32(tq + (uint32_t)col, v);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) S[lane * kStnPitch + part * 32 + j] = __uint_as_float(v[j]);
+                        }
+                        __syncwarp();
+                        const int m = 32 * k + lane;
+                        const int wa = m >> 4, wc = m & 15;
+                        const int oh = oh_base + wa, ow = ow_base + wc;
+                        if (wa >= 1 && wa <= 14 && wc >= 1 && wc <= 14 && oh < a.H_out && ow < a.W_out) {
+#pragma unroll
+                            for (int cl = 0; cl < 3; ++cl) {
+                                const int c = 3 * q + cl;
+                                float acc = stn_bias[cl];
+#pragma unroll
+                                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                                    for (int j = 0; j < 3; ++j)
+                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + 32 + lane + (i - 1) * 16 + (j - 1)];
+                                const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
+                                y[((row0 + 2 * (size_t)oh + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
+                                    cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, acc)));
+                            }
+                        }
+                        __syncwarp();
+                    }
                 } else if (CTR) {
                     // Temporal pass of the split head: accumulator row r = (i*3+j)*12 + c goes to plane
                     // p = i*3+j of G at channel c. Each warp stages its 32 rows x 32 positions as
                     // [position][row] fp32, then writes 4-row groups (16 bytes of fp32 or 8 of bf16;
                     // quarter boundaries fall on 4-channel steps of a plane) for 32 positions at a time.
-                    float* S = reinterpret_cast<float*>(stage_ptr + ew * kStageWarpBytes);  // [32][kGPitch]
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [32][kGPitch]
                     const long long hw = (long long)a.H_out * a.W_out;
                     for (int chunk = 0; chunk < kBNP / 32; ++chunk) {
                         uint32_t v[32];
@@ -707,7 +771,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 } else {
                     // Each warp transposes its own 32 channels x 32 positions through a private staging
                     // block (no barrier across warps), then writes 64 contiguous bytes per position row.
-                    uint8_t* wst = stage_ptr + ew * kStageWarpBytes;
+                    uint8_t* wst = stage_ptr + ew * a.stage_warp;
                     // W2: the two windows of the tile, accumulators in TMEM columns 0-255 and 256-511
                     for (int chunk = 0; chunk < (W2 ? 2 : 1) * (kBNP / 32); ++chunk) {
                         uint32_t v[32];
@@ -882,7 +946,8 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     }
     // the conv_out head (12 channels to unpatchified RGB) runs in the kw-folded form
     g.kwm = d.unpatchify2x2 ? 1 : 0;
-    g.ctr = (d.kernel == X3_KERNEL_HEAD_TWO_PASS || d.kernel == X3_KERNEL_HEAD_SPLIT) ? 1 : 0;
+    g.stn = (d.kernel == X3_KERNEL_HEAD_STENCIL) ? 1 : 0;
+    g.ctr = (d.kernel == X3_KERNEL_HEAD_TWO_PASS || d.kernel == X3_KERNEL_HEAD_SPLIT || g.stn) ? 1 : 0;
     if (g.ctr) {
         // temporal pass of the two-pass head: 12 output channels x 9 spatial taps = 108 (112) channels
         if (!d.unpatchify2x2 || d.dims != 3 || d.layout != X3_NDHWC || d.dtype != X3_BF16) return false;
@@ -897,7 +962,8 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     g.n_tiles = g.ctr ? 1 : (d.C_out + kBM - 1) / kBM;
     g.frames = d.N * (d.dims == 3 ? d.D : 1);
     const int H_out = p->H_out, W_out = p->W_out;
-    const int fixed = 1024 + 4 * kStageWarpBytes + 512 + (g.nchw ? 4 * 32 * 16 : 0);
+    g.stage_warp = g.stn ? kStnStageBytes : kStageWarpBytes;
+    const int fixed = 1024 + 4 * g.stage_warp + 512 + (g.nchw ? 4 * 32 * 16 : 0);
     bool found = false;
     long long best_cost = -1;
     int cands[80], nc = 0;
@@ -907,7 +973,21 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // resident in shared memory; if no tiling leaves room for them, the 128-row form
     g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
     if (g.m64) g.n_tiles = 1;
-    if (g.ctr) {
+    if (g.stn) {
+        // stencil head: 16 x 16 raster windows (pitch 16, 14 output columns and rows inside one
+        // halo column and row on each side), consecutive windows of a strip two rows apart in overlap
+        g.Wt = 14; g.P = 16; g.HR = 16;
+        g.strips = (W_out + 13) / 14;
+        g.windows = (H_out + 13) / 14;
+        g.win_adv = 14 * 16;
+        g.h_bytes = g.h_tx_bytes = kCtrW + kWBlock;
+        g.n_h = 3; g.n_w = 1;
+        g.w_smem = 0;
+        g.smem_bytes = fixed + g.n_h * g.h_bytes;
+        if (g.smem_bytes > kSmemLimit) return false;
+        g.tiles = (long long)g.strips * g.windows * g.frames;
+        found = true;
+    } else if (g.ctr) {
         // the centre tap needs no halo: a window is 256 consecutive positions of a frame's flattened
         // H x W plane (one strip as wide as the image, rows of pitch W), staged by one 32 KB box
         g.Wt = g.P = W_out; g.HR = 1; g.strips = 1;
@@ -1082,6 +1162,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.C_in = d.C_in; a.C_out = d.C_out; a.N = d.N; a.D = d.D; a.H = d.H; a.W = d.W;
     a.H_out = H_out; a.W_out = W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
     a.sub2 = g.sub2; a.out_nchw = out_nchw; a.yH = yH; a.yW = yW; a.w_smem = g.w_smem;
+    a.stage_warp = g.stage_warp;
     a.frame_inner = g.ctr;
     a.g_f32 = d.kernel == X3_KERNEL_HEAD_SPLIT ? 1 : 0;
     a.has_carry = carry != nullptr;
@@ -1103,8 +1184,9 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     } else {
         const uint64_t frames_x = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
         // the flat form views each frame as one row of H*W positions
-        const uint64_t mw = g.ctr ? (uint64_t)d.H * d.W : (uint64_t)d.W, mh = g.ctr ? 1 : (uint64_t)d.H;
-        const uint32_t bw = g.ctr ? (uint32_t)kBNP : (uint32_t)g.P, bh = g.ctr ? 1u : (uint32_t)g.HR;
+        const bool flat = g.ctr && !g.stn;
+        const uint64_t mw = flat ? (uint64_t)d.H * d.W : (uint64_t)d.W, mh = flat ? 1 : (uint64_t)d.H;
+        const uint32_t bw = flat ? (uint32_t)kBNP : (uint32_t)g.P, bh = flat ? 1u : (uint32_t)g.HR;
         st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh);
         if (st != X3_OK) return st;
         if (carry) {
@@ -1145,6 +1227,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     }
     if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, true>
                        : igemm_cl_kernel<false, false, false, false, false, false, true>;
+    else if (g.stn) k = igemm_cl_kernel<true, false, false, true, false, false, false, true>;
     else if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
     else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
     else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;

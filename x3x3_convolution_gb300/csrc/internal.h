@@ -74,6 +74,8 @@ struct ClGeom {
     int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
     int mc;                      // 1: clusters of two CTAs sharing each weight block by multicast
     int w2;                      // 1: a tile is two consecutive windows sharing every weight K slice
+    int stn;                     // 1: head with the spatial stencil in the epilogue (centre-tap MMAs)
+    int stage_warp;              // epilogue staging bytes per warp
     long long tiles;
     int smem_bytes, grid;
 };
