@@ -58,8 +58,8 @@ constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + p
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
 constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
-constexpr int kStnPitch = 97;     // STN: fp32 staging row (96 TMEM columns + pad) per lane
-constexpr int kStnStageBytes = 32 * kStnPitch * 4;
+constexpr int kStnPitch = 67;     // STN: fp32 staging row (the 66 TMEM columns a chunk reads + pad) per tap row
+constexpr int kStnStageBytes = 27 * kStnPitch * 4;  // 27 rows: 9 taps x 3 channels
 
 struct ClArgs {
     int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
@@ -695,10 +695,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 } else if (STN) {
                     // Window position m = 16a + c holds G at plane row a, column c (row 0 and 15, column 0
                     // and 15 are halo). Per chunk of 32 output positions, the warp stages TMEM columns
-                    // [32k - 32, 32k + 64) of its rows (9 taps x 3 channels) as S[lane][0..95]; thread
-                    // t then sums, for output m = 32k + t, bias + the nine taps in (i, j) order at
-                    // m + (i-1)*16 + (j-1), all inside the staged range since |offset| <= 17.
-                    float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [32][kStnPitch]
+                    // [32k - 17, 32k + 49) of its 27 rows (9 taps x 3 channels) as S[lane][0..65];
+                    // thread t then sums, for output m = 32k + t, bias + the nine taps in (i, j) order
+                    // at m + (i-1)*16 + (j-1), all inside the staged range since |offset| <= 17.
+                    float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [27][kStnPitch]
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
                     const int oh_base = tc.win * (a.HR - 2) - 1, ow_base = ow0 - 1;
                     const size_t W2o = 2 * (size_t)a.W_out;
@@ -711,8 +711,13 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             uint32_t v[32];
                             ptx::tmem_ld32(tq + (uint32_t)col, v);
                             ptx::tmem_ld_wait();
+                            if (lane < 27) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) S[lane * kStnPitch + part * 32 + j] = __uint_as_float(v[j]);
+                                for (int j = 0; j < 32; ++j) {
+                                    const int sc = part * 32 + j - 15;  // staged column of TMEM column col + j
+                                    if (sc >= 0 && sc < 66) S[lane * kStnPitch + sc] = __uint_as_float(v[j]);
+                                }
+                            }
                         }
                         __syncwarp();
                         const int m = 32 * k + lane;
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 for (int i = 0; i < 3; ++i)
 #pragma unroll
                                     for (int j = 0; j < 3; ++j)
-                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + 32 + lane + (i - 1) * 16 + (j - 1)];
+                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + 17 + lane + (i - 1) * 16 + (j - 1)];
                                 const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
                                 y[((row0 + 2 * (size_t)oh + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
                                     cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, acc)));
@@ -981,10 +986,11 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         g.windows = (H_out + 13) / 14;
         g.win_adv = 14 * 16;
         g.h_bytes = g.h_tx_bytes = kCtrW + kWBlock;
-        g.n_h = 3; g.n_w = 1;
+        g.n_h = (kSmemLimit - fixed) / g.h_bytes < 4 ? (kSmemLimit - fixed) / g.h_bytes : 4;
+        g.n_w = 1;
         g.w_smem = 0;
         g.smem_bytes = fixed + g.n_h * g.h_bytes;
-        if (g.smem_bytes > kSmemLimit) return false;
+        if (g.n_h < 2) return false;
         g.tiles = (long long)g.strips * g.windows * g.frames;
         found = true;
     } else if (g.ctr) {
