@@ -384,6 +384,38 @@ size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers
     return n_layers > 1 ? (n_layers > 2 ? 2 * biggest : biggest) : 0;
 }
 
+// The stack driver's side stream for carry copies, one per thread and device: calls from different
+// threads never share its events. Created on first use and kept until the process exits.
+struct SideStream {
+    static constexpr int kEvents = 4;  // a wait always names one of the last two layers' copies
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork[kEvents] = {};
+    cudaEvent_t done[kEvents] = {};
+};
+
+static x3_status side_stream(SideStream** out) {
+    constexpr int kMaxDevices = 64;
+    static thread_local SideStream per_dev[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "side stream: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(X3_ERR_UNSUPPORTED, "side stream: device %d out of range", dev);
+    SideStream& ss = per_dev[dev];
+    if (!ss.s) {
+        e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+        for (int k = 0; k < SideStream::kEvents && e == cudaSuccess; ++k) {
+            e = cudaEventCreateWithFlags(&ss.fork[k], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.done[k], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) {
+            ss = SideStream{};  // leaks what was made; the next call retries
+            return fail(X3_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+        }
+    }
+    *out = &ss;
+    return X3_OK;
+}
+
 // Copy the last two frames of the sequence [history, input] of a layer into its carry buffer.
 static x3_status update_carry(const x3_conv_plan* p, const void* input, void* carry, int history_valid,
                               cudaStream_t s) {
@@ -466,18 +498,51 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
         return X3_OK;
     }
     const size_t half = n_layers > 2 ? need / 2 : need;
+    // Layer i's carry copy reads its input and overwrites carries[i], so it follows layer i's kernel;
+    // it runs on a side stream, beside the next layers, until a kernel is about to overwrite the
+    // buffer it reads (the ping-pong buffer layer i+1 writes when i >= 1). The caller's stream waits
+    // for every copy before the call's work ends.
+    SideStream* side = nullptr;
+    bool any_carry = false;
+    for (int i = 0; i < n_layers; ++i) any_carry |= plans[i]->d.dims == 3 && carries && carries[i];
+    if (any_carry) {
+        x3_status st = side_stream(&side);
+        if (st != X3_OK) return st;
+    }
+    int pending[2] = {-1, -1};  // per workspace half: the layer whose carry copy reads it, or -1
+    int last_copy = -1;
     const void* in = x;
     for (int i = 0; i < n_layers; ++i) {
-        void* out = (i == n_layers - 1) ? y : (char*)workspace + (size_t)(i % 2) * half;
+        const int ob = i % 2;
+        void* out = (i == n_layers - 1) ? y : (char*)workspace + (size_t)ob * half;
+        cudaError_t e = cudaSuccess;
+        if (i < n_layers - 1 && pending[ob] >= 0) {
+            e = cudaStreamWaitEvent(s, side->done[pending[ob] % SideStream::kEvents], 0);
+            pending[ob] = -1;
+        }
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "conv_stack_forward: %s", cudaGetErrorString(e));
         void* carry = (plans[i]->d.dims == 3 && carries) ? carries[i] : nullptr;
         x3_status st = conv_forward(plans[i], in, (carry && carry_valid) ? carry : nullptr, w_packed[i],
                                     bias ? bias[i] : nullptr, out, stream);
         if (st != X3_OK) return st;
         if (carry) {
-            st = update_carry(plans[i], in, carry, carry_valid, s);
+            const int k = i % SideStream::kEvents;
+            e = cudaEventRecord(side->fork[k], s);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork[k], 0);
+            if (e != cudaSuccess) return fail(X3_ERR_CUDA, "conv_stack_forward: %s", cudaGetErrorString(e));
+            st = update_carry(plans[i], in, carry, carry_valid, side->s);
             if (st != X3_OK) return st;
+            e = cudaEventRecord(side->done[k], side->s);
+            if (e != cudaSuccess) return fail(X3_ERR_CUDA, "conv_stack_forward: %s", cudaGetErrorString(e));
+            if (i >= 1) pending[(i - 1) % 2] = i;  // layer i's input is the half layer i-1 wrote
+            last_copy = i;
         }
         in = out;
+    }
+    if (last_copy >= 0) {
+        // copies run in order on the side stream: waiting for the last one covers all of them
+        cudaError_t e = cudaStreamWaitEvent(s, side->done[last_copy % SideStream::kEvents], 0);
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "conv_stack_forward: %s", cudaGetErrorString(e));
     }
     return X3_OK;
 }
