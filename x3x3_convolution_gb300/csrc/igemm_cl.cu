@@ -255,6 +255,12 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // Launched as a programmatic dependent, this grid may start while the previous kernel of the
+    // stream is still running: the set-up above (barriers, TMEM) overlaps its tail, and nothing of
+    // global memory is read or written before the wait. The next kernel may then be scheduled; it
+    // waits in the same way before it touches this one's output.
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     if (MC) ptx::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
@@ -1241,8 +1247,24 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     else k = bf16 ? igemm_cl_kernel<true, false, false> : igemm_cl_kernel<false, false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
-    k<<<g.grid, g.nchw ? 320 : 192, g.smem_bytes, s>>>(mx, mc, a);
-    e = cudaGetLastError();
+    // a programmatic dependent of the previous kernel in the stream (the kernel waits for it before
+    // touching global memory); X3CONV_PDL=0 in the environment launches it fully serialised
+    static const bool pdl = [] {
+        const char* v = getenv("X3CONV_PDL");
+        return !(v && !strcmp(v, "0"));
+    }();
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)g.grid);
+    cfg.blockDim = dim3(g.nchw ? 320u : 192u);
+    cfg.dynamicSmemBytes = (size_t)g.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, k, mx, mc, a);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl launch: %s", cudaGetErrorString(e));
     return X3_OK;
 }

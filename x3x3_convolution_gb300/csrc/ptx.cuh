@@ -18,6 +18,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have completed and their
+// memory is visible; let the next grid of the stream (when launched as a programmatic dependent) be
+// scheduled once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
