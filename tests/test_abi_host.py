@@ -269,12 +269,20 @@ def test_nchw_layers_have_channels_last_forms(lib, name):
         g = x3.conv_plan_describe(p)
         s = g["shadow"]
         P, HR, Wt = s["P"], s["HR"], s["Wt"]
-        assert P == Wt + 2 and P <= 256 and HR <= 256
-        for win in range(min(s["windows"], 4 * P)):
-            need = (256 * win) % P + 255 + 2 * P + 2 + 1
-            assert need <= HR * P
-        assert s["strips"] * Wt >= cfg["W"] and s["windows"] * 256 >= cfg["H"] * P
-        assert s["sub2"] == (cfg.get("stride", 1) == 2)
+        s2 = cfg.get("stride", 1) == 2
+        assert s["s2"] == s2 and s["sub2"] == 0  # stride 2 from the four input phases
+        if s2:
+            # output raster of pitch Wt + 1; each phase box spans 2P x 2HR input positions (<= 256)
+            Ho, Wo = (cfg["H"] + 1) // 2, (cfg["W"] + 1) // 2
+            assert P == Wt + 1 and 2 * P <= 256 and 2 * HR <= 256
+            for win in range(min(s["windows"], 4 * P)):
+                assert (256 * win) % P + 255 + P + 1 + 1 <= HR * P  # shifts of one row and one column
+        else:
+            Ho, Wo = cfg["H"], cfg["W"]
+            assert P == Wt + 2 and P <= 256 and HR <= 256
+            for win in range(min(s["windows"], 4 * P)):
+                assert (256 * win) % P + 255 + 2 * P + 2 + 1 <= HR * P
+        assert s["strips"] * Wt >= Wo and s["windows"] * 256 >= Ho * P
         assert s["n_chunks"] == (cfg["C_in"] + 63) // 64
         assert s["n_tiles"] == (cfg["C_out"] + (63 if s["m64"] else 127)) // (64 if s["m64"] else 128)
         assert s["smem_bytes"] <= 232448 and s["w_off"] % 256 == 0

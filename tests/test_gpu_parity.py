@@ -94,10 +94,35 @@ def test_conv2d_nhwc(case, variant, dtype):
     L = synth.make_layer([key], 2, Ci, Co, dtype, stride=s, act=act, variant=variant)
     got, conv = run2d(x, L, layout="NHWC")
     g = x3.conv_plan_describe(conv.plan)
-    assert g["kernel"] == "igemm_tcgen05_sw128" and g["sub2"] == (s == 2) and g["m64"] == (Co <= 64 and Ci <= 64)
+    assert g["kernel"] == "igemm_tcgen05_sw128" and g["s2"] == (s == 2) and g["m64"] == (Co <= 64 and Ci <= 64)
     ref = oracle2d(x, L, layout="NHWC")
     if variant == "int":
         assert_exact(got, ref, dtype)
+    else:
+        assert_close(got, ref)
+
+
+@pytest.mark.parametrize("variant", ["int", "random"])
+@pytest.mark.parametrize("case", [(4, 64, 64, 64, 64, "relu"), (1, 64, 64, 33, 97, "none"),
+                                  (2, 8, 32, 17, 255, "relu"), (1, 64, 128, 20, 66, "relu"),
+                                  (1, 96, 64, 15, 40, "none"), (1, 136, 200, 9, 31, "none")], ids=str)
+@pytest.mark.parametrize("form", ["phases", "raster"])
+def test_conv2d_nhwc_stride2_forms(case, variant, form, monkeypatch):
+    """Stride 2 on the channels-last engine in both forms: from the four input phases (element-strided
+    boxes; the default), and with X3CONV_S2=0 as the stride-1 raster with even positions kept. Odd
+    input sizes put the bottom and right taps in the zero padding; C_out > 64 takes the 128-row form
+    and C_in > 64 two chunks per phase."""
+    monkeypatch.setenv("X3CONV_S2", "1" if form == "phases" else "0")
+    N, Ci, Co, H, W, act = case
+    key = 2700 + sum(case[:5])
+    x = synth.activation([key, 0], (N, H, W, Ci), "bf16", variant, ("uniform", -1.0, 1.0))
+    L = synth.make_layer([key], 2, Ci, Co, "bf16", stride=2, act=act, variant=variant)
+    got, conv = run2d(x, L, layout="NHWC")
+    g = x3.conv_plan_describe(conv.plan)
+    assert (g["s2"], g["sub2"]) == ((1, 0) if form == "phases" else (0, 1))
+    ref = oracle2d(x, L, layout="NHWC")
+    if variant == "int":
+        assert_exact(got, ref, "bf16")
     else:
         assert_close(got, ref)
 

@@ -143,9 +143,12 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
     }
     if (choice != X3_KERNEL_DIRECT && !(force && !strcmp(force, "igemm_nsub"))) {
         // 2D channels-last layers of any width run on the swapped engine (the M = 64 form for at most
-        // 64 output channels); stride 2 as the stride-1 raster with even positions kept
+        // 64 output channels); stride 2 from the four input phases, else as the stride-1 raster with
+        // even positions kept
         const bool nhwc2d = p->d.dims == 2 && p->d.layout == X3_NHWC;
-        if (nhwc2d && p->d.stride == 2) {
+        if (nhwc2d && p->d.stride == 2 && igemm_cl_plan(p, p->num_sms, true)) {
+            cl_ok = true;
+        } else if (nhwc2d && p->d.stride == 2) {
             x3_conv_plan q = *p;
             q.d.stride = 1;
             q.H_out = q.d.H;
@@ -184,13 +187,18 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
         x3_conv_plan q = *p;
         q.d.layout = X3_NHWC;
         q.d.C_in = (q.d.C_in + 7) / 8 * 8;
-        q.d.stride = 1;
-        q.H_out = q.d.H;
-        q.W_out = q.d.W;
-        if (igemm_cl_plan(&q, p->num_sms, true)) {
+        // stride 2 from the four input phases when the engine takes it, else as the stride-1 raster
+        bool q_ok = p->d.stride == 2 && igemm_cl_plan(&q, p->num_sms, true);
+        if (!q_ok) {
+            q.d.stride = 1;
+            q.H_out = q.d.H;
+            q.W_out = q.d.W;
+            q_ok = igemm_cl_plan(&q, p->num_sms, true);
+            q.cl.sub2 = p->d.stride == 2 ? 1 : 0;
+        }
+        if (q_ok) {
             p->has_shadow = 1;
             p->cl_shadow = q.cl;
-            p->cl_shadow.sub2 = p->d.stride == 2 ? 1 : 0;
             // the channels-last engine's weight blocks; the NCHW form of the same engine uses the
             // same blocks (n_chunks agree: C_in and its round-up to 8 need the same 64-channel chunks)
             if (p->kind == K_IGEMM_CL && !p->cl.kwm && !p->cl.ctr && !q.cl.m64 && p->cl.n_chunks == q.cl.n_chunks &&
@@ -231,10 +239,10 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, \"mc\": %d, "
-                        "\"m64\": %d, \"sub2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d}",
+                        "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.mc, c.m64, c.sub2, c.ctr, c.w2, c.stn);
+                        c.mc, c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
@@ -260,9 +268,9 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
         const ClGeom& c = plan->cl_shadow;
         const int m = snprintf(tmp + n - 1, sizeof tmp - (size_t)(n - 1),
                                ", \"shadow\": {\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, "
-                               "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"n_h\": %d, \"sub2\": %d, \"tiles\": %lld, "
+                               "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"n_h\": %d, \"sub2\": %d, \"s2\": %d, \"tiles\": %lld, "
                                "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d}}",
-                               c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.n_h, c.sub2, c.tiles,
+                               c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.n_h, c.sub2, c.s2, c.tiles,
                                c.smem_bytes, c.grid, plan->shadow_w_off, c.m64);
         n = n - 1 + m;
     }

@@ -136,6 +136,18 @@ __device__ __forceinline__ bool cl_wait(uint32_t bar, uint32_t parity, volatile 
     }
 }
 
+// Stride 2: the taps that read input phase ph = 2a + b (a: odd input rows, b: odd input columns) and
+// their shifts in the phase's raster. Output row oh reads input rows 2oh - 1 + kh: kh = 0 and 2 are
+// odd rows (phase rows oh - 1 and oh), kh = 1 the even row oh; the phase raster starts one row and
+// one column before the output window, so the shift is 0 for kh = 0 and 1 otherwise (same for kw).
+__device__ __forceinline__ int s2_ntaps(int ph) { return ((ph >> 1) ? 2 : 1) * ((ph & 1) ? 2 : 1); }
+__device__ __forceinline__ void s2_tap(int ph, int i, int& kh, int& kw) {
+    const int nw = (ph & 1) ? 2 : 1;
+    const int ih = i / nw, iw = i - ih * nw;
+    kh = (ph >> 1) ? 2 * ih : 1;
+    kw = (ph & 1) ? 2 * iw : 1;
+}
+
 __device__ __forceinline__ float cl_act(float v, int act) {
     if (act == X3_ACT_RELU) return fmaxf(v, 0.0f);
     if (act == X3_ACT_CLAMP1) return fminf(1.0f, fmaxf(-1.0f, v));
@@ -190,8 +202,12 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // 32q + 9cl + tap for channel 3q + cl, so each epilogue warp holds all nine taps of its three channels;
 // the epilogue adds, in fp32, the bias and the nine taps' values at the shifted window positions
 // (staged through shared memory), clamps, rounds once and writes the unpatchified RGB pixels.
+// S2 (2D channels-last, stride 2): the raster is the output plane (pitch Wt + 1) and the input is
+// staged as its four phases, even or odd rows by even or odd columns, each box loaded by the TMA
+// unit with element strides of 2. A phase is one pipeline group that feeds only the taps reading it
+// (one, two, two and four of the nine), each at a shift of 0 or 1 row and column (s2_tap).
 template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false, bool W2 = false,
-          bool STN = false>
+          bool STN = false, bool S2 = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     // slower with it, so they keep the natural order). Both CTAs of a cluster share one order. Only
     // the fp32 summation order depends on it.
     constexpr int kTapsK = KWM ? 3 : (CTR ? 1 : 9);
-    const int n_groups = a.KT * a.n_chunks;
+    const int n_groups = (S2 ? 4 : a.KT) * a.n_chunks;  // S2: (phase, chunk) groups
     const int k_id = KWM ? (int)(MC ? blockIdx.x >> 1 : blockIdx.x) : 0;
     const int rot_g = k_id % n_groups, rot_t = (k_id / n_groups) % kTapsK;
 
@@ -344,14 +360,22 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 ptx::bulk_load(sH + sh * a.h_bytes + (uint32_t)kCtrW,
                                                a.w + ((size_t)kt * a.n_chunks + cc) * (size_t)kWBlock, (uint32_t)kWBlock,
                                                bar_h_full + 8 * sh);
-                            } else
+                            } else if (S2)  // phase kt = 2a + b: input rows 2(r0 - 1 + v) + a, columns 2(ow0 - 1 + u) + b
+                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK,
+                                                 2 * (ow0 - 1) + (kt & 1), 2 * (r0 - 1) + (kt >> 1), fcoord);
+                            else
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
                         }
                         const uint8_t* wblk =
-                            a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
-                        for (int ti = 0; ti < ((M64 || CTR) ? 0 : kTapsK); ++ti) {
-                            const int tap = KWM ? (ti + rot_t < kTapsK ? ti + rot_t : ti + rot_t - kTapsK) : ti;
+                            a.w + ((((size_t)tc.nt * a.KT + (S2 ? 0 : kt)) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
+                        for (int ti = 0; ti < ((M64 || CTR) ? 0 : (S2 ? s2_ntaps(kt) : kTapsK)); ++ti) {
+                            int tap = KWM ? (ti + rot_t < kTapsK ? ti + rot_t : ti + rot_t - kTapsK) : ti;
+                            if (S2) {  // the phase's taps, in the MMA issuer's order
+                                int kh, kw;
+                                s2_tap(kt, ti, kh, kw);
+                                tap = kh * 3 + kw;
+                            }
                             const uint32_t sw = w_cnt % a.n_w;
                             if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
@@ -441,7 +465,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         ptx::tc_fence_after();
                         a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
                     }
-                    const uint32_t row_addr = CTR ? hbase : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u;
+                    const uint32_t row_addr =
+                        CTR ? hbase
+                            : (S2 ? hbase + (uint32_t)(pos_off + (kh ? a.P : 0) + (kw ? 1 : 0)) * 128u
+                                  : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u);
 #pragma unroll
                     for (int ks = 0; ks < kCK / 16; ++ks) {
                         if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
@@ -484,6 +511,22 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         if (!ok) break;
                         ptx::mma_commit(bar_h_empty + 8 * sh);
                         ++h_cnt;
+                    }
+                } else if constexpr (S2) {
+                    // stride 2: (phase, chunk) groups, each with the taps that read the phase
+                    for (int ph = 0; ph < 4 && ok; ++ph) {
+                        for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                            uint32_t sh, hbase;
+                            if (!group_begin(sh, hbase)) { ok = false; break; }
+                            for (int i = 0; i < s2_ntaps(ph); ++i) {
+                                int kh, kw;
+                                s2_tap(ph, i, kh, kw);
+                                if (!tap_mmas(cc, 0, kh, kw, hbase)) { ok = false; break; }
+                            }
+                            if (!ok) break;
+                            ptx::mma_commit(bar_h_empty + 8 * sh);
+                            ++h_cnt;
+                        }
                     }
                 } else {
                     for (int kt = 0; kt < a.KT && ok; ++kt) {
@@ -889,8 +932,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// es = 2: every second position along W and H (the box spans 2 box_w x 2 box_h positions of the
+// tensor and lands box_w x box_h rows in shared memory); box_w and box_h are the landed counts.
 x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, uint64_t W, uint64_t H,
-                       uint64_t F, uint32_t box_w, uint32_t box_h) {
+                       uint64_t F, uint32_t box_w, uint32_t box_h, uint32_t es_wh = 1) {
     static EncodeTiledFn fn = nullptr;
     if (!fn) {
         void* f = nullptr;
@@ -905,8 +950,8 @@ x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, u
     }
     cuuint64_t gd[4] = {C, W, H, F};
     cuuint64_t gs[3] = {C * 2, C * 2 * W, C * 2 * W * H};
-    cuuint32_t bd[4] = {(cuuint32_t)kCK, box_w, box_h, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
+    cuuint32_t bd[4] = {(cuuint32_t)kCK, box_w * es_wh, box_h * es_wh, 1};
+    cuuint32_t es[4] = {1, es_wh, es_wh, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                     const_cast<void*>(ptr), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -944,9 +989,19 @@ x3_status encode_nchw_raw(CUtensorMap* m, bool bf16, const void* ptr, uint64_t W
 
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     const x3_conv_desc& d = p->d;
-    if (d.stride != 1) return false;
     ClGeom g;
     memset(&g, 0, sizeof g);
+    // stride 2: 2D channels-last layers only, from their four input phases (X3CONV_S2=0 in the
+    // environment declines it, so that the caller computes them as the stride-1 raster instead)
+    if (d.stride == 2) {
+        const char* s2_env = getenv("X3CONV_S2");
+        if (d.dims != 2 || d.layout != X3_NHWC || d.unpatchify2x2 || d.kernel == X3_KERNEL_HEAD_STENCIL ||
+            (s2_env && !strcmp(s2_env, "0")))
+            return false;
+        g.s2 = 1;
+    } else if (d.stride != 1) {
+        return false;
+    }
     // NCHW 2D input (raw tiles transposed in shared memory) or channels-last input (swizzled TMA boxes)
     g.nchw = (d.dims == 2 && d.layout == X3_NCHW) ? 1 : 0;
     if (g.nchw) {
@@ -979,7 +1034,11 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     long long best_cost = -1;
     int cands[80], nc = 0;
     for (int k = 1; k <= 64; ++k) cands[nc++] = (W_out + k - 1) / k;
-    cands[nc++] = 30; cands[nc++] = 62; cands[nc++] = 126; cands[nc++] = 254;  // P divides 256
+    if (g.s2) {  // P = Wt + 1 divides 256
+        cands[nc++] = 31; cands[nc++] = 63; cands[nc++] = 127;
+    } else {     // P = Wt + 2 divides 256
+        cands[nc++] = 30; cands[nc++] = 62; cands[nc++] = 126; cands[nc++] = 254;
+    }
     // layers with at most 64 output channels (when asked for): the M = 64 form with every weight block
     // resident in shared memory; if no tiling leaves room for them, the 128-row form
     g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
@@ -1023,15 +1082,17 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     const bool light = g.m64 && d.C_in <= 16;
     for (int ci = 0; ci < nc; ++ci) {
         const int Wt = g.nchw ? (cands[ci] + 7) / 8 * 8 : cands[ci];  // NCHW: strips start 16-byte aligned
-        const int P = Wt + 2;
-        if (P > 256 || (g.nchw && Wt + 16 > 256)) continue;
+        // stride 2: tap shifts of 0 or 1 in each phase raster, and the phase boxes span 2P x 2HR
+        // input positions (a box side is at most 256)
+        const int P = g.s2 ? Wt + 1 : Wt + 2;
+        if (P > (g.s2 ? 128 : 256) || (g.nchw && Wt + 16 > 256)) continue;
         // halo rows of a 256-position window starting anywhere in a row, plus one above and below
         // furthest B row read: window start offset within its row (0 when windows of 256 tile the
         // rows exactly), the window's last column, kh = 2 (+2P) and, unless folded into M, kw = 2 (+2)
         const int pos_off_max = (g.win_adv == 256 && (256 % P) == 0) ? 0 : P - 1;
-        const int need_pos = pos_off_max + 255 + 2 * P + (g.kwm ? 0 : 2) + 1;
+        const int need_pos = g.s2 ? pos_off_max + 255 + P + 1 + 1 : pos_off_max + 255 + 2 * P + (g.kwm ? 0 : 2) + 1;
         const int HR = (need_pos + P - 1) / P;
-        if (HR > 256) continue;
+        if (HR > (g.s2 ? 128 : 256)) continue;
         const int pos = HR * P > need_pos ? HR * P : need_pos;
         const int h_bytes = (pos * 128 + 1023) / 1024 * 1024;
         // NCHW raw slices: 16 channels x HR rows x (Wt + 16) columns, two stages
@@ -1115,7 +1176,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
     // the weights measured no faster on any layer of the decoder (each SM still receives every block).
     const char* cl_env = getenv("X3CONV_CLUSTER");
-    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && !g.w2 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
+    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && !g.w2 && !g.s2 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
@@ -1199,7 +1260,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         const bool flat = g.ctr && !g.stn;
         const uint64_t mw = flat ? (uint64_t)d.H * d.W : (uint64_t)d.W, mh = flat ? 1 : (uint64_t)d.H;
         const uint32_t bw = flat ? (uint32_t)kBNP : (uint32_t)g.P, bh = flat ? 1u : (uint32_t)g.HR;
-        st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh);
+        st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh, g.s2 ? 2u : 1u);
         if (st != X3_OK) return st;
         if (carry) {
             st = encode_sw128(&mc, bf16, carry, d.C_in, mw, mh, (uint64_t)d.N * 2, bw, bh);
@@ -1241,6 +1302,10 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
                        : igemm_cl_kernel<false, false, false, false, false, false, true>;
     else if (g.stn) k = igemm_cl_kernel<true, false, false, true, false, false, false, true>;
     else if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
+    else if (g.s2 && g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true, false, false, false, true>
+                                     : igemm_cl_kernel<false, false, false, false, true, false, false, false, true>;
+    else if (g.s2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
+                            : igemm_cl_kernel<false, false, false, false, false, false, false, false, true>;
     else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
     else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
     else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false> : igemm_cl_kernel<false, true, false>;
@@ -1284,8 +1349,9 @@ x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const voi
     x3_conv_desc d = p->d;
     d.layout = X3_NHWC;
     d.C_in = (d.C_in + 7) / 8 * 8;
-    d.stride = 1;
-    return launch_cl(d, p->cl_shadow, d.H, d.W, p->H_out, p->W_out, out_nchw, x, nullptr,
+    // S2: the raster is the output plane; sub2: the stride-1 raster over the input plane
+    const int rh = p->cl_shadow.s2 ? p->H_out : d.H, rw = p->cl_shadow.s2 ? p->W_out : d.W;
+    return launch_cl(d, p->cl_shadow, rh, rw, p->H_out, p->W_out, out_nchw, x, nullptr,
                      (const uint8_t*)w_packed + p->shadow_w_off, bias, y, s);
 }
 

@@ -70,6 +70,7 @@ struct ClGeom {
     int ngroups;                 // kwm: groups of 10 output channels (one TMEM lane quarter each)
     int ctr;                     // 1: centre spatial tap only (temporal pass of the two-pass head)
     int sub2;                    // 1: stride 2 computed as the stride-1 raster, even positions kept
+    int s2;                      // 1: stride 2 from the four input phases (element-strided TMA boxes)
     int m64;                     // 1: M = 64 MMAs (at most 64 output channels), weights resident
     int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
     int mc;                      // 1: clusters of two CTAs sharing each weight block by multicast
