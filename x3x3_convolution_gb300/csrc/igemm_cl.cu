@@ -88,25 +88,30 @@ struct ClTile {
     int nt, win, strip, fr;
 };
 
-__device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long t) {
+// The planner keeps tile counts below 2^31, so the decode runs in 32-bit unsigned arithmetic (a 64-bit
+// division is a long software sequence, and every role of the kernel decodes every tile).
+__device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
     ClTile c;
+    uint32_t t = (uint32_t)tile;
     if (a.frame_inner) {
         // frames fastest: the output frames of one window are in flight together, so the input frames
         // they share (three temporal taps each) are read from DRAM once and then hit in L2
-        c.fr = (int)(t % a.frames);
-        t /= a.frames;
-        c.nt = (int)(t % a.n_tiles);
-        t /= a.n_tiles;
-        c.win = (int)(t % a.windows);
-        c.strip = (int)(t / a.windows);
+        const uint32_t fr = (uint32_t)a.frames, nt = (uint32_t)a.n_tiles, wn = (uint32_t)a.windows;
+        c.fr = (int)(t % fr);
+        t /= fr;
+        c.nt = (int)(t % nt);
+        t /= nt;
+        c.win = (int)(t % wn);
+        c.strip = (int)(t / wn);
         return c;
     }
-    c.nt = (int)(t % a.n_tiles);
-    t /= a.n_tiles;
-    c.win = (int)(t % a.windows);
-    t /= a.windows;
-    c.strip = (int)(t % a.strips);
-    t /= a.strips;
+    const uint32_t nt = (uint32_t)a.n_tiles, wn = (uint32_t)a.windows, st = (uint32_t)a.strips;
+    c.nt = (int)(t % nt);
+    t /= nt;
+    c.win = (int)(t % wn);
+    t /= wn;
+    c.strip = (int)(t % st);
+    t /= st;
     c.fr = (int)t;
     return c;
 }
@@ -684,11 +689,12 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 } else if (M64) {
                     // M = 64: this quarter's 16 channels x 32 positions per chunk come in the MMA
                     // fragment layout (16 lanes x 256 bits, four column groups); each thread rounds its
-                    // pairs of positions into packed 32-bit words, stmatrix.trans writes them as
-                    // [position][16 channels] rows of the warp's staging block, and each position's
-                    // 32 bytes go out as two 16-byte stores. The next chunk's TMEM load is in flight
-                    // while this one is processed.
-                    const uint32_t wst = sStage + (uint32_t)(ew * a.stage_warp);  // [32][16] x 2 B
+                    // pairs of positions into packed 32-bit words and stmatrix.trans writes them as
+                    // [position][16 channels] rows, four chunks into four 1 KB slots of the warp's
+                    // staging block before one warp barrier; then each position's 32 bytes go out as
+                    // two 16-byte stores, the sixteen loads and stores of the four chunks in flight
+                    // together. The second half's TMEM load is in flight while the first is processed.
+                    const uint32_t wst = sStage + (uint32_t)(ew * a.stage_warp);  // [4][32][16] x 2 B
                     const uint8_t* wstp = stage_ptr + ew * a.stage_warp;
                     const float b0 = m64_b0, b1 = m64_b1;
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
@@ -700,7 +706,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // its offset by a float reciprocal (exact: offsets < 512, pitch <= 256)
                     const int oh0 = m0 / a.P, c00 = m0 - oh0 * a.P;
                     uint16_t* yf = y + ((size_t)n * a.dout + t) * (size_t)a.yH * a.yW * a.C_out;
-                    auto process = [&](int chunk, const uint32_t (&v)[16]) {
+                    auto stage = [&](int slot, const uint32_t (&v)[16]) {
                         uint32_t h[8];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -709,24 +715,29 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             h[2 * i + 1] = cl_pack2<BF16>(fminf(fmaxf(__uint_as_float(v[4 * i + 2]) + b1, act_lo), act_hi),
                                                           fminf(fmaxf(__uint_as_float(v[4 * i + 3]) + b1, act_lo), act_hi));
                         }
-                        __syncwarp();
-                        ptx::stsm_x4_trans(st_addr, h[0], h[1], h[2], h[3]);            // positions 0..15
-                        ptx::stsm_x4_trans(st_addr + 16u * 32u, h[4], h[5], h[6], h[7]);  // positions 16..31
-                        __syncwarp();
+                        const uint32_t sa = st_addr + (uint32_t)slot * 1024u;
+                        ptx::stsm_x4_trans(sa, h[0], h[1], h[2], h[3]);            // positions 0..15
+                        ptx::stsm_x4_trans(sa + 16u * 32u, h[4], h[5], h[6], h[7]);  // positions 16..31
+                    };
+                    auto drain = [&](int chunk0) {
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int piece = k * 32 + lane;
-                            const int pos = piece >> 1, half = piece & 1;
-                            const int cc = c00 + chunk * 32 + pos;
-                            const int dr = __float2int_rz(((float)cc + 0.5f) * inv_p);
-                            const int oh = oh0 + dr, c = cc - dr * a.P;
-                            const int ow = ow0 + c;
-                            const int co = q * 16 + half * 8;
-                            if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
-                                !(a.sub2 && ((oh | ow) & 1))) {
-                                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
-                                const uint4 val = *reinterpret_cast<const uint4*>(wstp + pos * 32 + half * 16);
-                                *reinterpret_cast<uint4*>(yf + ((size_t)yh * a.yW + yw) * a.C_out + co) = val;
+                        for (int slot = 0; slot < 4; ++slot) {
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const int piece = k * 32 + lane;
+                                const int pos = piece >> 1, half = piece & 1;
+                                const int cc = c00 + (chunk0 + slot) * 32 + pos;
+                                const int dr = __float2int_rz(((float)cc + 0.5f) * inv_p);
+                                const int oh = oh0 + dr, c = cc - dr * a.P;
+                                const int ow = ow0 + c;
+                                const int co = q * 16 + half * 8;
+                                if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
+                                    !(a.sub2 && ((oh | ow) & 1))) {
+                                    const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
+                                    const uint4 val =
+                                        *reinterpret_cast<const uint4*>(wstp + slot * 1024 + pos * 32 + half * 16);
+                                    *reinterpret_cast<uint4*>(yf + ((size_t)yh * a.yW + yw) * a.C_out + co) = val;
+                                }
                             }
                         }
                     };
@@ -736,11 +747,17 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) ptx::tmem_ld16x256b_x4(tq + (uint32_t)((4 + c) * 32), rb[c]);
+                    __syncwarp();  // the previous tile's loads from the slots are done
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) process(c, ra[c]);
+                    for (int c = 0; c < 4; ++c) stage(c, ra[c]);
+                    __syncwarp();
+                    drain(0);
                     ptx::tmem_ld_wait();
+                    __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) process(4 + c, rb[c]);
+                    for (int c = 0; c < 4; ++c) stage(c, rb[c]);
+                    __syncwarp();
+                    drain(4);
                 } else if (STN) {
                     // Window position m = 16a + c holds G at plane row a, column c (row 0 and 15, column 0
                     // and 15 are halo). Per chunk of 32 output positions, the warp stages TMEM columns
@@ -1171,6 +1188,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
             }
         }
     }
+    if (g.tiles >= (1LL << 31)) return false;  // the kernel decodes tile indices in 32 bits
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
     // one output tile and streamed weights: pairs of CTAs can share the weight stream (the launcher
     // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
