@@ -41,7 +41,9 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
 AB_STAGES = ["head_fused", "head_two_pass", "head_split"]
-TRAFFIC_DOMINANT_BYTES = 876.3e6
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel (674.8 + 200.8 MB),
+# from one ncu capture of that launch (the kernel's profile summary under profiles/)
+TRAFFIC_DOMINANT_BYTES = 875.6e6
 
 
 def flop2d(N, Ci, Co, Ho, Wo):
@@ -586,13 +588,14 @@ def main():
     ab = head_ab(wl, stream)
     peaks = load_peaks()
     # dominant kernel: the causal 128->128 tcgen05 implicit GEMM, launched twice per step by the stack
-    # stage; its per-launch time is the stage time over 2 (which also carries the two 2-frame carry copies)
+    # stage; its per-launch time is the stage time over 2 (the second layer's 2-frame carry copy ends the
+    # stage, the first one's runs on a side stream beside the second layer)
     launch_ms = stage_ms["stack"] / 2
     achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, from the ncu
-                # capture summarised in profiles/igemm_cl_causal128_4x352x624.md (algorithmic: 563.2 MB)
+                # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, from an ncu
+                # capture of that launch (algorithmic: 563.2 MB)
                 "traffic": TRAFFIC_DOMINANT_BYTES, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms}
     stages = {}
