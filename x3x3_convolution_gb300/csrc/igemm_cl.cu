@@ -54,7 +54,10 @@ constexpr int kCK = 64;         // input channels per staged chunk (one 128-byte
 constexpr int kWBlock = kBM * kCK * 2;  // bytes of one packed weight block (one tap, one chunk)
 constexpr int kWBlock64 = 64 * kCK * 2; // the same for the M = 64 form
 constexpr int kCtrW = kBNP * kCK * 2;    // centre-tap form: offset of the weight block in a stage
-constexpr int kStagePitch = 80;  // epilogue staging row: 32 channels (64 B) + pad, per warp
+// generic epilogue staging row: 32 channels (64 B), no pad: a store of one row spans 64 contiguous
+// bytes and a 16-byte load phase reads 8 whole rows (512 contiguous bytes), both free of conflicts
+constexpr int kStagePitch = 64;
+constexpr int kStageGenericBytes = 32 * kStagePitch;  // per-warp staging block of the generic epilogue
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
 constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
@@ -1045,7 +1048,11 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     g.n_tiles = g.ctr ? 1 : (d.C_out + kBM - 1) / kBM;
     g.frames = d.N * (d.dims == 3 ? d.D : 1);
     const int H_out = p->H_out, W_out = p->W_out;
-    g.stage_warp = g.stn ? kStnStageBytes : kStageWarpBytes;
+    // the generic channels-last epilogue (3D layers, C_out >= 96) stages 2 KB per warp, which leaves
+    // room for a seventh weight-ring stage in the dominant layers; the other epilogues (and NCHW
+    // output, possible for the 2D plans) stage up to 4.5 KB
+    g.stage_warp = g.stn ? kStnStageBytes
+                         : ((!small_cout && !g.kwm && !g.ctr && !g.nchw) ? kStageGenericBytes : kStageWarpBytes);
     const int fixed = 1024 + 4 * g.stage_warp + 512 + (g.nchw ? 4 * 32 * 16 : 0);
     bool found = false;
     long long best_cost = -1;
@@ -1121,11 +1128,11 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
             while (n_raw < 4 && fixed + 2 * h_bytes + (n_raw + 1) * raw_bytes + 3 * kWBlock <= kSmemLimit) ++n_raw;
         }
         int n_w = (kSmemLimit - fixed - 2 * h_bytes - n_raw * raw_bytes) / kWBlock;
-        if (n_w > 6) n_w = 6;
+        if (n_w > 7) n_w = 7;
         int n_h = 2;
         if (g.m64) {
             if (fixed + 2 * h_bytes + wres > kSmemLimit) continue;
-            n_w = 6;  // no weight ring: rank as the deepest one
+            n_w = 7;  // no weight ring: rank as the deepest one
             // at most 16 input channels: one K step per tap, so a tile's MMAs take less time than a
             // halo load's latency; stage as many halos ahead as fit
             if (light) n_h = (int)((kSmemLimit - fixed - wres) / h_bytes) < 4 ? (int)((kSmemLimit - fixed - wres) / h_bytes) : 4;
@@ -1137,7 +1144,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         const long long waves = (tiles + num_sms - 1) / num_sms;
         // every tile costs the same MMA work: rank by waves, then by weight-ring depth and halo size
         // (light M = 64 layers: by halo pipeline depth first)
-        const long long cost = (light ? (4 - n_h) * 10000000LL : 0) + waves * 100000 + (6 - n_w) * 10000 +
+        const long long cost = (light ? (4 - n_h) * 10000000LL : 0) + waves * 100000 + (7 - n_w) * 10000 +
                                (g.nchw ? (4 - n_raw) * 20000 : 0) + (long long)HR * P;
         if (!found || cost < best_cost) {
             found = true;
