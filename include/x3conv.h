@@ -31,6 +31,24 @@
  *   - Every device-side wait in the library's kernels is bounded. A wait that runs out records
  *     X3_ERR_TIMEOUT in the device status word (read with conv_device_status) and the kernel
  *     returns early, leaving the context usable.
+ *   - conv_stack_forward issues each layer's carry copy on a side stream of the library's own (one
+ *     per calling thread and device, created on first use with eight events and kept until the
+ *     process exits) and joins it back into `stream` with events before the call's work ends, so
+ *     all of a call's work is ordered as work on `stream`, including under stream capture.
+ *   - The tensor-core kernels launch as programmatic dependents of the previous kernel in `stream`:
+ *     they set up shared memory and TMEM while that kernel drains and wait for it to finish before
+ *     touching global memory.
+ *
+ * Environment switches (read when a plan is created; X3CONV_STACK_LAYOUT at each
+ * conv_stack_forward call, X3CONV_PDL once per process). The results are the same under every
+ * setting; only the kernels that compute them change:
+ *   X3CONV_FORCE_KERNEL=direct|igemm  plans made with X3_KERNEL_AUTO use that engine
+ *   X3CONV_STACK_LAYOUT=nchw          2D NCHW stacks run every layer in NCHW (no channels-last pass)
+ *   X3CONV_S2=0                       stride 2 as the stride-1 raster with even positions kept,
+ *                                     instead of the four input phases
+ *   X3CONV_W2=1                       two-window tiles for causal channels-last layers
+ *   X3CONV_CLUSTER=1                  weight blocks shared by clusters of two CTAs (multicast)
+ *   X3CONV_PDL=0                      launches fully serialised (no programmatic dependent launch)
  */
 #ifndef X3CONV_H
 #define X3CONV_H
