@@ -237,8 +237,9 @@ class Workload:
         self.head_split = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, kernel="head_split", **head_desc),
                                   HL.w.torch(dev), HL.b.torch(dev))
         self.head_split_y = torch.empty(self.head_split.out_shape(), dtype=torch.bfloat16, device=dev)
-        # kernels per step: layout conversion + 7 TAESD convs, 2 stack convs, l3, the head
-        self.kernels_per_step = 1 + len(convs) + len(sc) + 1 + 1
+        # kernels per step: layout conversion + 7 TAESD convs, 2 stack convs and their 2 carry copies,
+        # l3, the head
+        self.kernels_per_step = 1 + len(convs) + 2 * len(sc) + 1 + 1
         self.plans = {"taesd": [x3.conv_plan_describe(c.plan) for c in convs],
                       "stack": x3.conv_plan_describe(sc[0].plan),
                       "l3": x3.conv_plan_describe(self.l3.plan),

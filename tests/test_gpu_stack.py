@@ -207,3 +207,29 @@ def test_stack2d_layouts_agree_on_odd_shapes(monkeypatch):
         ref, _ = oracle.round_to(oracle.conv2d(ref, L.w.vals, L.b.vals, stride=L.stride, act=L.act), "bf16")
     assert_close(y_cl, ref)
     assert_close(y_nc, ref)
+
+
+def test_stack3d_carry_copies_finish_within_the_call():
+    """The carry copies run on the library's side stream, joined back into the caller's stream:
+    work the caller enqueues on that stream right after the call (here: overwriting the input, which
+    the first layer's copy reads) must not reach a copy still reading it. Four layers, so the second
+    layer's copy reads a workspace half that the third layer overwrites inside the call."""
+    chans, acts = [64, 32, 32, 32, 16], ["relu", "relu", "relu", "none"]
+    D, H, W = 4, 24, 200
+    layers = make_3d_layers(chans, acts, "int", 4700)
+    x = synth.activation([4700, 1], (1, D, H, W, chans[0]), "bf16", "int", None)
+    carries = [synth.activation([4700, 2, i], (1, 2, H, W, c), "bf16", "int", None)
+               for i, c in enumerate(chans[:-1])]
+    _, stack = build_stack(layers, D, H, W)
+    side = torch.cuda.Stream()
+    xd = dev(x)
+    cdev = [dev(c).contiguous() for c in carries]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        y = stack(xd, carries=cdev, carry_valid=True, stream=side)
+        xd.fill_(0)  # same stream, right after the call
+    torch.cuda.synchronize()
+    want, want_carries = oracle_rounded_chain_3d(x.vals, [c.vals for c in carries], layers)
+    assert_exact(host_values(y, "bf16"), want, "bf16")
+    for i, c in enumerate(cdev):
+        assert np.array_equal(host_values(c, "bf16"), want_carries[i]), f"carry {i}"

@@ -506,14 +506,30 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
         return X3_OK;
     }
     const size_t half = n_layers > 2 ? need / 2 : need;
-    // Layer i's carry copy reads its input and overwrites carries[i], so it follows layer i's kernel;
-    // it runs on a side stream, beside the next layers, until a kernel is about to overwrite the
-    // buffer it reads (the ping-pong buffer layer i+1 writes when i >= 1). The caller's stream waits
-    // for every copy before the call's work ends.
+    // Layer i's carry copy reads its input and overwrites carries[i], which layer i's kernel reads.
+    // On the channels-last tensor-core engine it is a kernel of its own, launched as a programmatic
+    // dependent of layer i's kernel: that kernel signals once its reads of the carry are done, the
+    // copy runs beside the rest of it and waits for it before finishing, and layer i+1 (which may
+    // overwrite the copy's source) waits for the copy in turn. Otherwise the copy is a
+    // cudaMemcpy2DAsync on a side stream, forked after layer i's kernel, that runs beside the next
+    // layers until a kernel is about to overwrite the buffer it reads (the ping-pong buffer layer i+1
+    // writes when i >= 1); the caller's stream waits for every such copy before the call's work ends.
+    auto dep_copy = [&](int i, const void* in, const void* carry) {
+        const x3_conv_desc& d = plans[i]->d;
+        return pdl_enabled() && plans[i]->kind == K_IGEMM_CL && d.layout == X3_NDHWC && aligned(in, 16) &&
+               aligned(carry, 16);
+    };
     SideStream* side = nullptr;
-    bool any_carry = false;
-    for (int i = 0; i < n_layers; ++i) any_carry |= plans[i]->d.dims == 3 && carries && carries[i];
-    if (any_carry) {
+    bool any_side = false;
+    {
+        const void* in_i = x;
+        for (int i = 0; i < n_layers; ++i) {
+            const bool c = plans[i]->d.dims == 3 && carries && carries[i];
+            any_side |= c && !dep_copy(i, in_i, carries[i]);
+            in_i = (i == n_layers - 1) ? y : (char*)workspace + (size_t)(i % 2) * half;
+        }
+    }
+    if (any_side) {
         x3_status st = side_stream(&side);
         if (st != X3_OK) return st;
     }
@@ -533,7 +549,12 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
         x3_status st = conv_forward(plans[i], in, (carry && carry_valid) ? carry : nullptr, w_packed[i],
                                     bias ? bias[i] : nullptr, out, stream);
         if (st != X3_OK) return st;
-        if (carry) {
+        if (carry && dep_copy(i, in, carry)) {
+            const x3_conv_desc& d = plans[i]->d;
+            st = launch_carry_update(in, carry, d.N, d.D, (size_t)d.H * d.W * d.C_in * 2, carry_valid,
+                                     plans[i]->num_sms, s);
+            if (st != X3_OK) return st;
+        } else if (carry) {
             const int k = i % SideStream::kEvents;
             e = cudaEventRecord(side->fork[k], s);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork[k], 0);

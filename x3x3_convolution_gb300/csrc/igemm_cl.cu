@@ -282,9 +282,11 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     // Launched as a programmatic dependent, this grid may start while the previous kernel of the
     // stream is still running: the set-up above (barriers, TMEM) overlaps its tail, and nothing of
     // global memory is read or written before the wait. The next kernel may then be scheduled; it
-    // waits in the same way before it touches this one's output.
+    // waits in the same way before it touches this one's output. With a carry, the next kernel may
+    // be the copy that overwrites it, so the MMA issuer signals only once every read of the carry
+    // by this CTA has landed in shared memory (one signal per CTA counts; the first one).
     ptx::grid_dep_wait();
-    ptx::grid_dep_launch();
+    if (!a.has_carry) ptx::grid_dep_launch();
     if (MC) ptx::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
@@ -436,6 +438,17 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             // 128-byte rows (a spatial tap) or by 32-byte K steps needs no base-offset correction;
             // the integer-exact parity tests pin this.
             const uint32_t b_hi_fixed = (1024u >> 4) | (1u << 14) | (2u << 29);
+            // with a carry: the last of this CTA's tiles that reads it (output frame 0 or 1 of the
+            // pass); the launch signal follows that tile's halo waits
+            long long last_carry_k = -1;
+            if (a.has_carry) {
+                for (long long k = 0;; ++k) {
+                    const long long tile = cl_tile_of(k, MC, rank);
+                    if (tile - (long long)rank >= a.tiles) break;
+                    if (tile < a.tiles && a.KT == 3 && cl_decode(a, tile).fr % a.dout < 2) last_carry_k = k;
+                }
+                if (last_carry_k < 0) ptx::grid_dep_launch();
+            }
             for (long long k = 0; ok; ++k) {
                 const long long tile = cl_tile_of(k, MC, rank);
                 if (tile - (long long)rank >= a.tiles) break;
@@ -553,6 +566,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     }
                 }
                 if (!ok) break;
+                if (k == last_carry_k) ptx::grid_dep_launch();  // this CTA's carry reads have landed
                 ptx::mma_commit(bar_acc_full + 8 * ab);
                 ++it;
             }
@@ -1007,6 +1021,15 @@ x3_status encode_nchw_raw(CUtensorMap* m, bool bf16, const void* ptr, uint64_t W
 
 }  // namespace
 
+// Programmatic dependent launches, unless X3CONV_PDL=0 in the environment (read once per process).
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = getenv("X3CONV_PDL");
+        return !(v && !strcmp(v, "0"));
+    }();
+    return on;
+}
+
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     const x3_conv_desc& d = p->d;
     ClGeom g;
@@ -1338,11 +1361,8 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
     // a programmatic dependent of the previous kernel in the stream (the kernel waits for it before
-    // touching global memory); X3CONV_PDL=0 in the environment launches it fully serialised
-    static const bool pdl = [] {
-        const char* v = getenv("X3CONV_PDL");
-        return !(v && !strcmp(v, "0"));
-    }();
+    // touching global memory)
+    const bool pdl = pdl_enabled();
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)g.grid);

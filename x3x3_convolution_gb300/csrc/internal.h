@@ -129,6 +129,12 @@ x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const voi
                                  void* y, int out_nchw, cudaStream_t s);
 // NCHW [N][C][H][W] -> NHWC [N][H][W][C8], channels C..C8-1 zero.
 x3_status launch_nchw_to_nhwc(const void* x, void* y, int N, int C, int C8, int H, int W, cudaStream_t s);
+// Carry update of a channels-last causal layer, launched as a programmatic dependent of the layer's
+// kernel (layout.cu); requires that kernel to signal only after its reads of the carry.
+x3_status launch_carry_update(const void* input, void* carry, int N, int D, size_t frame_bytes, int history_valid,
+                              int num_sms, cudaStream_t s);
+// Programmatic dependent launches on (X3CONV_PDL unset or not "0").
+bool pdl_enabled();
 // Two-pass head: temporal pass into the 112-channel g plane, then the spatial stencil.
 x3_status launch_head_stencil(const x3_conv_plan* p, const void* g, const void* bias, void* y, cudaStream_t s);
 x3_status read_device_status(int reset);
