@@ -589,8 +589,8 @@ def main():
     ab = head_ab(wl, stream)
     peaks = load_peaks()
     # dominant kernel: the causal 128->128 tcgen05 implicit GEMM, launched twice per step by the stack
-    # stage; its per-launch time is the stage time over 2 (the second layer's 2-frame carry copy ends the
-    # stage, the first one's runs on a side stream beside the second layer)
+    # stage; its per-launch time is the stage time over 2 (the stage also holds the two 2-frame carry
+    # copies, kernels that run beside the second half of each layer)
     launch_ms = stage_ms["stack"] / 2
     achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]

@@ -31,13 +31,17 @@
  *   - Every device-side wait in the library's kernels is bounded. A wait that runs out records
  *     X3_ERR_TIMEOUT in the device status word (read with conv_device_status) and the kernel
  *     returns early, leaving the context usable.
- *   - conv_stack_forward issues each layer's carry copy on a side stream of the library's own (one
+ *   - conv_stack_forward updates each layer's carry inside the call's work on `stream`. For layers
+ *     on the channels-last tensor-core engine it is a small kernel launched as a programmatic
+ *     dependent of the layer's kernel, which runs beside the layer once the layer has read the old
+ *     carry and finishes after it. Otherwise it is a copy on a side stream of the library's own (one
  *     per calling thread and device, created on first use with eight events and kept until the
- *     process exits) and joins it back into `stream` with events before the call's work ends, so
- *     all of a call's work is ordered as work on `stream`, including under stream capture.
+ *     process exits), joined back into `stream` with events before the call's work ends. Either
+ *     way all of a call's work is ordered as work on `stream`, including under stream capture.
  *   - The tensor-core kernels launch as programmatic dependents of the previous kernel in `stream`:
  *     they set up shared memory and TMEM while that kernel drains and wait for it to finish before
- *     touching global memory.
+ *     touching global memory. A kernel that reads a carry lets the next kernel start only after
+ *     its last read of the carry.
  *
  * Environment switches (read when a plan is created; X3CONV_STACK_LAYOUT at each
  * conv_stack_forward call, X3CONV_PDL once per process). The results are the same under every
