@@ -490,6 +490,19 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         CTR ? hbase
                             : (S2 ? hbase + (uint32_t)(pos_off + (kh ? a.P : 0) + (kw ? 1 : 0)) * 128u
                                   : hbase + (uint32_t)(pos_off + kh * a.P + kw) * 128u);
+                    if (!W2 && !M64 && a.C_in - cc * kCK >= kCK) {
+                        // a full 64-channel block: its four K steps as one issue group (the M = 64
+                        // form measured slower this way: 0.151 -> 0.160 ms for the TAESD chain)
+                        uint64_t ad[4], bd[4];
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            ad[ks] = ((uint64_t)a_hi << 32) | (uint64_t)(a_lo + (uint32_t)ks * (uint32_t)((2 * kRows * 16) >> 4));
+                            bd[ks] = ((uint64_t)b_hi_fixed << 32) |
+                                     (uint64_t)((((row_addr + (uint32_t)ks * 32u) >> 4) & 0x3FFFu) | (1u << 16));
+                        }
+                        ptx::mma4_f16(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3], a.idesc, acc);
+                        acc = 1;
+                    } else
 #pragma unroll
                     for (int ks = 0; ks < kCK / 16; ++ks) {
                         if (ks * 16 >= a.C_in - cc * kCK) break;  // channels past C_in: nothing to add
@@ -656,7 +669,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         const int oh = m / a.P, c = m % a.P;
                         const int ow = ow0 + c;
                         if (jw < a.win_adv && c < a.Wt && ow < a.W_out && oh < a.H_out) {
-                            const size_t W2 = 2 * (size_t)a.W_out;
+                            const size_t W2o = 2 * (size_t)a.W_out;
                             const size_t row0 = (((size_t)n * a.dout + t) * 2 * (size_t)a.H_out + 2 * (size_t)oh);
 #pragma unroll
                             for (int r = 0; r < 10; ++r) {
@@ -666,7 +679,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                                       S[(20 + r) * kSPitch + lane + 2] + bias_g[r];
                                     // unpatchify: channel co = rgb*4 + dy*2 + dx -> pixel (2oh+dy, 2ow+dx)
                                     const int rgb = co >> 2, dy = (co >> 1) & 1, dx = co & 1;
-                                    y[((row0 + dy) * W2 + 2 * (size_t)ow + dx) * 3 + rgb] =
+                                    y[((row0 + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
                                         cl_round<BF16>(cl_act(acc, a.act));
                                 }
                             }

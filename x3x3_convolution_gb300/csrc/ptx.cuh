@@ -140,6 +140,25 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The four 16-channel K steps of one 64-channel block, descriptors a[k], b[k], as one issue group
+// (measured on one GB300 against four separately issued MMAs: two causal 128->128 layers 1.054 ->
+// 1.003 ms, the 256->128 layer 0.258 -> 0.245 ms, the stencil head 0.204 -> 0.195 ms). The first
+// MMA accumulates when `accumulate` is non-zero, the other three always.
+__device__ __forceinline__ void mma4_f16(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                         uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 t, %10, %10;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, t;\n\t}"
+        ::"r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+          "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
