@@ -13,14 +13,14 @@ namespace {
 
 // One thread per position: the position's C values (one per channel plane; consecutive threads
 // read consecutive positions, so each channel's reads are coalesced) are written as C8 contiguous
-// channels in 16-byte pieces, zero past C.
+// channels in 16-byte pieces, zero past C. Position indices fit in 32 bits (checked by the
+// launcher), so the image/pixel split is a 32-bit division.
 __global__ void __launch_bounds__(256) nchw_to_nhwc_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
-                                                           int C, int C8, size_t plane, size_t positions) {
-    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < positions;
-         idx += (size_t)gridDim.x * blockDim.x) {
-        const size_t n = idx / plane, pix = idx % plane;
-        const uint16_t* xs = x + n * C * plane + pix;
-        uint4* yd = reinterpret_cast<uint4*>(y + idx * C8);
+                                                           int C, int C8, uint32_t plane, uint32_t positions) {
+    for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < positions; idx += gridDim.x * blockDim.x) {
+        const uint32_t n = idx / plane, pix = idx - n * plane;
+        const uint16_t* xs = x + (size_t)n * C * plane + pix;
+        uint4* yd = reinterpret_cast<uint4*>(y + (size_t)idx * C8);
         for (int c0 = 0; c0 < C8; c0 += 8) {
             uint32_t w[4];
 #pragma unroll
@@ -107,9 +107,12 @@ x3_status launch_nchw_to_nhwc(const void* x, void* y, int N, int C, int C8, int 
     if (N < 1 || C < 1 || C8 < C || C8 % 8 != 0 || H < 1 || W < 1)
         return fail(X3_ERR_UNSUPPORTED, "layout conversion: shape out of range");
     const size_t plane = (size_t)H * W, positions = (size_t)N * plane;
+    if (positions + 8192ull * 256ull >= (1ull << 32))
+        return fail(X3_ERR_UNSUPPORTED, "layout conversion: more than 2^32 - 2^21 positions");
     size_t blocks = (positions + 255) / 256;
     if (blocks > 8192) blocks = 8192;
-    nchw_to_nhwc_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)x, (uint16_t*)y, C, C8, plane, positions);
+    nchw_to_nhwc_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)x, (uint16_t*)y, C, C8, (uint32_t)plane,
+                                                          (uint32_t)positions);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "layout conversion launch: %s", cudaGetErrorString(e));
     return X3_OK;
