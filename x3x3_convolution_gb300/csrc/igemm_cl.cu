@@ -122,6 +122,18 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
 // Tile of this CTA at iteration k. With weight multicast (MC) the two CTAs of a cluster take the two
 // tiles of a pair, so both walk the same number of iterations and stream the same weight blocks; the
 // second tile of the last pair can lie past the end (a phantom iteration: weight blocks only).
+// Position in a ring of n stages: the stage index and the parity of its current phase, advanced
+// without a division (the MMA issuer takes one per weight block).
+struct RingPos {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ long long cl_tile_of(long long k, bool mc, uint32_t rank) {
     if (!mc) return (long long)blockIdx.x + k * gridDim.x;
     return 2 * ((long long)(blockIdx.x >> 1) + k * (gridDim.x >> 1)) + rank;
@@ -305,6 +317,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t h_cnt = 0, w_cnt = 0, r_cnt = 0;
+            RingPos hr, wr;  // halo and weight ring positions of h_cnt and w_cnt
             bool ok = true;
             if (M64) {  // every weight block of the layer, once, on the first weight barrier
                 const int nblk = a.KT * a.n_chunks * 9;
@@ -312,6 +325,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 for (int b = 0; b < nblk; ++b)
                     ptx::bulk_load(sW + (uint32_t)(b * kWBlock64), a.w + (size_t)b * kWBlock64, (uint32_t)kWBlock64, bar_w_full);
                 w_cnt = 1;
+                wr.next(a.n_w);
             }
             for (long long k = 0; ok; ++k) {
                 const long long tile = cl_tile_of(k, MC, rank);
@@ -355,8 +369,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             }
                             if (!ok) break;
                         } else if (real) {
-                            const uint32_t sh = h_cnt % a.n_h;
-                            if (!cl_wait(bar_h_empty + 8 * sh, ((h_cnt / a.n_h) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                            const uint32_t sh = hr.slot;
+                            if (!cl_wait(bar_h_empty + 8 * sh, hr.phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
                             if (CTR) {
                                 // 256 consecutive positions of the frame's flattened plane (STN: the
@@ -376,6 +390,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             else
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
                             ++h_cnt;
+                            hr.next(a.n_h);
                         }
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + (S2 ? 0 : kt)) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
@@ -386,8 +401,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 s2_tap(kt, ti, kh, kw);
                                 tap = kh * 3 + kw;
                             }
-                            const uint32_t sw = w_cnt % a.n_w;
-                            if (!cl_wait(bar_w_empty + 8 * sw, ((w_cnt / a.n_w) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                            const uint32_t sw = wr.slot;
+                            if (!cl_wait(bar_w_empty + 8 * sw, wr.phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
                             if (!MC)
                                 ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
@@ -396,6 +411,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 ptx::bulk_load_multicast(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock,
                                                          (uint32_t)kWBlock, bar_w_full + 8 * sw, (uint16_t)3);
                             ++w_cnt;
+                            wr.next(a.n_w);
                         }
                     }
                 }
@@ -421,6 +437,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         // ------------------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
             uint32_t h_cnt = 0, w_cnt = 0, it = 0;
+            RingPos hr, wr;  // halo and weight ring positions of h_cnt and w_cnt
             bool ok = true;
             // A (weights), no swizzle: SBO = 128 B between 8-row groups, LBO = 2 KB between the two
             // 8-channel halves of a 16-channel K step; version 1 in bits 46-47.
@@ -456,11 +473,12 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // phantom iteration: take the pair's weight blocks through the ring (the peer's
                     // producer waits for this CTA's arrivals on every stage it refills)
                     for (int b = 0; b < n_groups * kTapsK && ok; ++b) {
-                        const uint32_t sw = w_cnt % a.n_w;
-                        if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) { ok = false; break; }
+                        const uint32_t sw = wr.slot;
+                        if (!cl_wait(bar_w_full + 8 * sw, wr.phase, abort_flag, a.status)) { ok = false; break; }
                         ptx::tc_fence_after();
                         ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
                         ++w_cnt;
+                        wr.next(a.n_w);
                     }
                     continue;
                 }
@@ -475,14 +493,14 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 uint32_t acc = 0;
                 // the MMAs of one tap: four K steps of 16 channels into the tile's accumulator
                 auto tap_mmas = [&](int cc, int kt, int kh, int kw, uint32_t hbase) -> bool {
-                    const uint32_t sw = w_cnt % a.n_w;
+                    const uint32_t sw = wr.slot;
                     uint32_t a_lo;
                     if (M64) {
                         a_lo = a_lo0 + (uint32_t)(((kt * a.n_chunks + cc) * 9 + kh * 3 + kw) * (kWBlock64 >> 4));
                     } else if (CTR) {  // the weight block shares the stage (and its barrier) with the window
                         a_lo = (((hbase + (uint32_t)kCtrW) >> 4) & 0x3FFFu) | ((uint32_t)((kBM * 16) >> 4) << 16);
                     } else {
-                        if (!cl_wait(bar_w_full + 8 * sw, (w_cnt / a.n_w) & 1u, abort_flag, a.status)) return false;
+                        if (!cl_wait(bar_w_full + 8 * sw, wr.phase, abort_flag, a.status)) return false;
                         ptx::tc_fence_after();
                         a_lo = a_lo0 + sw * (uint32_t)(kWBlock >> 4);
                     }
@@ -520,12 +538,13 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         if (MC) ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
                         else ptx::mma_commit(bar_w_empty + 8 * sw);
                         ++w_cnt;
+                        wr.next(a.n_w);
                     }
                     return true;
                 };
                 auto group_begin = [&](uint32_t& sh, uint32_t& hbase) -> bool {
-                    sh = h_cnt % a.n_h;
-                    if (!cl_wait(bar_h_full + 8 * sh, (h_cnt / a.n_h) & 1u, abort_flag, a.status)) return false;
+                    sh = hr.slot;
+                    if (!cl_wait(bar_h_full + 8 * sh, hr.phase, abort_flag, a.status)) return false;
                     ptx::tc_fence_after();
                     hbase = sH + sh * (uint32_t)a.h_bytes;
                     return true;
@@ -545,6 +564,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         if (!ok) break;
                         ptx::mma_commit(bar_h_empty + 8 * sh);
                         ++h_cnt;
+                        hr.next(a.n_h);
                     }
                 } else if constexpr (S2) {
                     // stride 2: (phase, chunk) groups, each with the taps that read the phase
@@ -560,6 +580,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             if (!ok) break;
                             ptx::mma_commit(bar_h_empty + 8 * sh);
                             ++h_cnt;
+                            hr.next(a.n_h);
                         }
                     }
                 } else {
@@ -575,6 +596,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             if (!ok) break;
                             ptx::mma_commit(bar_h_empty + 8 * sh);
                             ++h_cnt;
+                            hr.next(a.n_h);
                         }
                     }
                 }
