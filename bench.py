@@ -598,7 +598,10 @@ def main():
                 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, from an ncu
                 # capture of that launch (algorithmic: 563.2 MB)
                 "traffic": TRAFFIC_DOMINANT_BYTES, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
-                "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms}
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms,
+                # the sustained figure was taken under the power cap (its SM clock median is recorded
+                # beside it); the same kernel against the burst figure, for a run whose clocks stayed high
+                "frac_of_burst": achieved / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None}
     stages = {}
     for k in STAGES:
         t = stage_ms[k] * 1e-3

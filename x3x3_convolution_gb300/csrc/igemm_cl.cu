@@ -162,8 +162,7 @@ __device__ __forceinline__ bool cl_wait(uint32_t bar, uint32_t parity, volatile 
 // one column before the output window, so the shift is 0 for kh = 0 and 1 otherwise (same for kw).
 __device__ __forceinline__ int s2_ntaps(int ph) { return ((ph >> 1) ? 2 : 1) * ((ph & 1) ? 2 : 1); }
 __device__ __forceinline__ void s2_tap(int ph, int i, int& kh, int& kw) {
-    const int nw = (ph & 1) ? 2 : 1;
-    const int ih = i / nw, iw = i - ih * nw;
+    const int ih = (ph & 1) ? i >> 1 : i, iw = (ph & 1) ? i & 1 : 0;  // two column taps when b = 1
     kh = (ph >> 1) ? 2 * ih : 1;
     kw = (ph & 1) ? 2 * iw : 1;
 }
