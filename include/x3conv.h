@@ -69,7 +69,7 @@ typedef struct CUstream_st* x3_stream_t; /* identical to cudaStream_t */
 typedef enum {
     X3_OK = 0,
     X3_ERR_INVALID = 1,     /* bad argument: shape, pointer, alignment or combination */
-    X3_ERR_UNSUPPORTED = 2, /* valid, but no kernel in this build handles it (caller falls back) */
+    X3_ERR_UNSUPPORTED = 2, /* valid, but no kernel of the library handles it (caller falls back) */
     X3_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
     X3_ERR_OOM = 4,         /* a caller-provided buffer is too small */
     X3_ERR_TIMEOUT = 5      /* a bounded device wait ran out (see conv_device_status) */
