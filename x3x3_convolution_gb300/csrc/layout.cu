@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_kernel(const uint16_t* __res
 // a programmatic dependent of the layer's kernel, which signals once all of its reads of the old
 // history are done, so the copy runs beside the rest of that kernel; every thread then waits for
 // that kernel to complete before it exits, which keeps the stream's order for whatever follows.
+// Its loads go to L2 only (ld.global.cg): the kernel overlaps others, so no L1 line of an earlier
+// pass may serve them.
 __global__ void __launch_bounds__(256) carry_update_kernel(const uint4* __restrict__ in, uint4* __restrict__ carry,
                                                            int rows, uint32_t unit, int D, int history_valid) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -53,17 +55,18 @@ __global__ void __launch_bounds__(256) carry_update_kernel(const uint4* __restri
             uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
             // four independent 16-byte copies in flight per thread
             for (; e + 3 * stride < per_row; e += 4 * stride) {
-                const uint4 v0 = src[e], v1 = src[e + stride], v2 = src[e + 2 * stride], v3 = src[e + 3 * stride];
+                const uint4 v0 = __ldcg(src + e), v1 = __ldcg(src + e + stride), v2 = __ldcg(src + e + 2 * stride),
+                            v3 = __ldcg(src + e + 3 * stride);
                 c[e] = v0; c[e + stride] = v1; c[e + 2 * stride] = v2; c[e + 3 * stride] = v3;
             }
-            for (; e < per_row; e += stride) c[e] = src[e];
+            for (; e < per_row; e += stride) c[e] = __ldcg(src + e);
         } else {
             // one frame: the older history frame is the previous newer one (or zero), the newer one
             // the input; each thread moves both frames of its own pieces
             for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < per_row; e += stride) {
-                const uint4 h = history_valid ? c[unit + e] : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 h = history_valid ? __ldcg(c + unit + e) : make_uint4(0u, 0u, 0u, 0u);
                 c[e] = h;
-                c[unit + e] = x[e];
+                c[unit + e] = __ldcg(x + e);
             }
         }
     }
