@@ -28,8 +28,11 @@
 // so the epilogue of one tile overlaps the MMAs of the next), add the bias, apply the activation,
 // round once and write channels-last rows through a shared-memory transpose (the NCHW form adds
 // four transposer warps). Every wait is bounded (1 s); a wait that runs out sets the device status
-// word and every role gives up cleanly. The forms (head, NCHW, centre tap, M = 64, cluster, two
-// windows) are described at the kernel template below.
+// word and every role gives up cleanly. The MMA issuer is a single thread whose own instruction
+// stream measurably gates the tensor pipe, so its loop keeps ring positions as wrapping counters
+// (no division per weight block) and issues a full block's four K steps as one group. The forms
+// (head, NCHW, centre tap, stencil head, M = 64, stride-2 phases, cluster, two windows) are
+// described at the kernel template below.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
