@@ -897,11 +897,6 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     // Each warp transposes its own 32 channels x 32 positions through a private staging
                     // block (no barrier across warps), then writes 64 contiguous bytes per position row.
                     uint8_t* wst = stage_ptr + ew * a.stage_warp;
-                    // the window's first raster row and column; a position's row and column follow from
-                    // its offset by a float reciprocal (exact: offsets < 1024, pitch <= 256), which
-                    // keeps integer divisions off the SM sub-partition this warp shares with the MMA
-                    // issuer or the producer
-                    const int oh0 = m0 / a.P, c00 = m0 - oh0 * a.P;
                     // W2: the two windows of the tile, accumulators in TMEM columns 0-255 and 256-511
                     for (int chunk = 0; chunk < (W2 ? 2 : 1) * (kBNP / 32); ++chunk) {
                         uint32_t v[32];
@@ -911,16 +906,15 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
-                                cl_round<BF16>(fminf(fmaxf(__uint_as_float(v[j]) + bias_r, act_lo), act_hi));
+                                cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
                         __syncwarp();
 #pragma unroll
                         for (int k = 0; k < (M64 ? 2 : 4); ++k) {
                             // 32 positions x (kCpw / 8) 16-byte channel segments per chunk
                             const int row = M64 ? k * 16 + (lane >> 1) : k * 8 + (lane >> 2);
                             const int seg = M64 ? (lane & 1) : (lane & 3);
-                            const int cc = c00 + chunk * 32 + row;
-                            const int dr = __float2int_rz(((float)cc + 0.5f) * inv_p);
-                            const int oh = oh0 + dr, c = cc - dr * a.P;
+                            const int m = m0 + chunk * 32 + row;
+                            const int oh = m / a.P, c = m % a.P;
                             const int ow = ow0 + c;
                             const int co = tc.nt * (M64 ? 64 : kBM) + q * kCpw + seg * 8;
                             if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
