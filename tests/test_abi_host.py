@@ -304,3 +304,35 @@ def test_stack_workspace_covers_the_channels_last_input(lib):
     finally:
         x3.conv_plan_destroy(a)
         x3.conv_plan_destroy(b)
+
+
+@pytest.mark.parametrize("shape", [(4, 64, 64, 256, 256), (1, 64, 64, 33, 97), (2, 8, 32, 17, 255),
+                                   (1, 64, 128, 20, 66), (1, 96, 64, 15, 40)], ids=str)
+@pytest.mark.parametrize("form", ["phases", "raster"])
+def test_stride2_channels_last_forms_planned(lib, shape, form, monkeypatch):
+    """Stride-2 NHWC layers plan the four-input-phase form by default (output raster of pitch
+    Wt + 1, each phase box spanning 2P x 2HR input positions, at most 256 a side) and, with
+    X3CONV_S2=0, the stride-1 raster over the input plane with even positions kept. Plan geometry
+    only: no GPU needed."""
+    monkeypatch.setenv("X3CONV_S2", "1" if form == "phases" else "0")
+    N, Ci, Co, H, W = shape
+    p = x3.conv_plan_create(x3.make_desc(2, N, Ci, Co, H, W, stride=2, layout="NHWC", dtype="bf16"))
+    try:
+        g = x3.conv_plan_describe(p)
+        Ho, Wo = (H + 1) // 2, (W + 1) // 2
+        assert (g["H_out"], g["W_out"]) == (Ho, Wo)
+        if form == "phases":
+            assert (g["s2"], g["sub2"]) == (1, 0)
+            P, HR, Wt = g["P"], g["HR"], g["Wt"]
+            assert P == Wt + 1 and 2 * P <= 256 and 2 * HR <= 256
+            assert g["strips"] * Wt >= Wo and g["windows"] * 256 >= Ho * P
+            # every window's rows, shifted by one row and one column, stay inside its phase box
+            for win in range(min(g["windows"], 4 * P)):
+                assert (256 * win) % P + 255 + P + 1 + 1 <= HR * P
+            assert g["h_bytes"] >= HR * P * 128 and g["h_bytes"] % 1024 == 0
+        else:
+            assert (g["s2"], g["sub2"]) == (0, 1)
+            assert g["P"] == g["Wt"] + 2 and g["strips"] * g["Wt"] >= W and g["windows"] * 256 >= H * g["P"]
+        assert g["m64"] == (Co <= 64 and Ci <= 64) and g["smem_bytes"] <= 232448
+    finally:
+        x3.conv_plan_destroy(p)
