@@ -51,7 +51,6 @@
  *   X3CONV_S2=0                       stride 2 as the stride-1 raster with even positions kept,
  *                                     instead of the four input phases
  *   X3CONV_W2=1                       two-window tiles for causal channels-last layers
- *   X3CONV_CLUSTER=1                  weight blocks shared by clusters of two CTAs (multicast)
  *   X3CONV_PDL=0                      launches fully serialised (no programmatic dependent launch)
  */
 #ifndef X3CONV_H

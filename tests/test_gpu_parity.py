@@ -267,30 +267,3 @@ def test_full_size_head_sampled():
     g = np.stack([[got[0, t, 2 * h + (c // 2) % 2, 2 * w + c % 2, c // 4] for c in range(12)] for (t, h, w) in pos])
     assert_close(g, ref)
     assert psnr(g, ref) >= PSNR_MIN
-
-
-# ------------------------------------------------------------------ clusters of two CTAs
-
-@pytest.mark.parametrize("form", ["cl_128", "head_single_pass"])
-def test_cluster_weight_multicast(form, monkeypatch):
-    """The cluster form of the swapped engine (X3CONV_CLUSTER=1: pairs of CTAs share each weight
-    block by multicast, phantom iterations when a pair has one tile left) gives the same values as
-    the oracle, exactly on integer data (the channels-last case has an odd number of tiles)."""
-    monkeypatch.setenv("X3CONV_CLUSTER", "1")
-    if form == "cl_128":
-        x, carry, L = synth.conv3d_single(C_in=128, C_out=128, D=3, H=9, W=301, variant="int", act="relu", seed=3801)
-        got, conv = run3d(x, carry, L)
-        ref = oracle3d(x, carry, L)
-    else:
-        x, carry, L = synth.head(D=3, H=7, W=150, variant="sparse1", seed=3802)
-        N, D, H, W, C = x.shape
-        d = x3.make_desc(3, N, C, 12, H, W, D=D, act="clamp", unpatchify2x2=True, kernel="igemm")
-        conv = x3.Conv(d, dev(L.w), dev(L.b))
-        got = host_values(conv(dev(x), dev(carry)), "bf16")
-        torch.cuda.synchronize()
-        ref = oracle.unpatchify2x2(oracle3d(x, carry, L).transpose(0, 4, 1, 2, 3)).transpose(0, 2, 3, 4, 1)
-    g = x3.conv_plan_describe(conv.plan)
-    assert g["mc"] == 1
-    if form == "cl_128":
-        assert g["tiles"] % 2 == 1
-    assert_exact(got, ref, "bf16")

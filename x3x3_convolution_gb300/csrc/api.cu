@@ -238,11 +238,11 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"BM\": 128, \"BN\": 256, \"CK\": 64, \"n_tiles\": %d, \"n_chunks\": %d, \"KT\": %d, "
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
-                        "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, \"mc\": %d, "
+                        "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, "
                         "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.mc, c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn);
+                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",

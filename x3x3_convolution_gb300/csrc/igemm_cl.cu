@@ -31,7 +31,7 @@
 // word and every role gives up cleanly. The MMA issuer is a single thread whose own instruction
 // stream measurably gates the tensor pipe, so its loop keeps ring positions as wrapping counters
 // (no division per weight block) and issues a full block's four K steps as one group. The forms
-// (head, NCHW, centre tap, stencil head, M = 64, stride-2 phases, cluster, two windows) are
+// (head, NCHW, centre tap, stencil head, M = 64, stride-2 phases, two windows) are
 // described at the kernel template below.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -39,8 +39,6 @@
 #include <cuda_runtime.h>
 #include <stdlib.h>
 #include <string.h>
-
-#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -122,9 +120,6 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
     return c;
 }
 
-// Tile of this CTA at iteration k. With weight multicast (MC) the two CTAs of a cluster take the two
-// tiles of a pair, so both walk the same number of iterations and stream the same weight blocks; the
-// second tile of the last pair can lie past the end (a phantom iteration: weight blocks only).
 // Position in a ring of n stages: the stage index and the parity of its current phase, advanced
 // without a division (the MMA issuer takes one per weight block).
 struct RingPos {
@@ -137,10 +132,8 @@ struct RingPos {
     }
 };
 
-__device__ __forceinline__ long long cl_tile_of(long long k, bool mc, uint32_t rank) {
-    if (!mc) return (long long)blockIdx.x + k * gridDim.x;
-    return 2 * ((long long)(blockIdx.x >> 1) + k * (gridDim.x >> 1)) + rank;
-}
+// Tile of this (persistent) CTA at iteration k.
+__device__ __forceinline__ long long cl_tile_of(long long k) { return (long long)blockIdx.x + k * gridDim.x; }
 
 __device__ __forceinline__ bool cl_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -211,10 +204,6 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // M64 (layers with at most 64 output channels): MMAs of M = 64, whose accumulator rows 16q..16q+15
 // sit in TMEM lanes 32q..32q+15; every weight block of the layer stays resident in shared memory
 // (loaded once per CTA), so a tile only streams its halo.
-// MC (one 128-channel output tile): the kernel runs as clusters of two CTAs that stream the same
-// weight blocks; each block is fetched once from L2 by one of the two (alternating) and multicast into
-// both CTAs' ring stage, and a stage is refilled only after the MMAs of both CTAs have read it (each
-// MMA issuer's commit arrives on the stage's empty barrier in both CTAs).
 // W2 (channels-last, one output tile; opt-in): a tile is two consecutive 256-position windows whose
 // halo is staged by one box; each weight K slice feeds an MMA for the first window and then one for
 // the second, which re-uses the A operand it just fetched, the two accumulators filling all 512 TMEM
@@ -228,7 +217,7 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // staged as its four phases, even or odd rows by even or odd columns, each box loaded by the TMA
 // unit with element strides of 2. A phase is one pipeline group that feeds only the taps reading it
 // (one, two, two and four of the nine), each at a shift of 0 or 1 row and column (s2_tap).
-template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool MC = false, bool W2 = false,
+template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool W2 = false,
           bool STN = false, bool S2 = false>
 __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
@@ -272,7 +261,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         }
         for (int i = 0; i < a.n_w; ++i) {
             ptx::mbar_init(bar_w_full + 8 * i, 1);
-            ptx::mbar_init(bar_w_empty + 8 * i, MC ? 2 : 1);  // MC: the MMAs of both CTAs
+            ptx::mbar_init(bar_w_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_acc_full + 8 * i, 1);
@@ -301,18 +290,16 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     // by this CTA has landed in shared memory (one signal per CTA counts; the first one).
     ptx::grid_dep_wait();
     if (!a.has_carry) ptx::grid_dep_launch();
-    if (MC) ptx::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
     // K order of this CTA. In the head form (kw folded into M: few, small weight blocks per tile) each
     // CTA walks its (kt, chunk) groups and the kh taps inside a group from a CTA-dependent starting
     // point, so the CTAs, which run in near lockstep, fetch different weight blocks at any moment
     // instead of all asking L2 for the same one (measured: 15 % faster there; the other forms run
-    // slower with it, so they keep the natural order). Both CTAs of a cluster share one order. Only
+    // slower with it, so they keep the natural order). Only
     // the fp32 summation order depends on it.
     constexpr int kTapsK = KWM ? 3 : (CTR ? 1 : 9);
     const int n_groups = (S2 ? 4 : a.KT) * a.n_chunks;  // S2: (phase, chunk) groups
-    const int k_id = KWM ? (int)(MC ? blockIdx.x >> 1 : blockIdx.x) : 0;
+    const int k_id = KWM ? (int)blockIdx.x : 0;
     const int rot_g = k_id % n_groups, rot_t = (k_id / n_groups) % kTapsK;
 
     if (warp == 0) {
@@ -330,10 +317,9 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 wr.next(a.n_w);
             }
             for (long long k = 0; ok; ++k) {
-                const long long tile = cl_tile_of(k, MC, rank);
-                if (tile - (long long)rank >= a.tiles) break;
-                const bool real = tile < a.tiles;
-                const ClTile tc = cl_decode(a, real ? tile : 0);
+                const long long tile = cl_tile_of(k);
+                if (tile >= a.tiles) break;
+                const ClTile tc = cl_decode(a, tile);
                 const int n = tc.fr / a.dout, t = tc.fr % a.dout;
                 const int r0 = (tc.win * a.win_adv) / a.P;
                 const int ow0 = tc.strip * a.Wt;
@@ -370,7 +356,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 ++r_cnt;
                             }
                             if (!ok) break;
-                        } else if (real) {
+                        } else {
                             const uint32_t sh = hr.slot;
                             if (!cl_wait(bar_h_empty + 8 * sh, hr.phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
@@ -406,12 +392,8 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             const uint32_t sw = wr.slot;
                             if (!cl_wait(bar_w_empty + 8 * sw, wr.phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_w_full + 8 * sw, (uint32_t)kWBlock);
-                            if (!MC)
-                                ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
-                                               bar_w_full + 8 * sw);
-                            else if ((w_cnt & 1u) == rank)  // alternate blocks, into both CTAs
-                                ptx::bulk_load_multicast(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock,
-                                                         (uint32_t)kWBlock, bar_w_full + 8 * sw, (uint16_t)3);
+                            ptx::bulk_load(sW + sw * kWBlock, wblk + (size_t)tap * kWBlock, (uint32_t)kWBlock,
+                                           bar_w_full + 8 * sw);
                             ++w_cnt;
                             wr.next(a.n_w);
                         }
@@ -462,28 +444,15 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             long long last_carry_k = -1;
             if (a.has_carry) {
                 for (long long k = 0;; ++k) {
-                    const long long tile = cl_tile_of(k, MC, rank);
-                    if (tile - (long long)rank >= a.tiles) break;
-                    if (tile < a.tiles && a.KT == 3 && cl_decode(a, tile).fr % a.dout < 2) last_carry_k = k;
+                    const long long tile = cl_tile_of(k);
+                    if (tile >= a.tiles) break;
+                    if (a.KT == 3 && cl_decode(a, tile).fr % a.dout < 2) last_carry_k = k;
                 }
                 if (last_carry_k < 0) ptx::grid_dep_launch();
             }
             for (long long k = 0; ok; ++k) {
-                const long long tile = cl_tile_of(k, MC, rank);
-                if (tile - (long long)rank >= a.tiles) break;
-                if (MC && tile >= a.tiles) {
-                    // phantom iteration: take the pair's weight blocks through the ring (the peer's
-                    // producer waits for this CTA's arrivals on every stage it refills)
-                    for (int b = 0; b < n_groups * kTapsK && ok; ++b) {
-                        const uint32_t sw = wr.slot;
-                        if (!cl_wait(bar_w_full + 8 * sw, wr.phase, abort_flag, a.status)) { ok = false; break; }
-                        ptx::tc_fence_after();
-                        ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
-                        ++w_cnt;
-                        wr.next(a.n_w);
-                    }
-                    continue;
-                }
+                const long long tile = cl_tile_of(k);
+                if (tile >= a.tiles) break;
                 const ClTile tc = cl_decode(a, tile);
                 const int pos_off = (tc.win * a.win_adv) % a.P;
                 // two accumulator buffers used alternately, or (W2) one pair of them per tile
@@ -537,8 +506,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         acc = 1;
                     }
                     if (!M64 && !CTR) {
-                        if (MC) ptx::mma_commit_multicast(bar_w_empty + 8 * sw, (uint16_t)3);
-                        else ptx::mma_commit(bar_w_empty + 8 * sw);
+                        ptx::mma_commit(bar_w_empty + 8 * sw);
                         ++w_cnt;
                         wr.next(a.n_w);
                     }
@@ -650,7 +618,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
         const float inv_p = 1.0f / (float)a.P;
         for (long long k = 0;; ++k, ++it) {
-            const long long tile = cl_tile_of(k, MC, rank);
+            const long long tile = cl_tile_of(k);
             if (tile >= a.tiles) break;
             const uint32_t ab = W2 ? 0u : (it & 1u);
             if (!cl_wait(bar_acc_full + 8 * ab, (W2 ? it : (it >> 1)) & 1u, abort_flag, a.status)) break;
@@ -996,7 +964,6 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem_base, 512u);
-    if (MC) ptx::cluster_sync();  // no multicast copy or commit still targets this CTA's shared memory
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1257,11 +1224,6 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     }
     if (g.tiles >= (1LL << 31)) return false;  // the kernel decodes tile indices in 32 bits
     g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
-    // one output tile and streamed weights: pairs of CTAs can share the weight stream (the launcher
-    // sizes the grid to the clusters that fit). Off unless X3CONV_CLUSTER=1: halving the L2 reads of
-    // the weights measured no faster on any layer of the decoder (each SM still receives every block).
-    const char* cl_env = getenv("X3CONV_CLUSTER");
-    g.mc = (g.n_tiles == 1 && !g.nchw && !g.m64 && !g.ctr && !g.w2 && !g.s2 && cl_env && !strcmp(cl_env, "1")) ? 1 : 0;
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
@@ -1271,44 +1233,6 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
 }
 
 namespace {
-
-// Clusters of two CTAs of kernel `func` (with `smem` bytes of dynamic shared memory each) that can be
-// resident at once on the current device; cached per kernel, size and device.
-x3_status active_pairs(const void* func, int smem, int* out) {
-    struct Entry { const void* f; int smem, dev, n; };
-    static std::mutex mu;
-    static Entry cache[32];
-    static int n_cache = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return fail(X3_ERR_CUDA, "cudaGetDevice failed"); }
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n_cache; ++i)
-            if (cache[i].f == func && cache[i].smem == smem && cache[i].dev == dev) { *out = cache[i].n; return X3_OK; }
-    }
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
-    if (e != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        return fail(X3_ERR_CUDA, "no cluster of two CTAs fits (%s)", cudaGetErrorString(e));
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (n_cache < 32) cache[n_cache++] = Entry{func, smem, dev, n};
-    *out = n;
-    return X3_OK;
-}
 
 // One launch of the engine for descriptor d (its layout, C_in and stride as the kernel sees them)
 // with tiling g over an H_out x W_out raster; the stored plane is yH x yW.
@@ -1355,42 +1279,14 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         }
     }
     void (*k)(CUtensorMap, CUtensorMap, ClArgs);
-    if (g.mc) {
-        if (g.ctr) k = igemm_cl_kernel<true, false, false, true, false, true>;
-        else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false, false, false, true> : igemm_cl_kernel<false, true, false, false, false, true>;
-        else k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true> : igemm_cl_kernel<false, false, false, false, false, true>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
-        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl smem attribute: %s", cudaGetErrorString(e));
-        int clusters = 0;
-        x3_status st2 = active_pairs((const void*)k, g.smem_bytes, &clusters);
-        if (st2 != X3_OK) return st2;
-        const long long pairs = (g.tiles + 1) / 2;
-        if (clusters > pairs) clusters = (int)pairs;
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3((unsigned)(2 * clusters));
-        cfg.blockDim = dim3(192);
-        cfg.dynamicSmemBytes = (size_t)g.smem_bytes;
-        cfg.stream = s;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, k, mx, mc, a);
-        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl cluster launch: %s", cudaGetErrorString(e));
-        return X3_OK;
-    }
-    if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, true>
-                       : igemm_cl_kernel<false, false, false, false, false, false, true>;
-    else if (g.stn) k = igemm_cl_kernel<true, false, false, true, false, false, false, true>;
+    if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true>
+                       : igemm_cl_kernel<false, false, false, false, false, true>;
+    else if (g.stn) k = igemm_cl_kernel<true, false, false, true, false, false, true>;
     else if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
-    else if (g.s2 && g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true, false, false, false, true>
-                                     : igemm_cl_kernel<false, false, false, false, true, false, false, false, true>;
-    else if (g.s2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
-                            : igemm_cl_kernel<false, false, false, false, false, false, false, false, true>;
+    else if (g.s2 && g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true, false, false, true>
+                                     : igemm_cl_kernel<false, false, false, false, true, false, false, true>;
+    else if (g.s2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, true>
+                            : igemm_cl_kernel<false, false, false, false, false, false, false, true>;
     else if (g.m64) k = bf16 ? igemm_cl_kernel<true, false, false, false, true> : igemm_cl_kernel<false, false, false, false, true>;
     else if (g.nchw) k = bf16 ? igemm_cl_kernel<true, false, true> : igemm_cl_kernel<false, false, true>;
     else if (g.kwm) k = bf16 ? igemm_cl_kernel<true, true, false> : igemm_cl_kernel<false, true, false>;

@@ -73,7 +73,6 @@ struct ClGeom {
     int s2;                      // 1: stride 2 from the four input phases (element-strided TMA boxes)
     int m64;                     // 1: M = 64 MMAs (at most 64 output channels), weights resident
     int w_smem;                  // shared-memory bytes for weights (the ring, or all blocks when m64)
-    int mc;                      // 1: clusters of two CTAs sharing each weight block by multicast
     int w2;                      // 1: a tile is two consecutive windows sharing every weight K slice
     int stn;                     // 1: head with the spatial stencil in the epilogue (centre-tap MMAs)
     int stage_warp;              // epilogue staging bytes per warp
