@@ -46,6 +46,25 @@ AB_STAGES = ["head_fused", "head_two_pass", "head_split"]
 TRAFFIC_DOMINANT_BYTES = 875.7e6
 
 
+def layer_descs():
+    """The descriptors (keyword arguments of x3x3_convolution_gb300.make_desc) of every layer this
+    benchmark runs, by stage: the step's four stages and the two single-layer configurations timed
+    beside it (the 16->16 64x64 NCHW f16 conv and the causal 256->256 4+2x88x156 layer). The full-size
+    parity tests build their plans from these, so they cover the launch configurations timed here."""
+    from x3x3_convolution_gb300.synth import TAESD_CHAIN
+    taesd, H, W = [], 256, 256
+    for ci, co, s in TAESD_CHAIN:
+        taesd.append(dict(dims=2, N=4, C_in=ci, C_out=co, H=H, W=W, stride=s, layout="NCHW", dtype="f16",
+                          act="relu"))
+        H, W = (H - 1) // s + 1, (W - 1) // s + 1
+    stack = [dict(dims=3, N=1, C_in=128, C_out=128, H=352, W=624, D=FRAMES, act="relu") for _ in range(2)]
+    return {"taesd": taesd, "stack": stack,
+            "l3": dict(dims=3, N=1, C_in=256, C_out=128, H=176, W=312, D=FRAMES, act="none"),
+            "head": dict(dims=3, N=1, C_in=256, C_out=12, H=352, W=624, D=FRAMES, act="clamp", unpatchify2x2=True),
+            "conv16": dict(dims=2, N=1, C_in=16, C_out=16, H=64, W=64, layout="NCHW", dtype="f16", act="relu"),
+            "conv256": dict(dims=3, N=1, C_in=256, C_out=256, H=88, W=156, D=FRAMES, act="none")}
+
+
 def flop2d(N, Ci, Co, Ho, Wo):
     return 2.0 * N * Ci * Co * 9 * Ho * Wo
 
@@ -195,34 +214,29 @@ class Workload:
         import x3x3_convolution_gb300 as x3
         from x3x3_convolution_gb300 import synth
         dev = device
+        descs = layer_descs()
         xt, layers = synth.taesd_chain(seed=1002 + seed_base)
-        convs, H, W = [], 256, 256
-        for L in layers:
-            d = x3.make_desc(2, 4, L.C_in, L.C_out, H, W, stride=L.stride, layout="NCHW", dtype="f16", act="relu")
-            convs.append(x3.Conv(d, L.w.torch(dev), L.b.torch(dev)))
-            H, W = convs[-1].H_out, convs[-1].W_out
+        convs = [x3.Conv(x3.make_desc(**dd), L.w.torch(dev), L.b.torch(dev)) for dd, L in zip(descs["taesd"], layers)]
         self.taesd = x3.ConvStack(convs)
         self.taesd_x = xt.torch(dev)
         self.taesd_y = torch.empty(convs[-1].out_shape(), dtype=torch.float16, device=dev)
         st = synth.conv3d_stack(seed=1004 + seed_base)
         sc = []
-        for L in st["layers"]:
-            d = x3.make_desc(3, 1, L.C_in, L.C_out, 352, 624, D=FRAMES, act=L.act)
-            sc.append(x3.Conv(d, L.w.torch(dev), L.b.torch(dev)))
+        for dd, L in zip(descs["stack"], st["layers"]):
+            sc.append(x3.Conv(x3.make_desc(**dd), L.w.torch(dev), L.b.torch(dev)))
         self.stack = x3.ConvStack(sc)
         self.stack_x = st["x"].torch(dev)
         self.stack_carries = [c.torch(dev).contiguous() for c in st["carries"]]
         self.stack_y = torch.empty(sc[-1].out_shape(), dtype=torch.bfloat16, device=dev)
         L3 = st["L3"]
-        self.l3 = x3.Conv(x3.make_desc(3, 1, 256, 128, 176, 312, D=FRAMES, act="none"), L3.w.torch(dev),
-                          L3.b.torch(dev))
+        self.l3 = x3.Conv(x3.make_desc(**descs["l3"]), L3.w.torch(dev), L3.b.torch(dev))
         self.l3_x = st["x3"].torch(dev)
         self.l3_c = st["carry3"].torch(dev)
         self.l3_y = torch.empty(self.l3.out_shape(), dtype=torch.bfloat16, device=dev)
         hx, hc, HL = synth.head(seed=1005 + seed_base)
         head_desc = dict(D=FRAMES, act="clamp", unpatchify2x2=True)
         # the step's head: the library's default (the stencil head: one kernel, G kept in fp32 on chip)
-        self.head = x3.Conv(x3.make_desc(3, 1, 256, 12, 352, 624, **head_desc), HL.w.torch(dev), HL.b.torch(dev))
+        self.head = x3.Conv(x3.make_desc(**descs["head"]), HL.w.torch(dev), HL.b.torch(dev))
         self.head_x = hx.torch(dev)
         self.head_c = hc.torch(dev)
         self.head_y = torch.empty(self.head.out_shape(), dtype=torch.bfloat16, device=dev)

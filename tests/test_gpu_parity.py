@@ -219,8 +219,8 @@ W2_CASES = [
 @pytest.mark.parametrize("variant", ["int", "random"])
 @pytest.mark.parametrize("case", W2_CASES, ids=lambda c: "x".join(map(str, c[:6])) + ("c" if c[7] else "z"))
 def test_conv3d_two_window_form(case, variant, monkeypatch):
-    """The two-window form (X3CONV_W2=1 takes it on these small shapes; the planner picks it for the
-    352x624 128->128 layers): a tile is two consecutive windows sharing each weight K slice."""
+    """The two-window form (opt-in: X3CONV_W2=1; no plan takes it by default): a tile is two consecutive
+    windows sharing each weight K slice."""
     monkeypatch.setenv("X3CONV_W2", "1")
     N, Ci, Co, D, H, W, act, with_carry = case
     x, carry, L = synth.conv3d_single(C_in=Ci, C_out=Co, D=D, H=H, W=W, N=N, variant=variant, act=act,
@@ -234,27 +234,7 @@ def test_conv3d_two_window_form(case, variant, monkeypatch):
         assert_close(got, ref)
 
 
-# ------------------------------------------------------------------ full sizes, sampled
-
-FULL_3D = {
-    "causal_256_4x88x156": dict(C_in=256, C_out=256, D=4, H=88, W=156, act="none"),
-    "causal_128_4x352x624": dict(C_in=128, C_out=128, D=4, H=352, W=624, act="relu"),
-    "causal_256to128_4x176x312": dict(C_in=256, C_out=128, D=4, H=176, W=312, act="none"),
-}
-
-
-@pytest.mark.parametrize("name", sorted(FULL_3D))
-def test_full_size_sampled(name):
-    cfg = FULL_3D[name]
-    x, carry, L = synth.conv3d_single(N=1, seed=3900 + len(name), **cfg)
-    got, conv = run3d(x, carry, L)
-    assert conv.kernel_name.startswith("igemm_tcgen05")
-    seq = np.concatenate([carry.vals, x.vals], axis=1)
-    pos = sample_positions(cfg["D"], cfg["H"], cfg["W"], 400, seed=len(name))
-    ref = oracle_sampled_3d(seq, L.w.vals, L.b.vals, cfg["act"], pos)
-    g = np.stack([got[0, t, h, w] for (t, h, w) in pos])
-    assert_close(g, ref)
-
+# ------------------------------------------------------------------ full size, sampled (the single-pass head)
 
 def test_full_size_head_sampled():
     x, carry, L = synth.head(seed=3950)

@@ -1,9 +1,11 @@
-"""Pass-by-pass decoding of a long sequence (carries between passes) equals one long pass, and the
-device memory it needs does not grow with the sequence length."""
+"""Pass-by-pass decoding of a long sequence (carries between passes) equals the oracle over the whole
+sequence and one long pass on the GPU, and the device memory it needs does not grow with the sequence
+length."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import x3x3_convolution_gb300 as x3
 from x3x3_convolution_gb300 import synth
 from x3x3_convolution_gb300.video import PassDecoder
@@ -34,6 +36,12 @@ def test_passes_equal_one_long_pass():
     _, convsT = _layers(T, H, W, 7100)
     x = synth.activation([7100, 0], (1, T, H, W, 16), "bf16", "int")
     want = host_values(x3.ConvStack(convsT)(dev(x)), "bf16")
+    # the one long pass against the oracle run layer by layer over the whole sequence (zero history,
+    # each intermediate rounded to bf16 as the library stores it; integer data: exact)
+    ref = x.vals
+    for L in Ls:
+        ref = oracle.round_to(oracle.conv3d_causal(ref, L.w.vals, L.b.vals, act=L.act, layout="NDHWC"), "bf16")[0]
+    assert np.array_equal(want, ref)
     dec = PassDecoder(convs4, D)
     got = dec.decode(x.torch("cpu").pin_memory())                  # passes of 4, 4 and 2 frames
     assert got.device.type == "cpu"

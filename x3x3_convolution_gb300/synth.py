@@ -8,7 +8,8 @@ and returns the raw 16-bit patterns (fed to the GPU) together with their exact f
 
 Distributions follow the decoder workloads: activations U[-1,1] (2D) or N(0,1) (3D), weights
 N(0, 1/sqrt(taps*C_in)) (the second parameter read as the standard deviation), biases
-U[-0.1,0.1] (U[-0.05,0.05] for the head), and an integer variant with every value in {-2..2}.
+U[-0.1,0.1] (U[-0.05,0.05] for the head), and an integer variant with every value in {-2..2}
+("fewtaps": integer inputs and three +-1 weights per output channel, for exact long chains).
 Keys are numpy SeedSequence([1000 + workload id, tensor id]).
 """
 from __future__ import annotations
@@ -95,6 +96,17 @@ def make_layer(key, dims, C_in, C_out, dtype, stride=1, act="none", variant="ran
         v = g.choice([-1.0, 0.0, 1.0], size=wshape, p=[0.02, 0.96, 0.02])
         w = Tensor(*to_storage(v, dtype), dtype)
         b = tensor(list(key) + [2], (C_out,), ("int", 0, 0), dtype)
+    elif variant == "fewtaps":
+        # three non-zero weights (+1 or -1) per output channel at random (input channel, tap) places
+        # and a bias in {-1, 0, 1}: every output is an integer sum of at most three inputs and the
+        # bias, so a chain of many layers stays exact in fp32 and inside f16's range
+        g = _rng(list(key) + [1])
+        v = np.zeros(wshape)
+        flat = v.reshape(C_out, -1)
+        for co in range(C_out):
+            flat[co, g.choice(flat.shape[1], size=min(3, flat.shape[1]), replace=False)] = g.choice([-1.0, 1.0], size=3)
+        w = Tensor(*to_storage(v, dtype), dtype)
+        b = tensor(list(key) + [2], (C_out,), ("int", -1, 1), dtype)
     else:
         std = 1.0 / np.sqrt(taps * C_in)
         w = tensor(list(key) + [1], wshape, ("normal", std), dtype)
@@ -103,7 +115,7 @@ def make_layer(key, dims, C_in, C_out, dtype, stride=1, act="none", variant="ran
 
 
 def activation(key, shape, dtype, variant="random", dist=None) -> Tensor:
-    if variant == "int":
+    if variant in ("int", "fewtaps"):
         return tensor(key, shape, ("int", -2, 2), dtype)
     if variant == "sparse1":
         return tensor(key, shape, ("int", -1, 1), dtype)
