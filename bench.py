@@ -13,8 +13,11 @@ The step runs every stage of the path through the library's C ABI:
              the single-pass form and the two-pass forms are timed beside it).
 value = total convolution FLOP of the step / step time (TFLOP/s, whole job over all ranks).
 Also reported: decoder-stack ms per frame (stack + l3 + head over the 4 frames), per-stage times,
-the roofline fraction of the dominant kernel, an end-to-end number with host buffers, the SM
-clocks seen during the timed region, and the CPU oracle timed on a bounded sample.
+every configuration's time-based roofline (``configs``: the step's stages and layers, plus the
+16->16 64x64 conv and the causal 256->256 layer timed alone with L2 flushed between launches), the
+roofline fraction of the dominant kernel, peak device memory (the step, and a pass-by-pass decoder
+against one long pass for 16 to 64 frames), an end-to-end number with host buffers, the SM clocks
+seen during the timed region, and the CPU oracle timed on a bounded sample.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica of the step (weak scaling, no collective on the
@@ -41,9 +44,10 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
 AB_STAGES = ["head_fused", "head_two_pass", "head_split"]
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel (675.1 + 200.6 MB),
-# from one ncu capture of that launch (the kernel's profile summary under profiles/)
-TRAFFIC_DOMINANT_BYTES = 875.7e6
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of each kernel at the benchmark's size,
+# from one ncu capture of that launch of the current code (each kernel's summary under profiles/);
+# None where there is no such capture
+DRAM_BYTES = {"conv16": None, "taesd": None, "conv256": None, "stack_128": None, "l3": None, "head": None}
 
 
 def layer_descs():
@@ -299,6 +303,106 @@ class Workload:
             ev[4].record(stream)
 
 
+def time_alone(fn, stream, reps, flush):
+    """Mean device time (ms) of fn() over `reps` launches, each bracketed by its own CUDA events on
+    `stream`, with a write of `flush` (larger than L2) between launches, outside the events."""
+    import torch
+    for _ in range(3):
+        fn()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for e0, e1 in pairs:
+        flush.add_(1)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in pairs)
+
+
+def roof_entry(ms, flop, nbytes, peaks, timing, dram=None, frames=None):
+    """Time-based roofline of one kernel or stage: t_roof = max(bytes / HBM peak, FLOP / bf16 peak),
+    frac = t_roof / t_measured; the bound is the larger of the two terms."""
+    t = ms * 1e-3
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flop / (peaks["bf16_tflops"] * 1e12)
+    e = {"ms": ms, "tflops": flop / t / 1e12, "gbs": nbytes / t / 1e9, "gflop": flop / 1e9, "alg_mb": nbytes / 1e6,
+         "bound": "hbm" if t_hbm >= t_tc else "tensor", "t_roof_ms": max(t_hbm, t_tc) * 1e3,
+         "frac": max(t_hbm, t_tc) / t, "frac_tensor": flop / t / 1e12 / peaks["bf16_tflops"],
+         "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"], "timing": timing,
+         "dram_bytes_ncu": dram}
+    if frames:
+        e["ms_per_frame"] = ms / frames
+    return e
+
+
+def single_layer_configs(dev, stream, peaks, reps=20):
+    """The two single-layer configurations, each timed alone with L2 flushed between launches: the
+    16->16 64x64 NCHW f16 conv (bias, ReLU) and the causal 256->256 layer over 4+2 x 88x156."""
+    import torch
+    import x3x3_convolution_gb300 as x3
+    from x3x3_convolution_gb300 import synth
+    descs = layer_descs()
+    x1, L1 = synth.conv2d_single(seed=1001)
+    c1 = x3.Conv(x3.make_desc(**descs["conv16"]), L1.w.torch(dev), L1.b.torch(dev))
+    x1d = x1.torch(dev)
+    y1 = torch.empty(c1.out_shape(), dtype=torch.float16, device=dev)
+    x3_, cr3, L3 = synth.conv3d_single(seed=1003)
+    c3 = x3.Conv(x3.make_desc(**descs["conv256"]), L3.w.torch(dev), L3.b.torch(dev))
+    x3d, cr3d = x3_.torch(dev), cr3.torch(dev)
+    y3 = torch.empty(c3.out_shape(), dtype=torch.bfloat16, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB, twice the L2
+    ms1 = time_alone(lambda: c1(x1d, out=y1, stream=stream), stream, reps, flush)
+    ms3 = time_alone(lambda: c3(x3d, cr3d, out=y3, stream=stream), stream, reps, flush)
+    f1, b1 = flop2d(1, 16, 16, 64, 64), 2.0 * (16 * 64 * 64 * 2 + 16 * 16 * 9 + 16)
+    f3 = flop3d(256, 256, 4, 88, 156)
+    b3 = 2.0 * (6 * 88 * 156 * 256 + 4 * 88 * 156 * 256 + 256 * 256 * 27 + 256)
+    timing = f"alone, {reps} launches, L2 flushed between launches (256 MB write)"
+    return {"conv16_64x64": dict(roof_entry(ms1, f1, b1, peaks, timing, DRAM_BYTES["conv16"]),
+                                 note="launch-latency bound: 0.27 MB, far below a launch's fixed cost"),
+            "causal256_4x88x156": dict(roof_entry(ms3, f3, b3, peaks, timing, DRAM_BYTES["conv256"], frames=FRAMES),
+                                       plan=x3.conv_plan_describe(c3.plan))}
+
+
+def pass_memory_curve(wl, dev):
+    """Peak device memory of the causal 128->128 stack (the step's two layers, 352x624, 4 frames per
+    pass) decoding T = 16, 32 and 64 frames pass by pass from pinned host memory (PassDecoder: one pass
+    of frames, the histories and the two workspace buffers on the device), against one pass over all T
+    frames with the whole sequence, its intermediates and its output on the device at once."""
+    import torch
+    import x3x3_convolution_gb300 as x3
+    from x3x3_convolution_gb300.video import PassDecoder
+    convs = wl.stack.layers
+    out = []
+    for passes in (4, 8, 16):
+        T = FRAMES * passes
+        x = torch.zeros((1, T, 352, 624, 128), dtype=torch.bfloat16).pin_memory()
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        dec = PassDecoder(convs, FRAMES)
+        y = dec.decode(x)
+        torch.cuda.synchronize()
+        peak_pass = torch.cuda.max_memory_allocated() - base
+        del dec, y
+        longc = [x3.Conv(x3.make_desc(3, 1, 128, 128, 352, 624, D=T, act={0: "none", 1: "relu", 2: "clamp"}[c.desc.act]),
+                         torch.zeros((128, 128, 3, 3, 3), dtype=torch.bfloat16, device=dev),
+                         torch.zeros(128, dtype=torch.bfloat16, device=dev)) for c in convs]
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        st = x3.ConvStack(longc)
+        xd = x.to(dev)
+        yd = st(xd)
+        torch.cuda.synchronize()
+        peak_long = torch.cuda.max_memory_allocated() - base
+        del st, xd, yd, longc, x
+        torch.cuda.empty_cache()
+        out.append({"frames": T, "passes": passes, "pass_decoder_gib": peak_pass / 2 ** 30,
+                    "one_pass_gib": peak_long / 2 ** 30})
+    return out
+
+
 def cpu_baseline(target_s=12.0):
     """The oracle, as it stands, on the host cores, on a bounded sample of the dominant stage: the
     causal 128->128 layer at 352x624 restricted to a band of output rows of one frame."""
@@ -479,6 +583,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-memory", action="store_true", help="skip the pass-decoder peak-memory curve")
     ap.add_argument("--stage", choices=STAGES + AB_STAGES, default=None,
                     help="run only this stage per step (for profiler captures); prints its per-launch time")
     args = ap.parse_args()
@@ -524,6 +629,7 @@ def main():
         raise RuntimeError(f"device status after warm-up: {st} {x3.conv_last_error()}")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    torch.cuda.reset_peak_memory_stats()
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -538,6 +644,7 @@ def main():
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    step_peak = torch.cuda.max_memory_allocated()
     barrier(world)
     ms_per_step = reduce_max(world, t0.elapsed_time(t1)) / args.steps
     stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, name in enumerate(STAGES)}
@@ -607,21 +714,32 @@ def main():
     # copies, kernels that run beside the second half of each layer)
     launch_ms = stage_ms["stack"] / 2
     achieved = fl["stack"] / 2 / (launch_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # the timed region lasts milliseconds (ms_per_step x steps), not the seconds under the power cap of
+    # the sustained figure: the burst figure is the peak; the SM clock seen meanwhile is in `clocks`
+    peak = peaks["bf16_tflops"]
+    timed_ms = ms_per_step * args.steps
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, from an ncu
                 # capture of that launch (algorithmic: 563.2 MB)
-                "traffic": TRAFFIC_DOMINANT_BYTES, "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
-                "peak_source": f"{peaks['source']} bf16_tflops_sustained", "launch_ms": launch_ms,
-                # the sustained figure was taken under the power cap (its SM clock median is recorded
-                # beside it); the same kernel against the burst figure, for a run whose clocks stayed high
-                "frac_of_burst": achieved / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None}
+                "traffic": DRAM_BYTES["stack_128"],
+                "kernel": "igemm_cl_kernel (channels-last, swapped operands, 128-byte swizzle) causal 128->128 @4+2x352x624",
+                "peak_source": f"{peaks['source']} bf16_tflops (burst; the timed region lasts {timed_ms:.0f} ms)",
+                "launch_ms": launch_ms, "sm_mhz_during": clk.get("sm_mhz"),
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     stages = {}
     for k in STAGES:
-        t = stage_ms[k] * 1e-3
-        stages[k] = {"ms": stage_ms[k], "tflops": fl[k] / t / 1e12, "gbs": nb[k] / t / 1e9,
-                     "frac_tensor": fl[k] / t / 1e12 / peaks["bf16_tflops"],
-                     "frac_hbm": nb[k] / t / 1e9 / peaks["hbm_gbs"]}
+        stages[k] = roof_entry(stage_ms[k], fl[k], nb[k], peaks, "inside the step")
+    configs = {"taesd_chain_n4_256": dict(stages["taesd"], ms_per_image=stage_ms["taesd"] / 4,
+                                          dram_bytes_ncu=DRAM_BYTES["taesd"]),
+               "causal128_stack_4x352x624": dict(roof_entry(stage_ms["stack"] / 2, fl["stack"] / 2, nb["stack"] / 2,
+                                                            peaks, "inside the step: stack stage / 2",
+                                                            DRAM_BYTES["stack_128"], frames=FRAMES),
+                                                 stack_ms_per_frame=stage_ms["stack"] / FRAMES),
+               "causal256to128_4x176x312": roof_entry(stage_ms["l3"], fl["l3"], nb["l3"], peaks, "inside the step",
+                                                      DRAM_BYTES["l3"], frames=FRAMES),
+               "head_256to12_4x352x624": roof_entry(stage_ms["head"], fl["head"], nb["head"], peaks, "inside the step",
+                                                    DRAM_BYTES["head"], frames=FRAMES)}
+    configs.update(single_layer_configs(dev, stream, peaks))
     line = {
         "metric": METRIC, "value": world * total_flop / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -631,10 +749,15 @@ def main():
                    "l2": "inputs larger than L2 (each step streams ~3 GB; no explicit flush)",
                    "frames_per_pass": FRAMES},
         "decoder_ms_per_frame": (stage_ms["stack"] + stage_ms["l3"] + stage_ms["head"]) / FRAMES,
-        "stages": stages, "roofline": roofline, "gpu_launches": wl.kernels_per_step * args.steps,
+        "stages": stages, "configs": configs, "roofline": roofline, "gpu_launches": wl.kernels_per_step * args.steps,
         "clocks": clk, "e2e": e2e, "head_variants": ab,
         "plans": {k: (v if k != "taesd" else [p.get("kernel") for p in v]) for k, v in wl.plans.items()},
     }
+    line["peak_memory"] = {"step_gib": step_peak / 2 ** 30,
+                           "note": "torch.cuda.max_memory_allocated over the timed steps: every input, output, "
+                                   "weight and workspace of the step's workload (plus the A/B head forms' weights)"}
+    if not args.no_memory:
+        line["peak_memory"]["pass_decoder"] = pass_memory_curve(wl, dev)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline()
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
