@@ -138,14 +138,41 @@ WORKLOADS = {
     "ragged_3d": dict(dims=3, N=2, C_in=40, C_out=72, D=3, H=7, W=301),
     "ragged_3d_wide": dict(dims=3, N=2, C_in=40, C_out=136, D=3, H=7, W=301),
     "nhwc_2d_256": dict(dims=2, N=3, C_in=64, C_out=256, H=33, W=97, layout="NHWC"),
+    "nhwc_2d_64_tn": dict(dims=2, N=4, C_in=64, C_out=64, H=256, W=256, layout="NHWC", dtype="f16"),
+    "nhwc_2d_80_tn": dict(dims=2, N=1, C_in=136, C_out=80, H=19, W=301, layout="NHWC"),
+    "nhwc_2d_16_tn": dict(dims=2, N=2, C_in=8, C_out=16, H=7, W=9, layout="NHWC"),
     "head_two_pass_256to12": dict(dims=3, N=1, C_in=256, C_out=12, D=4, H=352, W=624, unpatchify2x2=True,
                                   kernel="head_two_pass"),
 }
 
 
+def _check_tn_plan(g, C_in, C_out):
+    """Positions-as-M form with the horizontal taps in N: a tile is four whole raster rows of pitch 32
+    (30 outputs and two junk columns each, one row per epilogue warp, so the kw shifts stay inside a
+    warp); A = 128 staged positions from kh P (kh <= 2); N = 3 x C_out padded to 16 rows of resident
+    weights; two TMEM buffers of N columns at a 256-column stride."""
+    P, HR, Wt = g["P"], g["HR"], g["Wt"]
+    assert g["tn"] == 1 and g["m64"] == 0 and g["win_adv"] == 128
+    assert (P, Wt, HR) == (32, 30, 6)
+    for win in range(min(g["windows"], 4 * P)):
+        pos_off = (128 * win) % P
+        assert pos_off == 0
+        need = pos_off + 127 + 2 * P + 1
+        assert need <= HR * P and need * 128 <= g["h_bytes"]
+    cp = (C_out + 15) // 16 * 16
+    assert 3 * cp <= 256 and g["h_bytes"] % 1024 == 0 and g["smem_bytes"] <= 232448
+    assert 2 <= g["n_h"] <= 4
+    assert g["strips"] * Wt >= g["W_out"] or g.get("sub2")
+    return cp
+
+
 def _check_sw128_plan(g):
     """Channels-last swapped engine: 256-position windows of strip rasters of pitch P."""
     P, HR, Wt = g["P"], g["HR"], g["Wt"]
+    if g.get("tn"):
+        assert g["windows"] * 128 >= g["H_out"] * P
+        assert g["tiles"] == g["strips"] * g["windows"] * g["frames"]
+        return
     assert P == Wt + 2 and P <= 256 and HR <= 256
     # the furthest halo row read: a window starting at offset P-1 of a row (or 0 when P divides
     # 256), its last position, tap (kh=2, kw=2)
@@ -185,6 +212,8 @@ def test_igemm_plans_cover_their_reads(lib, name):
             assert g["tiles"] == g["windows"] * g["frames"] and g["smem_bytes"] <= 232448
             return
         if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head"):
+            if g.get("tn"):
+                _check_tn_plan(g, WORKLOADS[name]["C_in"], WORKLOADS[name]["C_out"])
             _check_sw128_plan(g)
             return
         assert g["kernel"] == "igemm_tcgen05"
@@ -277,17 +306,26 @@ def test_nchw_layers_have_channels_last_forms(lib, name):
             assert P == Wt + 1 and 2 * P <= 256 and 2 * HR <= 256
             for win in range(min(s["windows"], 4 * P)):
                 assert (256 * win) % P + 255 + P + 1 + 1 <= HR * P  # shifts of one row and one column
+        elif cfg["C_out"] <= 80:
+            # stride 1 with at most 80 output channels: positions as M, horizontal taps in N
+            Ho, Wo = cfg["H"], cfg["W"]
+            assert s["tn"] == 1 and s["m64"] == 0 and (P, Wt, HR) == (32, 30, 6)
+            for win in range(min(s["windows"], 4 * P)):
+                assert (128 * win) % P + 127 + 2 * P + 1 <= HR * P
         else:
             Ho, Wo = cfg["H"], cfg["W"]
             assert P == Wt + 2 and P <= 256 and HR <= 256
             for win in range(min(s["windows"], 4 * P)):
                 assert (256 * win) % P + 255 + 2 * P + 2 + 1 <= HR * P
-        assert s["strips"] * Wt >= Wo and s["windows"] * 256 >= Ho * P
+        adv = 128 if s["tn"] else 256
+        assert s["strips"] * Wt >= Wo and s["windows"] * adv >= Ho * P
         assert s["n_chunks"] == (cfg["C_in"] + 63) // 64
-        assert s["n_tiles"] == (cfg["C_out"] + (63 if s["m64"] else 127)) // (64 if s["m64"] else 128)
+        assert s["n_tiles"] == (1 if s["tn"] else (cfg["C_out"] + (63 if s["m64"] else 127)) // (64 if s["m64"] else 128))
         assert s["smem_bytes"] <= 232448 and s["w_off"] % 256 == 0
-        assert s["m64"] == (cfg["C_out"] <= 64)
-        shadow_bytes = s["n_tiles"] * s["n_chunks"] * 9 * (64 if s["m64"] else 128) * 64 * 2
+        assert s["m64"] == (cfg["C_out"] <= 64 and not s["tn"])
+        cp = (cfg["C_out"] + 15) // 16 * 16
+        shadow_bytes = (s["n_chunks"] * 3 * 3 * cp * 128 if s["tn"] else
+                        s["n_tiles"] * s["n_chunks"] * 9 * (64 if s["m64"] else 128) * 64 * 2)
         assert x3.conv_packed_weight_bytes(p) == s["w_off"] + shadow_bytes or \
             (s["w_off"] == 0 and x3.conv_packed_weight_bytes(p) == shadow_bytes)
     finally:
@@ -330,9 +368,12 @@ def test_stride2_channels_last_forms_planned(lib, shape, form, monkeypatch):
             for win in range(min(g["windows"], 4 * P)):
                 assert (256 * win) % P + 255 + P + 1 + 1 <= HR * P
             assert g["h_bytes"] >= HR * P * 128 and g["h_bytes"] % 1024 == 0
+            assert g["m64"] == (Co <= 64 and Ci <= 64)
         else:
             assert (g["s2"], g["sub2"]) == (0, 1)
-            assert g["P"] == g["Wt"] + 2 and g["strips"] * g["Wt"] >= W and g["windows"] * 256 >= H * g["P"]
-        assert g["m64"] == (Co <= 64 and Ci <= 64) and g["smem_bytes"] <= 232448
+            adv = 128 if g["tn"] else 256
+            assert g["tn"] == (Co <= 80)
+            assert g["P"] == g["Wt"] + 2 and g["strips"] * g["Wt"] >= W and g["windows"] * adv >= H * g["P"]
+        assert g["smem_bytes"] <= 232448
     finally:
         x3.conv_plan_destroy(p)

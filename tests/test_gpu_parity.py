@@ -79,22 +79,37 @@ def test_conv2d_nchw(case, variant, kernel):
         assert_close(got, ref)
 
 
+NHWC_CASES = [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"), (1, 8, 16, 3, 5, 1, "none"),
+              (2, 64, 64, 34, 72, 2, "relu"), (1, 40, 24, 17, 33, 2, "none"), (2, 64, 128, 33, 97, 1, "relu"),
+              (1, 128, 64, 12, 130, 1, "relu"),
+              # positions-as-M form (horizontal taps in N): 80 channels (N = 240), 24 (padded to 32),
+              # 8 (padded to 16), a partial last input chunk (136 = 2 x 64 + 8), one-column images
+              (1, 64, 80, 19, 301, 1, "relu"), (2, 24, 24, 11, 40, 1, "none"), (1, 64, 8, 5, 260, 1, "relu"),
+              (1, 136, 32, 7, 45, 1, "none"), (3, 16, 16, 6, 1, 1, "relu")]
+
+
 @pytest.mark.parametrize("variant", ["int", "random"])
-@pytest.mark.parametrize("case", [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"),
-                                  (1, 8, 16, 3, 5, 1, "none"), (2, 64, 64, 34, 72, 2, "relu"),
-                                  (1, 40, 24, 17, 33, 2, "none"), (2, 64, 128, 33, 97, 1, "relu"),
-                                  (1, 128, 64, 12, 130, 1, "relu")], ids=str)
+@pytest.mark.parametrize("case", NHWC_CASES, ids=str)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_conv2d_nhwc(case, variant, dtype):
-    """Channels-last 2D layers on the swapped engine: the M = 64 form (C_out <= 64, weights resident
-    when they fit), the 128-row form, and stride 2 as the stride-1 raster with even positions kept."""
+@pytest.mark.parametrize("form", ["auto", "m64"])
+def test_conv2d_nhwc(case, variant, dtype, form, monkeypatch):
+    """Channels-last 2D layers on the swapped engine: stride 1 with at most 80 output channels in the
+    positions-as-M form with the horizontal taps in N (or, with X3CONV_TN=0, the M = 64 form for at
+    most 64 output channels, weights resident when they fit), the 128-row form, and stride 2 from the
+    four input phases."""
+    if form == "m64":
+        monkeypatch.setenv("X3CONV_TN", "0")
     N, Ci, Co, H, W, s, act = case
     key = 2100 + sum(case[:6])
     x = synth.activation([key, 0], (N, H, W, Ci), dtype, variant, ("uniform", -1.0, 1.0))
     L = synth.make_layer([key], 2, Ci, Co, dtype, stride=s, act=act, variant=variant)
     got, conv = run2d(x, L, layout="NHWC")
     g = x3.conv_plan_describe(conv.plan)
-    assert g["kernel"] == "igemm_tcgen05_sw128" and g["s2"] == (s == 2) and g["m64"] == (Co <= 64 and Ci <= 64)
+    assert g["kernel"] == "igemm_tcgen05_sw128" and g["s2"] == (s == 2)
+    if form == "auto" and s == 1 and Co <= 80 and not (Ci > 128 and Co > 32):
+        assert g["tn"] == 1
+    elif form == "m64":
+        assert g["tn"] == 0 and g["m64"] == (Co <= 64 and Ci <= 64)
     ref = oracle2d(x, L, layout="NHWC")
     if variant == "int":
         assert_exact(got, ref, dtype)

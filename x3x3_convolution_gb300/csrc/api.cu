@@ -170,8 +170,7 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
     }
     if (cl_ok) {
         p->kind = K_IGEMM_CL;
-        p->packed_bytes = (size_t)p->cl.n_tiles * p->cl.KT * p->cl.n_chunks * (p->cl.kwm ? 3 : 9) *
-                          ((p->cl.m64 ? 64 : 128) * 64 * 2);
+        p->packed_bytes = cl_packed_bytes(p->cl);
     } else if (igemm_ok) {
         p->kind = K_IGEMM;
         const IgemmGeom& g = p->g;
@@ -201,13 +200,12 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
             p->cl_shadow = q.cl;
             // the channels-last engine's weight blocks; the NCHW form of the same engine uses the
             // same blocks (n_chunks agree: C_in and its round-up to 8 need the same 64-channel chunks)
-            if (p->kind == K_IGEMM_CL && !p->cl.kwm && !p->cl.ctr && !q.cl.m64 && p->cl.n_chunks == q.cl.n_chunks &&
-                p->cl.n_tiles == q.cl.n_tiles) {
+            if (p->kind == K_IGEMM_CL && !p->cl.kwm && !p->cl.ctr && !q.cl.m64 && !q.cl.tn && !p->cl.m64 && !p->cl.tn &&
+                p->cl.n_chunks == q.cl.n_chunks && p->cl.n_tiles == q.cl.n_tiles) {
                 p->shadow_w_off = 0;
             } else {
                 p->shadow_w_off = (p->packed_bytes + 255) & ~(size_t)255;
-                p->packed_bytes = p->shadow_w_off +
-                                  (size_t)q.cl.n_tiles * q.cl.n_chunks * 9 * ((q.cl.m64 ? 64 : 128) * 64 * 2);
+                p->packed_bytes = p->shadow_w_off + cl_packed_bytes(q.cl);
             }
         }
     }
@@ -239,10 +237,10 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, "
-                        "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d}",
+                        "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d, \"tn\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn);
+                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn, c.tn);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
@@ -269,9 +267,9 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
         const int m = snprintf(tmp + n - 1, sizeof tmp - (size_t)(n - 1),
                                ", \"shadow\": {\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, "
                                "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"n_h\": %d, \"sub2\": %d, \"s2\": %d, \"tiles\": %lld, "
-                               "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d}}",
+                               "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d, \"tn\": %d}}",
                                c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.n_h, c.sub2, c.s2, c.tiles,
-                               c.smem_bytes, c.grid, plan->shadow_w_off, c.m64);
+                               c.smem_bytes, c.grid, plan->shadow_w_off, c.m64, c.tn);
         n = n - 1 + m;
     }
     return snprintf(buf, len, "%s", tmp);

@@ -157,6 +157,40 @@ __global__ void __launch_bounds__(256) pack_igemm_kernel(const uint16_t* __restr
     }
 }
 
+// Packed layout of the TN form of the channels-last engine (positions as M, horizontal taps in N):
+// blocks ordered [kt][chunk][kh], each the K-major canonical B tile of N = 3 * cp rows x 64 input
+// channels, [8 planes][N rows][8 channels], where row kw * cp + co carries tap (kt, kh, kw) of output
+// channel co (zero for co >= C_out and for input channels >= C_in).
+__global__ void __launch_bounds__(256) pack_tn_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                      int C_in, int C_out, int KT, int n_chunks, int cp, size_t total) {
+    const int N = 3 * cp;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        size_t r = i;
+        const int e = (int)(r % 8); r /= 8;
+        const int row = (int)(r % N); r /= N;
+        const int j = (int)(r % 8); r /= 8;
+        const int kh = (int)(r % 3); r /= 3;
+        const int cc = (int)(r % n_chunks); r /= n_chunks;
+        const int kt = (int)r;
+        const int kw = row / cp, co = row - kw * cp;
+        const int ci = cc * 64 + j * 8 + e;
+        uint16_t v = 0;
+        if (co < C_out && ci < C_in) v = w[(((size_t)co * C_in + ci) * KT + kt) * 9 + kh * 3 + kw];
+        out[i] = v;
+    }
+}
+
+static x3_status launch_pack_tn(const x3_conv_plan* p, const ClGeom& g, const void* w, void* out, cudaStream_t s) {
+    const size_t total = cl_packed_bytes(g) / 2;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pack_tn_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)out, p->d.C_in, p->d.C_out, g.KT,
+                                                   g.n_chunks, g.tn_cp, total);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+    return X3_OK;
+}
+
 // Packed layout of the head form of the channels-last engine: blocks ordered [kt][chunk][kh], each
 // the K-major canonical A tile of 128 rows x 64 input channels, [8 planes][128 rows][8 channels],
 // where row 32*g + kw*10 + r carries tap (kt, kh, kw) of output channel 10*g + r (zero elsewhere).
@@ -317,6 +351,7 @@ x3_status launch_pack_weights(const x3_conv_plan* p, const void* w, void* w_pack
     // the channels-last form's weight blocks (128, or 64 in the M = 64 form, output channels x 64
     // input channels per tap)
     const ClGeom& g = p->cl_shadow;
+    if (g.tn) return launch_pack_tn(p, g, w, (uint8_t*)w_packed + p->shadow_w_off, s);
     const int rows = g.m64 ? 64 : 128;
     PackArgs a{p->d.C_in, p->d.C_out, 1, rows, 64, g.n_chunks, g.n_tiles};
     const size_t total = (size_t)g.n_tiles * g.n_chunks * 9 * rows * 64;
@@ -340,6 +375,7 @@ static x3_status pack_primary(const x3_conv_plan* p, const void* w, void* w_pack
         if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
         return X3_OK;
     }
+    if (p->kind == K_IGEMM_CL && p->cl.tn) return launch_pack_tn(p, p->cl, w, w_packed, s);
     if (p->kind == K_IGEMM_CL && p->cl.stn) {
         const size_t total = p->packed_bytes / 2;
         size_t blocks = (total + 255) / 256;

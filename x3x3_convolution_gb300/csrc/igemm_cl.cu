@@ -65,6 +65,29 @@ constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (ev
 constexpr int kStnPitch = 67;     // STN: fp32 staging row (the 66 TMEM columns a chunk reads + pad) per tap row
 constexpr int kStnStageBytes = 27 * kStnPitch * 4;  // 27 rows: 9 taps x 3 channels
 
+// Division by a run-time constant d without a division instruction: for 0 <= x < 2^31,
+// x / d == (x * m) >> s with l = ceil(log2 d), s = 31 + l and m = ceil(2^s / d) < 2^32 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994: the error of m is below d,
+// so x * (m * d - 2^s) < 2^s and the floor is exact). Every role of the kernel decodes every tile, and
+// on the MMA issuer's single thread a run-time integer division costs hundreds of cycles.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    uint32_t l = 0;
+    while (l < 31 && (1u << l) < d) ++l;
+    f.d = d;
+    f.s = 31 + l;
+    f.m = (uint32_t)(((1ull << f.s) + d - 1) / d);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv& f) {
+    return (uint32_t)(((uint64_t)x * f.m) >> f.s);
+}
+
 struct ClArgs {
     int C_in, C_out, N, D, H, W, H_out, W_out, dout, act, has_carry;
     int KT, n_chunks, n_tiles, Wt, P, HR, strips, windows, frames;
@@ -80,7 +103,10 @@ struct ClArgs {
     int frame_inner; // tile order with the output frame varying fastest
     int g_f32;       // centre-tap form: the tap planes of G in fp32 (else bf16)
     int stage_warp;  // epilogue staging bytes per warp
+    int tn_cp, tn_n; // TN: output channels padded to 16, MMA N (3 horizontal taps x tn_cp)
+    int x_bytes;     // TN: bytes after the staging blocks (kw-sum exchange between warps, bias)
     long long tiles;
+    FastDiv fd_frames, fd_ntiles, fd_windows, fd_strips, fd_dout, fd_P, fd_chunks;
     uint32_t idesc;
     const uint8_t* w;
     const void* bias;
@@ -97,26 +123,30 @@ struct ClTile {
 __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
     ClTile c;
     uint32_t t = (uint32_t)tile;
+    uint32_t q;
     if (a.frame_inner) {
         // frames fastest: the output frames of one window are in flight together, so the input frames
         // they share (three temporal taps each) are read from DRAM once and then hit in L2
-        const uint32_t fr = (uint32_t)a.frames, nt = (uint32_t)a.n_tiles, wn = (uint32_t)a.windows;
-        c.fr = (int)(t % fr);
-        t /= fr;
-        c.nt = (int)(t % nt);
-        t /= nt;
-        c.win = (int)(t % wn);
-        c.strip = (int)(t / wn);
+        q = fdiv(t, a.fd_frames);
+        c.fr = (int)(t - q * a.fd_frames.d);
+        t = q;
+        q = fdiv(t, a.fd_ntiles);
+        c.nt = (int)(t - q * a.fd_ntiles.d);
+        t = q;
+        q = fdiv(t, a.fd_windows);
+        c.win = (int)(t - q * a.fd_windows.d);
+        c.strip = (int)q;
         return c;
     }
-    const uint32_t nt = (uint32_t)a.n_tiles, wn = (uint32_t)a.windows, st = (uint32_t)a.strips;
-    c.nt = (int)(t % nt);
-    t /= nt;
-    c.win = (int)(t % wn);
-    t /= wn;
-    c.strip = (int)(t % st);
-    t /= st;
-    c.fr = (int)t;
+    q = fdiv(t, a.fd_ntiles);
+    c.nt = (int)(t - q * a.fd_ntiles.d);
+    t = q;
+    q = fdiv(t, a.fd_windows);
+    c.win = (int)(t - q * a.fd_windows.d);
+    t = q;
+    q = fdiv(t, a.fd_strips);
+    c.strip = (int)(t - q * a.fd_strips.d);
+    c.fr = (int)q;
     return c;
 }
 
@@ -217,9 +247,21 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // staged as its four phases, even or odd rows by even or odd columns, each box loaded by the TMA
 // unit with element strides of 2. A phase is one pipeline group that feeds only the taps reading it
 // (one, two, two and four of the nine), each at a shift of 0 or 1 row and column (s2_tap).
+// TN (2D channels-last, stride 1, at most 80 output channels): the operands the other way round, with
+// the three horizontal taps in N. A = 128 consecutive raster positions of the staged halo (M = 128,
+// 128-byte swizzle), B = the weights of one kernel row kh for all three kw, N = 3 x C_out rows
+// (kw, output channel), resident in shared memory. One MMA per (kh, K step) leaves in TMEM
+// D[i][(kw, co)] = sum_kh w[co, kh, kw] . x[halo position i + kh P], i.e. the kw tap's contribution to
+// output position i - kw, so the epilogue forms out[j] = D[j][(0,co)] + D[j+1][(1,co)] + D[j+2][(2,co)].
+// The raster pitch is 32 (30 output columns and the two junk columns per strip row) and a tile is four
+// whole raster rows, so TMEM lane quarter q (epilogue warp q) holds exactly raster row q of the tile:
+// the j+1 and j+2 terms are shuffles down by one and two lanes inside the warp, and the two lanes that
+// would reach into the next row are the junk columns. Every MMA row is an output position (or one of
+// the two junk columns), where the M = 64 form leaves half of the tensor core's rows empty; three MMAs
+// per 16 input channels instead of nine.
 template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool W2 = false,
-          bool STN = false, bool S2 = false>
-__global__ void __launch_bounds__(NC ? 320 : 192, 1)
+          bool STN = false, bool S2 = false, bool TN = false>
+__global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ ClArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -229,7 +271,9 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
     const uint32_t sStage = sW + (uint32_t)a.w_smem;               // epilogue transpose tile
-    const uint32_t sRaw = sStage + 4u * (uint32_t)a.stage_warp;              // NCHW raw tiles (128-aligned)
+    constexpr int kEpiWarps = TN ? 8 : 4;  // TN: two epilogue warps per TMEM lane quarter
+    const uint32_t sBiasT = sStage + (uint32_t)kEpiWarps * (uint32_t)a.stage_warp;  // TN: each epilogue warp's bias copy
+    const uint32_t sRaw = sBiasT + (uint32_t)a.x_bytes;                      // NCHW raw tiles (128-aligned)
     const uint32_t sJunk = sRaw + (uint32_t)(a.n_raw * a.raw_bytes);         // NCHW: 16 B per transposer lane
     const uint32_t sBar = sJunk + (NC ? 4u * 32u * 16u : 0u);
     const uint32_t bar_h_full = sBar;
@@ -265,7 +309,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_acc_full + 8 * i, 1);
-            ptx::mbar_init(bar_acc_empty + 8 * i, 4);
+            ptx::mbar_init(bar_acc_empty + 8 * i, kEpiWarps);
         }
         ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -308,11 +352,12 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             uint32_t h_cnt = 0, w_cnt = 0, r_cnt = 0;
             RingPos hr, wr;  // halo and weight ring positions of h_cnt and w_cnt
             bool ok = true;
-            if (M64) {  // every weight block of the layer, once, on the first weight barrier
-                const int nblk = a.KT * a.n_chunks * 9;
-                ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)(nblk * kWBlock64));
+            if (M64 || TN) {  // every weight block of the layer, once, on the first weight barrier
+                const int nblk = a.KT * a.n_chunks * (TN ? 3 : 9);
+                const uint32_t bb = TN ? (uint32_t)a.tn_n * 128u : (uint32_t)kWBlock64;
+                ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)nblk * bb);
                 for (int b = 0; b < nblk; ++b)
-                    ptx::bulk_load(sW + (uint32_t)(b * kWBlock64), a.w + (size_t)b * kWBlock64, (uint32_t)kWBlock64, bar_w_full);
+                    ptx::bulk_load(sW + (uint32_t)b * bb, a.w + (size_t)b * bb, bb, bar_w_full);
                 w_cnt = 1;
                 wr.next(a.n_w);
             }
@@ -320,17 +365,17 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 const long long tile = cl_tile_of(k);
                 if (tile >= a.tiles) break;
                 const ClTile tc = cl_decode(a, tile);
-                const int n = tc.fr / a.dout, t = tc.fr % a.dout;
-                const int r0 = (tc.win * a.win_adv) / a.P;
+                const int n = (int)fdiv((uint32_t)tc.fr, a.fd_dout), t = tc.fr - n * a.dout;
+                const int r0 = (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P);
                 const int ow0 = tc.strip * a.Wt;
                 for (int gi = 0; gi < n_groups && ok; ++gi) {
                     int kt, cc;
                     if (KWM) {
                         const int gg = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
-                        kt = gg / a.n_chunks;
+                        kt = (int)fdiv((uint32_t)gg, a.fd_chunks);
                         cc = gg - kt * a.n_chunks;
                     } else {
-                        kt = gi / a.n_chunks;
+                        kt = (int)fdiv((uint32_t)gi, a.fd_chunks);
                         cc = gi - kt * a.n_chunks;
                     }
                     const void* map = &tm_x;
@@ -382,7 +427,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         }
                         const uint8_t* wblk =
                             a.w + ((((size_t)tc.nt * a.KT + (S2 ? 0 : kt)) * a.n_chunks + cc) * kTapsK) * (size_t)kWBlock;
-                        for (int ti = 0; ti < ((M64 || CTR) ? 0 : (S2 ? s2_ntaps(kt) : kTapsK)); ++ti) {
+                        for (int ti = 0; ti < ((M64 || CTR || TN) ? 0 : (S2 ? s2_ntaps(kt) : kTapsK)); ++ti) {
                             int tap = KWM ? (ti + rot_t < kTapsK ? ti + rot_t : ti + rot_t - kTapsK) : ti;
                             if (S2) {  // the phase's taps, in the MMA issuer's order
                                 int kh, kw;
@@ -428,7 +473,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             constexpr int kRows = M64 ? 64 : kBM;  // rows of a weight block (MMA M)
             const uint32_t a_hi = (128u >> 4) | (1u << 14);
             const uint32_t a_lo0 = ((sW >> 4) & 0x3FFFu) | ((uint32_t)((kRows * 16) >> 4) << 16);
-            if (M64) {  // resident weights
+            if (M64 || TN) {  // resident weights
                 if (!cl_wait(bar_w_full, 0, abort_flag, a.status)) ok = false;
                 ptx::tc_fence_after();
             }
@@ -446,7 +491,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 for (long long k = 0;; ++k) {
                     const long long tile = cl_tile_of(k);
                     if (tile >= a.tiles) break;
-                    if (a.KT == 3 && cl_decode(a, tile).fr % a.dout < 2) last_carry_k = k;
+                    if (a.KT == 3) {
+                        const int fr = cl_decode(a, tile).fr;
+                        if (fr - (int)fdiv((uint32_t)fr, a.fd_dout) * a.dout < 2) last_carry_k = k;
+                    }
                 }
                 if (last_carry_k < 0) ptx::grid_dep_launch();
             }
@@ -454,7 +502,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                 const long long tile = cl_tile_of(k);
                 if (tile >= a.tiles) break;
                 const ClTile tc = cl_decode(a, tile);
-                const int pos_off = (tc.win * a.win_adv) % a.P;
+                const int pos_off = tc.win * a.win_adv - (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P) * a.P;
                 // two accumulator buffers used alternately, or (W2) one pair of them per tile
                 const uint32_t ab = W2 ? 0u : (it & 1u);
                 const uint32_t use = W2 ? it : (it >> 1);
@@ -519,7 +567,49 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     hbase = sH + sh * (uint32_t)a.h_bytes;
                     return true;
                 };
-                if constexpr (KWM) {
+                if constexpr (TN) {
+                    // positions as M: per (kt, chunk) halo and kernel row kh, A = the 128 positions from
+                    // halo position pos_off + kh P (swizzled K-major rows), B = the resident (kw, co) rows
+                    // of weight block (kt, chunk, kh) (no swizzle: LBO = N x 16 B between the two
+                    // 8-channel halves of a K step, SBO = 128 B between 8-row groups)
+                    const uint32_t tn_blk = (uint32_t)a.tn_n * 128u;
+                    const uint32_t bw_hi = (128u >> 4) | (1u << 14);
+                    for (int kt = 0; kt < a.KT && ok; ++kt) {
+                        for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
+                            uint32_t sh, hbase;
+                            if (!group_begin(sh, hbase)) { ok = false; break; }
+                            for (int kh = 0; kh < 3; ++kh) {
+                                const uint32_t arow = hbase + (uint32_t)(pos_off + kh * a.P) * 128u;
+                                const uint32_t wb = sW + (uint32_t)((kt * a.n_chunks + cc) * 3 + kh) * tn_blk;
+                                const uint32_t bw_lo0 = ((wb >> 4) & 0x3FFFu) | ((uint32_t)((a.tn_n * 16) >> 4) << 16);
+                                const int nks = min(a.C_in - cc * kCK, kCK) > 48 ? 4 : (min(a.C_in - cc * kCK, kCK) + 15) / 16;
+                                if (nks == 4) {
+                                    uint64_t ad[4], bd[4];
+#pragma unroll
+                                    for (int ks = 0; ks < 4; ++ks) {
+                                        ad[ks] = ((uint64_t)b_hi_fixed << 32) |
+                                                 (uint64_t)((((arow + (uint32_t)ks * 32u) >> 4) & 0x3FFFu) | (1u << 16));
+                                        bd[ks] = ((uint64_t)bw_hi << 32) |
+                                                 (uint64_t)(bw_lo0 + (uint32_t)ks * (uint32_t)((2 * a.tn_n * 16) >> 4));
+                                    }
+                                    ptx::mma4_f16(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3], a.idesc, acc);
+                                } else {
+                                    for (int ks = 0; ks < nks; ++ks) {
+                                        const uint64_t adesc = ((uint64_t)b_hi_fixed << 32) |
+                                                               (uint64_t)((((arow + (uint32_t)ks * 32u) >> 4) & 0x3FFFu) | (1u << 16));
+                                        const uint64_t bdesc = ((uint64_t)bw_hi << 32) |
+                                                               (uint64_t)(bw_lo0 + (uint32_t)ks * (uint32_t)((2 * a.tn_n * 16) >> 4));
+                                        ptx::mma_f16(d, adesc, bdesc, a.idesc, ks > 0 ? 1u : acc);
+                                    }
+                                }
+                                acc = 1;
+                            }
+                            ptx::mma_commit(bar_h_empty + 8 * sh);
+                            ++h_cnt;
+                            hr.next(a.n_h);
+                        }
+                    }
+                } else if constexpr (KWM) {
                     // head form: rotated (kt, chunk) groups, rotated kh taps (kw is folded into M)
                     for (int gi = 0; gi < n_groups && ok; ++gi) {
                         const int gg = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
@@ -580,10 +670,10 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             cl_wait(bar_drain, 0, &dummy, a.status);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue: TMEM -> channels-last rows
         const int q = warp & 3;            // TMEM lane quarter = output channels 32q .. 32q+31
-        const int ew = warp - 2;           // 0..3: this warp's staging block
+        const int ew = warp - 2;           // 0..3 (TN: 0..7): this warp's staging block
         uint32_t it = 0;
         int cur_nt = -1;
         float bias_r = 0.0f;
@@ -617,6 +707,18 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
         const float act_lo = a.act == X3_ACT_RELU ? 0.0f : (a.act == X3_ACT_CLAMP1 ? -1.0f : -INFINITY);
         const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
         const float inv_p = 1.0f / (float)a.P;
+        if (TN) {  // this warp's copy of the bias (zero past C_out)
+            float* sb = reinterpret_cast<float*>(sbase + (sBiasT - base)) + ew * a.tn_cp;
+            for (int co = lane; co < a.tn_cp; co += 32) {
+                float b = 0.0f;
+                if (a.bias && co < a.C_out) {
+                    const uint16_t raw = __ldg(reinterpret_cast<const unsigned short*>(a.bias) + co);
+                    b = BF16 ? __uint_as_float((uint32_t)raw << 16) : __half2float(__ushort_as_half(raw));
+                }
+                sb[co] = b;
+            }
+            __syncwarp();
+        }
         for (long long k = 0;; ++k, ++it) {
             const long long tile = cl_tile_of(k);
             if (tile >= a.tiles) break;
@@ -624,7 +726,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
             if (!cl_wait(bar_acc_full + 8 * ab, (W2 ? it : (it >> 1)) & 1u, abort_flag, a.status)) break;
             ptx::tc_fence_after();
             const ClTile tc = cl_decode(a, tile);
-            const int n = tc.fr / a.dout, t = tc.fr % a.dout;
+            const int n = (int)fdiv((uint32_t)tc.fr, a.fd_dout), t = tc.fr - n * a.dout;
             constexpr int kCpw = M64 ? 16 : 32;  // accumulator rows per TMEM lane quarter
             const int co_lane = (M64 && lane >= 16) ? a.C_out : tc.nt * (M64 ? 64 : kBM) + q * kCpw + lane;
             if (tc.nt != cur_nt) {
@@ -658,7 +760,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                         __syncwarp();
                         const int jw = chunk * 32 + lane;  // column of the window
                         const int m = m0 + jw;
-                        const int oh = m / a.P, c = m % a.P;
+                        const int oh = (int)fdiv((uint32_t)m, a.fd_P), c = m - oh * a.P;
                         const int ow = ow0 + c;
                         if (jw < a.win_adv && c < a.Wt && ow < a.W_out && oh < a.H_out) {
                             const size_t W2o = 2 * (size_t)a.W_out;
@@ -676,6 +778,62 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 }
                             }
                         }
+                    }
+                }
+            } else if (TN) {
+                // Lane l of quarter q holds raster position (row q of the tile, column l): D[(kw, co)] in
+                // TMEM columns kw * cp + co of this accumulator buffer. out = D(l)[(0,co)] +
+                // D(l+1)[(1,co)] + D(l+2)[(2,co)] + bias: shuffles down by one and two lanes (lanes 30
+                // and 31 are the raster's junk columns). The two warps of a quarter take alternate
+                // 16-channel chunks (two each for 64 channels): all of a warp's TMEM loads are issued
+                // before one wait, and each lane stores its position's channels as 16-byte pieces.
+                const int cp = a.tn_cp, nck = cp >> 4, half = ew >> 2;
+                const float* sb = reinterpret_cast<const float*>(sbase + (sBiasT - base)) + ew * cp;
+                const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
+                const int m = m0 + q * 32 + lane;
+                const int oh = (int)fdiv((uint32_t)m, a.fd_P), cc0 = m - oh * a.P;
+                const int ow = ow0 + cc0;
+                const bool valid = cc0 < a.Wt && ow < a.W_out && oh < a.H_out && !(a.sub2 && ((oh | ow) & 1));
+                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
+                const size_t plane = (size_t)a.yH * a.yW;
+                uint16_t* yp = a.out_nchw ? y + (size_t)n * a.C_out * plane + (size_t)yh * a.yW + yw
+                                          : y + (((size_t)n * a.dout + t) * plane + (size_t)yh * a.yW + yw) * a.C_out;
+                auto load = [&](int c, uint32_t (&v0)[16], uint32_t (&v1)[16], uint32_t (&v2)[16]) {
+                    ptx::tmem_ld16(tq + (uint32_t)(16 * c), v0);
+                    ptx::tmem_ld16(tq + (uint32_t)(cp + 16 * c), v1);
+                    ptx::tmem_ld16(tq + (uint32_t)(2 * cp + 16 * c), v2);
+                };
+                auto sum = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16], const uint32_t (&v2)[16]) {
+                    float o[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
+                        const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
+                        o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
+                    }
+                    if (!valid) return;
+                    if (a.out_nchw) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (16 * c + k < a.C_out) yp[(size_t)(16 * c + k) * plane] = cl_round<BF16>(o[k]);
+                    } else {
+                        uint4 w0, w1;
+                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
+                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
+                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
+                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
+                        *reinterpret_cast<uint4*>(yp + 16 * c) = w0;
+                        if (16 * c + 8 < a.C_out) *reinterpret_cast<uint4*>(yp + 16 * c + 8) = w1;
+                    }
+                };
+                {
+                    uint32_t a0[16], a1[16], a2[16], b0[16], b1[16], b2[16];
+                    for (int c = half; c < nck; c += 4) {
+                        load(c, a0, a1, a2);
+                        if (c + 2 < nck) load(c + 2, b0, b1, b2);
+                        ptx::tmem_ld_wait();
+                        sum(c, a0, a1, a2);
+                        if (c + 2 < nck) sum(c + 2, b0, b1, b2);
                     }
                 }
             } else {
@@ -696,7 +854,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                                 T[lane * 34 + j] = cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
                             __syncwarp();
                             const int m = m0 + chunk * 32 + lane;
-                            const int oh = m / a.P, c = m % a.P;
+                            const int oh = (int)fdiv((uint32_t)m, a.fd_P), c = m - oh * a.P;
                             const int ow = ow0 + c;
                             const bool keep = c < a.Wt && ow < a.W_out && oh < a.H_out && !(a.sub2 && ((oh | ow) & 1));
                             if (keep) {
@@ -726,7 +884,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                     const uint32_t st_addr = wst + (uint32_t)((8 * (mi >> 1) + jr) * 32 + (mi & 1) * 16);
                     // the window's first raster row and column; a position's row and column follow from
                     // its offset by a float reciprocal (exact: offsets < 512, pitch <= 256)
-                    const int oh0 = m0 / a.P, c00 = m0 - oh0 * a.P;
+                    const int oh0 = (int)fdiv((uint32_t)m0, a.fd_P), c00 = m0 - oh0 * a.P;
                     uint16_t* yf = y + ((size_t)n * a.dout + t) * (size_t)a.yH * a.yW * a.C_out;
                     auto stage = [&](int slot, const uint32_t (&v)[16]) {
                         uint32_t h[8];
@@ -882,7 +1040,7 @@ __global__ void __launch_bounds__(NC ? 320 : 192, 1)
                             const int row = M64 ? k * 16 + (lane >> 1) : k * 8 + (lane >> 2);
                             const int seg = M64 ? (lane & 1) : (lane & 3);
                             const int m = m0 + chunk * 32 + row;
-                            const int oh = m / a.P, c = m % a.P;
+                            const int oh = (int)fdiv((uint32_t)m, a.fd_P), c = m - oh * a.P;
                             const int ow = ow0 + c;
                             const int co = tc.nt * (M64 ? 64 : kBM) + q * kCpw + seg * 8;
                             if (c < a.Wt && ow < a.W_out && oh < a.H_out && co < a.C_out &&
@@ -1034,6 +1192,11 @@ bool pdl_enabled() {
     return on;
 }
 
+size_t cl_packed_bytes(const ClGeom& g) {
+    if (g.tn) return (size_t)g.KT * g.n_chunks * 3 * g.tn_n * 128;
+    return (size_t)g.n_tiles * g.KT * g.n_chunks * (g.kwm ? 3 : 9) * ((g.m64 ? 64 : kBM) * kCK * 2);
+}
+
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     const x3_conv_desc& d = p->d;
     ClGeom g;
@@ -1094,6 +1257,43 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // resident in shared memory; if no tiling leaves room for them, the 128-row form
     g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
     if (g.m64) g.n_tiles = 1;
+    // 2D layers with at most 80 output channels (when asked for), stride 1: positions as M with the
+    // horizontal taps in N (TN), unless X3CONV_TN=0; falls back to the M = 64 form when no tiling fits
+    {
+        const char* tn_env = getenv("X3CONV_TN");
+        const int cp = (d.C_out + 15) / 16 * 16;
+        if (small_cout && d.dims == 2 && !g.s2 && !g.nchw && !g.kwm && !g.ctr && d.C_out <= 80 &&
+            !(tn_env && !strcmp(tn_env, "0"))) {
+            const int tn_n = 3 * cp;
+            // eight epilogue warps, two per TMEM lane quarter, each holding a copy of the bias (they store
+            // straight from registers: no staging blocks)
+            const int stage_warp = 0;
+            const int x_bytes = 32 * cp;
+            const int tfixed = 1024 + 8 * stage_warp + 512 + x_bytes;
+            const int wres = g.KT * g.n_chunks * 3 * tn_n * 128;
+            // pitch 32: a tile (128 positions) is four whole raster rows of 30 output columns and two
+            // junk columns, one row per TMEM lane quarter; the halo is those rows plus one above and
+            // one below (six rows of 32 positions)
+            const int P = 32, Wt = 30, HR = 6;
+            const int h_bytes = HR * P * 128;
+            int n_h = (kSmemLimit - tfixed - wres) / h_bytes;
+            if (n_h > 4) n_h = 4;
+            long long best = -1;
+            if (n_h >= 2) {
+                best = 0;
+                g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
+                g.n_h = n_h; g.n_w = 1; g.strips = (W_out + Wt - 1) / Wt; g.windows = (H_out + 3) / 4;
+                g.tiles = (long long)g.strips * g.windows * g.frames;
+                g.w_smem = wres; g.n_raw = 0; g.raw_w = g.raw_bytes = g.raw_tx_bytes = 0;
+                g.stage_warp = stage_warp; g.x_bytes = x_bytes;
+                g.smem_bytes = tfixed + n_h * h_bytes + wres;
+            }
+            if (best >= 0) {
+                g.tn = 1; g.tn_cp = cp; g.tn_n = tn_n; g.m64 = 0; g.n_tiles = 1; g.win_adv = 128;
+                found = true;
+            }
+        }
+    }
     if (g.stn) {
         // stencil head: 16 x 16 raster windows (pitch 16, 14 output columns and rows inside one
         // halo column and row on each side), consecutive windows of a strip two rows apart in overlap
@@ -1123,7 +1323,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         g.tiles = (long long)g.windows * g.frames;
         found = true;
     }
-  for (int attempt = 0; attempt < 2 && !found && !g.ctr; ++attempt) {
+  for (int attempt = 0; attempt < 2 && !found && !g.ctr && !g.tn; ++attempt) {
     if (attempt == 1) {
         if (!g.m64) break;
         g.m64 = 0;
@@ -1228,7 +1428,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
     p->g.BN = g.m64 ? 64 : kBM; p->g.CK = kCK; p->g.n_chunks = g.n_chunks; p->g.n_tiles = g.n_tiles; p->g.KT = g.KT;
-    p->g.b_bytes = g.m64 ? kWBlock64 : kWBlock;
+    p->g.b_bytes = g.tn ? g.tn_n * 128 : (g.m64 ? kWBlock64 : kWBlock);
     return true;
 }
 
@@ -1245,6 +1445,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.H_out = H_out; a.W_out = W_out; a.dout = d.dims == 3 ? d.D : 1; a.act = d.act;
     a.sub2 = g.sub2; a.out_nchw = out_nchw; a.yH = yH; a.yW = yW; a.w_smem = g.w_smem;
     a.stage_warp = g.stage_warp;
+    a.tn_cp = g.tn_cp; a.tn_n = g.tn_n; a.x_bytes = g.x_bytes;
     a.frame_inner = g.ctr;
     a.g_f32 = d.kernel == X3_KERNEL_HEAD_SPLIT ? 1 : 0;
     a.has_carry = carry != nullptr;
@@ -1253,7 +1454,14 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
     a.win_adv = g.win_adv; a.ngroups = g.ngroups; a.ctr = g.ctr;
     a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes; a.raw_tx_bytes = g.raw_tx_bytes; a.n_raw = g.n_raw;
-    a.idesc = ptx::idesc_f16(g.m64 ? 64 : kBM, kBNP, bf16);
+    a.idesc = g.tn ? ptx::idesc_f16(kBM, g.tn_n, bf16) : ptx::idesc_f16(g.m64 ? 64 : kBM, kBNP, bf16);
+    a.fd_frames = make_fastdiv((uint32_t)g.frames);
+    a.fd_ntiles = make_fastdiv((uint32_t)g.n_tiles);
+    a.fd_windows = make_fastdiv((uint32_t)g.windows);
+    a.fd_strips = make_fastdiv((uint32_t)g.strips);
+    a.fd_dout = make_fastdiv((uint32_t)a.dout);
+    a.fd_P = make_fastdiv((uint32_t)g.P);
+    a.fd_chunks = make_fastdiv((uint32_t)g.n_chunks);
     a.w = (const uint8_t*)w_packed; a.bias = bias; a.y = y;
     x3_status st0 = device_status_word(&a.status);
     if (st0 != X3_OK) return st0;
@@ -1279,7 +1487,9 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         }
     }
     void (*k)(CUtensorMap, CUtensorMap, ClArgs);
-    if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true>
+    if (g.tn) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
+                       : igemm_cl_kernel<false, false, false, false, false, false, false, false, true>;
+    else if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true>
                        : igemm_cl_kernel<false, false, false, false, false, true>;
     else if (g.stn) k = igemm_cl_kernel<true, false, false, true, false, false, true>;
     else if (g.ctr) k = igemm_cl_kernel<true, false, false, true>;  // bf16 only (checked by the planner)
@@ -1299,7 +1509,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)g.grid);
-    cfg.blockDim = dim3(g.nchw ? 320u : 192u);
+    cfg.blockDim = dim3((g.nchw || g.tn) ? 320u : 192u);
     cfg.dynamicSmemBytes = (size_t)g.smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr;

@@ -76,6 +76,9 @@ struct ClGeom {
     int w2;                      // 1: a tile is two consecutive windows sharing every weight K slice
     int stn;                     // 1: head with the spatial stencil in the epilogue (centre-tap MMAs)
     int stage_warp;              // epilogue staging bytes per warp
+    int tn;                      // 1: positions as M (128 per tile), the three horizontal taps in N
+    int tn_cp, tn_n;             // tn: output channels padded to 16; MMA N = 3 * tn_cp
+    int x_bytes;                 // tn: shared memory for the kw-sum exchange and the bias copies
     long long tiles;
     int smem_bytes, grid;
 };
@@ -120,6 +123,9 @@ bool igemm_plan(x3_conv_plan* p, int num_sms);  // fills p->g; false if the engi
 // Fills p->cl (+ packing fields of p->g); small_cout also accepts channels-last layers with fewer
 // than 96 output channels (the M tile is then partly empty).
 bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout = false);
+// Bytes of the packed weights of the channels-last engine with tiling g (all its forms but the head
+// forms, which pack their own layouts).
+size_t cl_packed_bytes(const ClGeom& g);
 x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carry, const void* w_packed,
                           const void* bias, void* y, cudaStream_t s);
 // The channels-last form (cl_shadow) of a 2D NCHW layer: x is NHWC with C_in rounded up to 8
