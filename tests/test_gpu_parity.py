@@ -85,7 +85,9 @@ NHWC_CASES = [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"), (
               # positions-as-M form (horizontal taps in N): 80 channels (N = 240), 24 (padded to 32),
               # 8 (padded to 16), a partial last input chunk (136 = 2 x 64 + 8), one-column images
               (1, 64, 80, 19, 301, 1, "relu"), (2, 24, 24, 11, 40, 1, "none"), (1, 64, 8, 5, 260, 1, "relu"),
-              (1, 136, 32, 7, 45, 1, "none"), (3, 16, 16, 6, 1, 1, "relu")]
+              (1, 136, 32, 7, 45, 1, "none"), (3, 16, 16, 6, 1, 1, "relu"),
+              # 64 channels: each raster row leaves by one TMA store, clipped at a ragged right edge
+              (2, 32, 64, 7, 61, 1, "relu")]
 
 
 @pytest.mark.parametrize("variant", ["int", "random"])

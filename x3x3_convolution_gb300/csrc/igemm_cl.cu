@@ -104,7 +104,8 @@ struct ClArgs {
     int g_f32;       // centre-tap form: the tap planes of G in fp32 (else bf16)
     int stage_warp;  // epilogue staging bytes per warp
     int tn_cp, tn_n; // TN: output channels padded to 16, MMA N (3 horizontal taps x tn_cp)
-    int x_bytes;     // TN: bytes after the staging blocks (kw-sum exchange between warps, bias)
+    int x_bytes;     // TN: bytes after the staging blocks (the epilogue warps' bias copies)
+    int tn_tma;      // TN: each warp writes its raster row (64 channels) with one TMA store (tm_y)
     long long tiles;
     FastDiv fd_frames, fd_ntiles, fd_windows, fd_strips, fd_dout, fd_P, fd_chunks;
     uint32_t idesc;
@@ -263,7 +264,7 @@ template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool
           bool STN = false, bool S2 = false, bool TN = false>
 __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
-                    const __grid_constant__ ClArgs a) {
+                    const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ ClArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     const uint32_t sH = base;                                      // halo stages (1024-aligned)
     const uint32_t sW = sH + (uint32_t)(a.n_h * a.h_bytes);        // weight blocks
     const uint32_t sStage = sW + (uint32_t)a.w_smem;               // epilogue transpose tile
-    constexpr int kEpiWarps = TN ? 8 : 4;  // TN: two epilogue warps per TMEM lane quarter
+    constexpr int kEpiWarps = TN ? 8 : 4;  // TN: two groups of four epilogue warps, taking alternate tiles
     const uint32_t sBiasT = sStage + (uint32_t)kEpiWarps * (uint32_t)a.stage_warp;  // TN: each epilogue warp's bias copy
     const uint32_t sRaw = sBiasT + (uint32_t)a.x_bytes;                      // NCHW raw tiles (128-aligned)
     const uint32_t sJunk = sRaw + (uint32_t)(a.n_raw * a.raw_bytes);         // NCHW: 16 B per transposer lane
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar_acc_full + 8 * i, 1);
-            ptx::mbar_init(bar_acc_empty + 8 * i, kEpiWarps);
+            ptx::mbar_init(bar_acc_empty + 8 * i, 4);  // the four warps that drain the buffer
         }
         ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -318,6 +319,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tm_x);
         ptx::prefetch_tmap(&tm_c);
+        if (TN && a.tn_tma) ptx::prefetch_tmap(&tm_y);
     }
     if (warp == 1) {
         ptx::tmem_alloc(s_tmem, 512u);
@@ -484,6 +486,13 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             // 128-byte rows (a spatial tap) or by 32-byte K steps needs no base-offset correction;
             // the integer-exact parity tests pin this.
             const uint32_t b_hi_fixed = (1024u >> 4) | (1u << 14) | (2u << 29);
+            // TN: descriptor of the first resident weight block (SBO 128 B, LBO N x 16 B, version 1), the
+            // descriptor step between blocks and between the K steps of a block (N x 32 B)
+            const uint64_t tn_wdesc0 = TN ? (((uint64_t)((128u >> 4) | (1u << 14)) << 32) |
+                                             (uint64_t)(((sW >> 4) & 0x3FFFu) | ((uint32_t)((a.tn_n * 16) >> 4) << 16)))
+                                          : 0;
+            const uint32_t tn_wstep = TN ? (uint32_t)a.tn_n * 8u : 0u;   // N x 128 B / 16
+            const uint32_t tn_kstep = TN ? (uint32_t)a.tn_n * 2u : 0u;   // N x 32 B / 16
             // with a carry: the last of this CTA's tiles that reads it (output frame 0 or 1 of the
             // pass); the launch signal follows that tile's halo waits
             long long last_carry_k = -1;
@@ -501,6 +510,53 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             for (long long k = 0; ok; ++k) {
                 const long long tile = cl_tile_of(k);
                 if (tile >= a.tiles) break;
+                if constexpr (TN) {
+                    // positions as M: per (kt, chunk) halo and kernel row kh, A = the 128 positions from
+                    // halo position kh P (swizzled K-major rows; windows start at a raster row), B = the
+                    // resident (kw, co) rows of weight block (kt, chunk, kh) (no swizzle: LBO = N x 16 B
+                    // between the two 8-channel halves of a K step, SBO = 128 B between 8-row groups).
+                    // Descriptors are a base descriptor plus the byte offset / 16 (the 14-bit address
+                    // field cannot carry: shared memory is below 256 KB). The tile needs no decode here;
+                    // its first halo is awaited before the accumulator, so that the MMAs follow the
+                    // accumulator wait directly.
+                    const uint32_t ab = it & 1u, use = it >> 1;
+                    const uint32_t d = tmem_base + ab * (uint32_t)kBNP;
+                    uint32_t acc = 0;
+                    for (int g = 0; g < a.KT * a.n_chunks && ok; ++g) {
+                        const int kt = (int)fdiv((uint32_t)g, a.fd_chunks), cc = g - kt * a.n_chunks;
+                        const uint32_t sh = hr.slot;
+                        if (!cl_wait(bar_h_full + 8 * sh, hr.phase, abort_flag, a.status)) { ok = false; break; }
+                        if (g == 0 && !cl_wait(bar_acc_empty + 8 * ab, (use & 1u) ^ 1u, abort_flag, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
+                        const uint64_t a0 = ((uint64_t)b_hi_fixed << 32) | (uint64_t)(((hbase >> 4) & 0x3FFFu) | (1u << 16));
+                        const uint64_t w0 = tn_wdesc0 + (uint64_t)((uint32_t)((kt * a.n_chunks + cc) * 3) * tn_wstep);
+                        const int rem = a.C_in - cc * kCK;
+#pragma unroll
+                        for (int kh = 0; kh < 3; ++kh) {
+                            const uint64_t ak = a0 + (uint64_t)((uint32_t)(kh * a.P) * 8u);  // kh P rows x 128 B / 16
+                            const uint64_t bk = w0 + (uint64_t)((uint32_t)kh * tn_wstep);
+                            if (rem >= kCK) {
+                                ptx::mma4_f16(d, ak, ak + 2, ak + 4, ak + 6, bk, bk + tn_kstep, bk + 2 * tn_kstep,
+                                              bk + 3 * tn_kstep, a.idesc, acc);
+                            } else {
+                                for (int ks = 0; ks * 16 < rem; ++ks)
+                                    ptx::mma_f16(d, ak + 2 * ks, bk + (uint64_t)(ks * tn_kstep), a.idesc, ks > 0 ? 1u : acc);
+                            }
+                            acc = 1;
+                        }
+                        ptx::mma_commit(bar_h_empty + 8 * sh);
+                        ++h_cnt;
+                        hr.next(a.n_h);
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(bar_acc_full + 8 * ab);
+                    ++it;
+                    continue;
+                }
                 const ClTile tc = cl_decode(a, tile);
                 const int pos_off = tc.win * a.win_adv - (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P) * a.P;
                 // two accumulator buffers used alternately, or (W2) one pair of them per tile
@@ -567,49 +623,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     hbase = sH + sh * (uint32_t)a.h_bytes;
                     return true;
                 };
-                if constexpr (TN) {
-                    // positions as M: per (kt, chunk) halo and kernel row kh, A = the 128 positions from
-                    // halo position pos_off + kh P (swizzled K-major rows), B = the resident (kw, co) rows
-                    // of weight block (kt, chunk, kh) (no swizzle: LBO = N x 16 B between the two
-                    // 8-channel halves of a K step, SBO = 128 B between 8-row groups)
-                    const uint32_t tn_blk = (uint32_t)a.tn_n * 128u;
-                    const uint32_t bw_hi = (128u >> 4) | (1u << 14);
-                    for (int kt = 0; kt < a.KT && ok; ++kt) {
-                        for (int cc = 0; cc < a.n_chunks && ok; ++cc) {
-                            uint32_t sh, hbase;
-                            if (!group_begin(sh, hbase)) { ok = false; break; }
-                            for (int kh = 0; kh < 3; ++kh) {
-                                const uint32_t arow = hbase + (uint32_t)(pos_off + kh * a.P) * 128u;
-                                const uint32_t wb = sW + (uint32_t)((kt * a.n_chunks + cc) * 3 + kh) * tn_blk;
-                                const uint32_t bw_lo0 = ((wb >> 4) & 0x3FFFu) | ((uint32_t)((a.tn_n * 16) >> 4) << 16);
-                                const int nks = min(a.C_in - cc * kCK, kCK) > 48 ? 4 : (min(a.C_in - cc * kCK, kCK) + 15) / 16;
-                                if (nks == 4) {
-                                    uint64_t ad[4], bd[4];
-#pragma unroll
-                                    for (int ks = 0; ks < 4; ++ks) {
-                                        ad[ks] = ((uint64_t)b_hi_fixed << 32) |
-                                                 (uint64_t)((((arow + (uint32_t)ks * 32u) >> 4) & 0x3FFFu) | (1u << 16));
-                                        bd[ks] = ((uint64_t)bw_hi << 32) |
-                                                 (uint64_t)(bw_lo0 + (uint32_t)ks * (uint32_t)((2 * a.tn_n * 16) >> 4));
-                                    }
-                                    ptx::mma4_f16(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3], a.idesc, acc);
-                                } else {
-                                    for (int ks = 0; ks < nks; ++ks) {
-                                        const uint64_t adesc = ((uint64_t)b_hi_fixed << 32) |
-                                                               (uint64_t)((((arow + (uint32_t)ks * 32u) >> 4) & 0x3FFFu) | (1u << 16));
-                                        const uint64_t bdesc = ((uint64_t)bw_hi << 32) |
-                                                               (uint64_t)(bw_lo0 + (uint32_t)ks * (uint32_t)((2 * a.tn_n * 16) >> 4));
-                                        ptx::mma_f16(d, adesc, bdesc, a.idesc, ks > 0 ? 1u : acc);
-                                    }
-                                }
-                                acc = 1;
-                            }
-                            ptx::mma_commit(bar_h_empty + 8 * sh);
-                            ++h_cnt;
-                            hr.next(a.n_h);
-                        }
-                    }
-                } else if constexpr (KWM) {
+                if constexpr (KWM) {
                     // head form: rotated (kt, chunk) groups, rotated kh taps (kw is folded into M)
                     for (int gi = 0; gi < n_groups && ok; ++gi) {
                         const int gg = gi + rot_g < n_groups ? gi + rot_g : gi + rot_g - n_groups;
@@ -722,6 +736,112 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
         for (long long k = 0;; ++k, ++it) {
             const long long tile = cl_tile_of(k);
             if (tile >= a.tiles) break;
+            // TN: warps 2-5 drain the even tiles (TMEM buffer 0), warps 6-9 the odd ones (buffer 1)
+            if (TN && (int)(it & 1u) != (ew >> 2)) continue;
+            if constexpr (TN) {
+                // everything that does not depend on the accumulator is set up before waiting for it
+                const uint32_t ab = it & 1u;
+                const ClTile tc = cl_decode(a, tile);
+                const int n = (int)fdiv((uint32_t)tc.fr, a.fd_dout), t = tc.fr - n * a.dout;
+                const int m0 = tc.win * a.win_adv;
+                const int ow0 = tc.strip * a.Wt;
+                // Lane l of quarter q holds raster position (row q of the tile, column l): D[(kw, co)] in
+                // TMEM columns kw * cp + co of this accumulator buffer. out = D(l)[(0,co)] +
+                // D(l+1)[(1,co)] + D(l+2)[(2,co)] + bias: shuffles down by one and two lanes (lanes 30
+                // and 31 are the raster's junk columns). Two 16-channel chunks at a time: their six TMEM
+                // loads are issued before one wait; each lane stores its position's channels as 16-byte
+                // pieces.
+                const int cp = a.tn_cp, nck = cp >> 4;
+                const float* sb = reinterpret_cast<const float*>(sbase + (sBiasT - base)) + ew * cp;
+                const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
+                const int m = m0 + q * 32 + lane;
+                const int oh = (int)fdiv((uint32_t)m, a.fd_P), cc0 = m - oh * a.P;
+                const int ow = ow0 + cc0;
+                const bool valid = cc0 < a.Wt && ow < a.W_out && oh < a.H_out && !(a.sub2 && ((oh | ow) & 1));
+                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
+                const size_t plane = (size_t)a.yH * a.yW;
+                uint16_t* yp = a.out_nchw ? y + (size_t)n * a.C_out * plane + (size_t)yh * a.yW + yw
+                                          : y + (((size_t)n * a.dout + t) * plane + (size_t)yh * a.yW + yw) * a.C_out;
+                // TMA-store form (64 channels, channels-last, stride 1): this lane's position is row `lane`
+                // of the warp's 4 KB buffer, 128 bytes, its 16-byte pieces placed by the 128-byte swizzle
+                // (piece u at u ^ (row & 7)), which is also conflict-free for these writes; the warp's
+                // 30 outputs then leave as one box {64 channels, 30 columns, 1 row, 1 frame}, clipped at
+                // the image edge by the TMA unit
+                const bool tma = a.tn_tma != 0;
+                const uint32_t ob = sStage + (uint32_t)(ew * a.stage_warp);
+                const int row_h = (int)fdiv((uint32_t)(m0 + q * 32), a.fd_P);
+                if (tma) {
+                    if (lane == 0) ptx::bulk_wait_group_read0();  // the previous store from this buffer has read it
+                    __syncwarp();
+                }
+                if (!cl_wait(bar_acc_full + 8 * ab, (it >> 1) & 1u, abort_flag, a.status)) break;
+                ptx::tc_fence_after();
+                auto load = [&](int c, uint32_t (&v0)[16], uint32_t (&v1)[16], uint32_t (&v2)[16]) {
+                    ptx::tmem_ld16(tq + (uint32_t)(16 * c), v0);
+                    ptx::tmem_ld16(tq + (uint32_t)(cp + 16 * c), v1);
+                    ptx::tmem_ld16(tq + (uint32_t)(2 * cp + 16 * c), v2);
+                };
+                auto sum = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16], const uint32_t (&v2)[16]) {
+                    float o[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
+                        const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
+                        o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
+                    }
+                    if (tma) {
+                        uint4 w0, w1;
+                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
+                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
+                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
+                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
+                        uint8_t* rowp = sbase + (ob - base) + lane * 128;
+                        *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (lane & 7)) << 4)) = w0;
+                        *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (lane & 7)) << 4)) = w1;
+                        return;
+                    }
+                    if (!valid) return;
+                    if (a.out_nchw) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (16 * c + k < a.C_out) yp[(size_t)(16 * c + k) * plane] = cl_round<BF16>(o[k]);
+                    } else {
+                        uint4 w0, w1;
+                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
+                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
+                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
+                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
+                        *reinterpret_cast<uint4*>(yp + 16 * c) = w0;
+                        if (16 * c + 8 < a.C_out) *reinterpret_cast<uint4*>(yp + 16 * c + 8) = w1;
+                    }
+                };
+                {
+                    uint32_t a0[16], a1[16], a2[16], b0[16], b1[16], b2[16];
+                    for (int c = 0; c < nck; c += 2) {
+                        load(c, a0, a1, a2);
+                        if (c + 1 < nck) load(c + 1, b0, b1, b2);
+                        ptx::tmem_ld_wait();
+                        if (c + 2 >= nck) {
+                            // the accumulator is in registers: hand the TMEM buffer back to the MMA issuer
+                            // before the last sums and stores
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(bar_acc_empty + 8 * ab);
+                        }
+                        sum(c, a0, a1, a2);
+                        if (c + 1 < nck) sum(c + 1, b0, b1, b2);
+                    }
+                }
+                if (tma) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row_h < a.H_out) {
+                        ptx::tma_store_4d(&tm_y, ob, 0, ow0, row_h, n * a.dout + t);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                continue;
+            }
             const uint32_t ab = W2 ? 0u : (it & 1u);
             if (!cl_wait(bar_acc_full + 8 * ab, (W2 ? it : (it >> 1)) & 1u, abort_flag, a.status)) break;
             ptx::tc_fence_after();
@@ -778,62 +898,6 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 }
                             }
                         }
-                    }
-                }
-            } else if (TN) {
-                // Lane l of quarter q holds raster position (row q of the tile, column l): D[(kw, co)] in
-                // TMEM columns kw * cp + co of this accumulator buffer. out = D(l)[(0,co)] +
-                // D(l+1)[(1,co)] + D(l+2)[(2,co)] + bias: shuffles down by one and two lanes (lanes 30
-                // and 31 are the raster's junk columns). The two warps of a quarter take alternate
-                // 16-channel chunks (two each for 64 channels): all of a warp's TMEM loads are issued
-                // before one wait, and each lane stores its position's channels as 16-byte pieces.
-                const int cp = a.tn_cp, nck = cp >> 4, half = ew >> 2;
-                const float* sb = reinterpret_cast<const float*>(sbase + (sBiasT - base)) + ew * cp;
-                const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
-                const int m = m0 + q * 32 + lane;
-                const int oh = (int)fdiv((uint32_t)m, a.fd_P), cc0 = m - oh * a.P;
-                const int ow = ow0 + cc0;
-                const bool valid = cc0 < a.Wt && ow < a.W_out && oh < a.H_out && !(a.sub2 && ((oh | ow) & 1));
-                const int yh = a.sub2 ? oh >> 1 : oh, yw = a.sub2 ? ow >> 1 : ow;
-                const size_t plane = (size_t)a.yH * a.yW;
-                uint16_t* yp = a.out_nchw ? y + (size_t)n * a.C_out * plane + (size_t)yh * a.yW + yw
-                                          : y + (((size_t)n * a.dout + t) * plane + (size_t)yh * a.yW + yw) * a.C_out;
-                auto load = [&](int c, uint32_t (&v0)[16], uint32_t (&v1)[16], uint32_t (&v2)[16]) {
-                    ptx::tmem_ld16(tq + (uint32_t)(16 * c), v0);
-                    ptx::tmem_ld16(tq + (uint32_t)(cp + 16 * c), v1);
-                    ptx::tmem_ld16(tq + (uint32_t)(2 * cp + 16 * c), v2);
-                };
-                auto sum = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16], const uint32_t (&v2)[16]) {
-                    float o[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
-                        const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
-                        o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
-                    }
-                    if (!valid) return;
-                    if (a.out_nchw) {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            if (16 * c + k < a.C_out) yp[(size_t)(16 * c + k) * plane] = cl_round<BF16>(o[k]);
-                    } else {
-                        uint4 w0, w1;
-                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
-                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
-                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
-                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
-                        *reinterpret_cast<uint4*>(yp + 16 * c) = w0;
-                        if (16 * c + 8 < a.C_out) *reinterpret_cast<uint4*>(yp + 16 * c + 8) = w1;
-                    }
-                };
-                {
-                    uint32_t a0[16], a1[16], a2[16], b0[16], b1[16], b2[16];
-                    for (int c = half; c < nck; c += 4) {
-                        load(c, a0, a1, a2);
-                        if (c + 2 < nck) load(c + 2, b0, b1, b2);
-                        ptx::tmem_ld_wait();
-                        sum(c, a0, a1, a2);
-                        if (c + 2 < nck) sum(c + 2, b0, b1, b2);
                     }
                 }
             } else {
@@ -1118,6 +1182,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
         }
     }
 
+    if (TN && a.tn_tma && warp >= 2 && lane == 0) ptx::bulk_wait_group0();  // this warp's row stores are done
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -1257,6 +1322,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     // resident in shared memory; if no tiling leaves room for them, the 128-row form
     g.m64 = (small_cout && d.C_out <= 64 && !g.nchw && !g.kwm && !g.ctr) ? 1 : 0;
     if (g.m64) g.n_tiles = 1;
+    constexpr int HR_TN = 6;
     // 2D layers with at most 80 output channels (when asked for), stride 1: positions as M with the
     // horizontal taps in N (TN), unless X3CONV_TN=0; falls back to the M = 64 form when no tiling fits
     {
@@ -1265,16 +1331,19 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         if (small_cout && d.dims == 2 && !g.s2 && !g.nchw && !g.kwm && !g.ctr && d.C_out <= 80 &&
             !(tn_env && !strcmp(tn_env, "0"))) {
             const int tn_n = 3 * cp;
-            // eight epilogue warps, two per TMEM lane quarter, each holding a copy of the bias (they store
-            // straight from registers: no staging blocks)
-            const int stage_warp = 0;
+            // eight epilogue warps, each holding a copy of the bias; with 64 channels each also stages its
+            // raster row (32 positions x 128 B, 1024-aligned) for a TMA store, other widths store straight
+            // from registers
             const int x_bytes = 32 * cp;
-            const int tfixed = 1024 + 8 * stage_warp + 512 + x_bytes;
             const int wres = g.KT * g.n_chunks * 3 * tn_n * 128;
+            int stage_warp = cp == 64 ? 4096 : 0;
+            if (stage_warp && 1024 + 8 * stage_warp + 512 + x_bytes + wres + 2 * HR_TN * 32 * 128 > kSmemLimit)
+                stage_warp = 0;  // no room for the row buffers next to two halo stages: direct stores
+            const int tfixed = 1024 + 8 * stage_warp + 512 + x_bytes;
             // pitch 32: a tile (128 positions) is four whole raster rows of 30 output columns and two
             // junk columns, one row per TMEM lane quarter; the halo is those rows plus one above and
             // one below (six rows of 32 positions)
-            const int P = 32, Wt = 30, HR = 6;
+            const int P = 32, Wt = 30, HR = HR_TN;
             const int h_bytes = HR * P * 128;
             int n_h = (kSmemLimit - tfixed - wres) / h_bytes;
             if (n_h > 4) n_h = 4;
@@ -1486,7 +1555,17 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
             mc = mx;
         }
     }
-    void (*k)(CUtensorMap, CUtensorMap, ClArgs);
+    // TN, 64 output channels, channels-last output, stride 1: the output's tensor map for the row stores
+    CUtensorMap my;
+    memcpy(&my, &mx, sizeof my);
+    if (g.tn && g.stage_warp >= 4096 && d.C_out == 64 && !out_nchw && !g.sub2 &&
+        (d.dims == 2 ? d.layout == X3_NHWC : d.layout == X3_NDHWC)) {
+        const uint64_t frames_y = (uint64_t)d.N * (d.dims == 3 ? d.D : 1);
+        st = encode_sw128(&my, bf16, y, 64, (uint64_t)yW, (uint64_t)yH, frames_y, 30u, 1u);
+        if (st != X3_OK) return st;
+        a.tn_tma = 1;
+    }
+    void (*k)(CUtensorMap, CUtensorMap, CUtensorMap, ClArgs);
     if (g.tn) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
                        : igemm_cl_kernel<false, false, false, false, false, false, false, false, true>;
     else if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true>
@@ -1517,7 +1596,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, k, mx, mc, a);
+    e = cudaLaunchKernelEx(&cfg, k, mx, mc, my, a);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "igemm_cl launch: %s", cudaGetErrorString(e));
     return X3_OK;
 }
