@@ -121,6 +121,19 @@ typedef struct {
                           [N][D][2H][2W][3] for X3_NDHWC and [N][3][D][2H][2W] for X3_NCDHW
                           (2D: [N][2H][2W][3] / [N][3][2H][2W]) */
     x3_kernel kernel;  /* kernel choice (X3_KERNEL_AUTO normally) */
+    /* Banded (row-band) mode, stride 1 only; all three 0 = the whole plane. The layer computes output
+       rows [band_lo, band_lo + band_rows) of an image H_global rows high (FastVideo head.cu page,
+       head_stencil_kernel and its wrapper: a band of the output plane with its own row offset and the
+       global height). The input (and each carried frame) then holds the global rows
+       [max(band_lo - 1, 0), min(band_lo + band_rows + 1, H_global)): the band's rows plus the halo
+       row above and below wherever that global row exists, so H must equal that count; zero padding
+       applies only at the global edges (rows -1 and H_global). The output holds band_rows rows.
+       A descriptor whose H misses a halo row that exists globally is rejected with X3_ERR_INVALID
+       (the page's kernel silently skips such rows instead). Bands of one plane, each with its halo,
+       give, concatenated, the whole plane's output bit for bit. Not for conv_stack_forward (each
+       layer's band needs its neighbours' rows: exchange them between layers) nor for the two-pass
+       head kernels. */
+    int band_lo, band_rows, H_global;
 } x3_conv_desc;
 
 typedef struct x3_conv_plan x3_conv_plan; /* opaque; host memory only */
@@ -245,11 +258,16 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
  * Arguments and results are those of conv_stack_forward; the caller still provides inputs,
  * outputs, carries and packed weights. The intermediate activations live in the library's own
  * X3_NOALLOC_SCRATCH_BYTES device buffer instead of a caller workspace, and this function calls
- * no allocator.
+ * no device-memory allocator (no cudaMalloc, cudaFree or allocating library routine).
  *   - Stacks whose conv_stack_workspace_bytes exceeds X3_NOALLOC_SCRATCH_BYTES are rejected with
  *     X3_ERR_OOM before anything is enqueued.
- *   - The first call on a device (with that device current) looks up the buffer's device address;
- *     make that first call before capturing any stream.
+ *   - The first call on a device (with that device current) looks up the buffer's device address,
+ *     and so does the first call after the device's context changed (a cudaDeviceReset, or another
+ *     context made current); make such a first call before capturing any stream.
+ *   - Like conv_stack_forward, the first call on a calling thread and device whose stack needs the
+ *     side stream for carry copies (3D NCDHW layers, or X3CONV_PDL=0) creates that stream and its
+ *     eight events, which reserves driver resources but no device memory of the caller's; make it
+ *     before any capture or allocation-free phase as well.
  *   - All calls on a device share the one buffer and it keeps the last call's contents (each
  *     layer overwrites every intermediate value it produces, so nothing needs clearing). Calls
  *     whose work overlaps on the GPU - on different streams, or from different threads - race on

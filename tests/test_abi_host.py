@@ -377,3 +377,70 @@ def test_stride2_channels_last_forms_planned(lib, shape, form, monkeypatch):
         assert g["smem_bytes"] <= 232448
     finally:
         x3.conv_plan_destroy(p)
+
+
+# ------------------------------------------------------------------ banded mode (validation only)
+
+def _band_desc(band_lo, band_rows, H_global, H=None, **kw):
+    lo, hi = x3.band_input_rows(band_lo, band_rows, H_global)
+    d = dict(dims=3, N=1, C_in=128, C_out=128, D=2, W=40)
+    d.update(kw)
+    return x3.make_desc(H=hi - lo if H is None else H, band_lo=band_lo, band_rows=band_rows, H_global=H_global, **d)
+
+
+@pytest.mark.parametrize("band", [(0, 5, 20), (5, 6, 20), (11, 9, 20), (0, 20, 20), (19, 1, 20)], ids=str)
+def test_band_plans(lib, band):
+    """A band of output rows [lo, lo + rows) of an H_global-row image: its input holds the band's rows and
+    the halo rows that exist globally; the plan's output height is the band's and its input starts one
+    row above the band unless the band is at the top."""
+    lo, rows, Hg = band
+    p = x3.conv_plan_create(_band_desc(lo, rows, Hg))
+    try:
+        g = x3.conv_plan_describe(p)
+        assert g["H_out"] == rows and g["row_shift"] == (1 if lo > 0 else 0)
+    finally:
+        x3.conv_plan_destroy(p)
+
+
+def test_band_validation(lib):
+    """Bands that miss a halo row which exists globally, lie outside the image, use stride 2 or the
+    two-pass head, or give band rows without H_global, are rejected before any launch."""
+    cases = [
+        dict(band_lo=5, band_rows=6, H_global=20, H=7),    # the row below is missing
+        dict(band_lo=5, band_rows=6, H_global=20, H=6),    # both halo rows missing
+        dict(band_lo=0, band_rows=6, H_global=20, H=8),    # one row too many
+        dict(band_lo=15, band_rows=6, H_global=20),        # past the bottom
+        dict(band_lo=-1, band_rows=6, H_global=20, H=7),
+        dict(band_lo=3, band_rows=0, H_global=20, H=2),
+    ]
+    for c in cases:
+        lo, rows, Hg = c["band_lo"], c["band_rows"], c["H_global"]
+        H = c.get("H", 8)
+        with pytest.raises(x3.X3Error) as e:
+            x3.conv_plan_create(_band_desc(lo, rows, Hg, H=H))
+        assert e.value.status == x3.X3_ERR_INVALID
+    with pytest.raises(x3.X3Error) as e:
+        x3.conv_plan_create(_band_desc(5, 6, 20, H=7))
+    assert "halo rows" in str(e.value)
+    with pytest.raises(x3.X3Error):
+        x3.conv_plan_create(_band_desc(4, 4, 16, dims=2, D=1, stride=2, layout="NHWC"))
+    with pytest.raises(x3.X3Error):
+        x3.conv_plan_create(_band_desc(4, 4, 16, C_in=256, C_out=12, unpatchify2x2=True, kernel="head_two_pass"))
+    with pytest.raises(x3.X3Error):
+        x3.conv_plan_create(x3.make_desc(3, 1, 8, 8, 10, 10, D=1, band_lo=2, band_rows=3))
+
+
+def test_band_plans_do_not_chain(lib):
+    """conv_stack_forward rejects banded layers: a band's output is narrower than the next band's input
+    (the halo rows come from the neighbouring bands)."""
+    a = x3.conv_plan_create(_band_desc(4, 8, 32))
+    b = x3.conv_plan_create(_band_desc(4, 8, 32))
+    try:
+        plans, k1 = x3._ptrs([a, b])
+        w, k2 = x3._ptrs([256, 256])
+        bias, k3 = x3._ptrs([32, 32])
+        st = lib.conv_stack_forward(plans, 2, 16, None, 0, w, bias, 1 << 40, 1 << 41, 1 << 30, None)
+        assert st == x3.X3_ERR_INVALID
+    finally:
+        x3.conv_plan_destroy(a)
+        x3.conv_plan_destroy(b)

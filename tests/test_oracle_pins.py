@@ -396,3 +396,44 @@ def test_head_two_pass_rounds_g_before_the_spatial_sum(oracle_mod):
     assert oracle_mod.head_two_pass(x, w, b)[0, 0, 0, 0, 0] == -0.5
     assert oracle_mod.head_two_pass(x, w, b, round_g=False)[0, 0, 0, 0, 0] == 0.5
     assert oracle_mod.conv3d_causal(x, w, b, act="clamp")[0, 0, 0, 0, 0] == 0.5
+
+
+# ------------------------------------------------------------------ banding (locality of the definition)
+
+@pytest.mark.parametrize("dims", [2, 3])
+def test_bands_with_halo_concatenate_to_the_plane(dims, oracle_mod):
+    """Output rows depend only on input rows one above and one below (pad 1, 3 taps): the oracle run on a
+    band's rows plus its halo rows (where they exist), with the rows it computes from its own zero padding
+    dropped, gives exactly the whole plane's rows; concatenated bands equal the plane bit for bit. This is
+    the banded mode's definition (FastVideo head.cu page: bands with their own row offset and the global
+    height)."""
+    oracle = oracle_mod
+    rng = np.random.default_rng(8301 + dims)
+    H, W = 17, 9
+    if dims == 2:
+        x = rng.integers(-2, 3, (2, 3, H, W)).astype(np.float32)
+        w = rng.integers(-2, 3, (4, 3, 3, 3)).astype(np.float32)
+        full = oracle.conv2d(x, w, None, act="relu")
+        ax = 2
+        run = lambda xs: oracle.conv2d(xs, w, None, act="relu")
+    else:
+        x = rng.integers(-2, 3, (1, 3, 2, H, W)).astype(np.float32)
+        c = rng.integers(-2, 3, (1, 3, 2, H, W)).astype(np.float32)
+        w = rng.integers(-2, 3, (4, 3, 3, 3, 3)).astype(np.float32)
+        full = oracle.conv3d_causal(x, w, None, carry=c, act="relu")
+        ax = 3
+        run = None
+    parts = []
+    for lo, rows in [(0, 5), (5, 7), (12, 5)]:
+        in_lo, in_hi = max(lo - 1, 0), min(lo + rows + 1, H)
+        xs = np.take(x, range(in_lo, in_hi), axis=ax)
+        if dims == 2:
+            y = run(xs)
+        else:
+            y = oracle.conv3d_causal(xs, w, None, carry=np.take(c, range(in_lo, in_hi), axis=ax), act="relu")
+        parts.append(np.take(y, range(lo - in_lo, lo - in_lo + rows), axis=ax))
+    assert np.array_equal(np.concatenate(parts, axis=ax), full)
+    # a band without its lower halo row differs (the halo is needed)
+    xs = np.take(x, range(4, 11), axis=ax)
+    y = run(xs) if dims == 2 else oracle.conv3d_causal(xs, w, None, carry=np.take(c, range(4, 11), axis=ax), act="relu")
+    assert not np.array_equal(np.take(y, range(1, 7), axis=ax), np.take(full, range(5, 11), axis=ax))

@@ -28,7 +28,7 @@ KERNEL = {"auto": 0, "igemm": 1, "direct": 2, "head_two_pass": 3, "head_split": 
 class ConvDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "dims", "N", "C_in", "C_out", "D", "H", "W", "stride", "layout", "dtype", "act", "has_bias",
-        "unpatchify2x2", "kernel")]
+        "unpatchify2x2", "kernel", "band_lo", "band_rows", "H_global")]
 
 
 class X3Error(RuntimeError):
@@ -177,12 +177,21 @@ def _torch():
 
 
 def make_desc(dims, N, C_in, C_out, H, W, D=1, stride=1, layout=None, dtype="bf16", act="none",
-              has_bias=True, unpatchify2x2=False, kernel="auto") -> ConvDesc:
+              has_bias=True, unpatchify2x2=False, kernel="auto", band_lo=0, band_rows=0, H_global=0) -> ConvDesc:
+    """A layer descriptor. band_lo / band_rows / H_global select the banded mode (output rows
+    [band_lo, band_lo + band_rows) of an H_global-row image; H = the band's rows plus its existing halo
+    rows); all 0 = the whole plane."""
     if layout is None:
         layout = "NDHWC" if dims == 3 else "NCHW"
     return ConvDesc(dims, N, C_in, C_out, D if dims == 3 else 1, H, W, stride, LAYOUT[layout],
                     DTYPE[dtype], ACT[act], int(bool(has_bias)), int(bool(unpatchify2x2)),
-                    KERNEL[kernel])
+                    KERNEL[kernel], int(band_lo), int(band_rows), int(H_global))
+
+
+def band_input_rows(band_lo, band_rows, H_global):
+    """The global input rows [lo, hi) a band of output rows needs (its rows plus the halo rows that
+    exist): the H of its descriptor is hi - lo."""
+    return max(band_lo - 1, 0), min(band_lo + band_rows + 1, H_global)
 
 
 def _stream(stream):
@@ -213,6 +222,8 @@ class Conv:
 
     @property
     def H_out(self):
+        if self.desc.H_global:
+            return self.desc.band_rows
         return (self.desc.H - 1) // self.desc.stride + 1
 
     @property

@@ -63,6 +63,25 @@ static x3_status validate(const x3_conv_desc* d) {
     if (d->unpatchify2x2 != 0 && d->unpatchify2x2 != 1) return fail(X3_ERR_INVALID, "unpatchify2x2 must be 0 or 1");
     if (d->unpatchify2x2 && d->C_out != 12) return fail(X3_ERR_INVALID, "unpatchify2x2 needs C_out == 12");
     if (d->kernel < X3_KERNEL_AUTO || d->kernel > X3_KERNEL_HEAD_STENCIL) return fail(X3_ERR_INVALID, "bad kernel choice");
+    if (d->H_global != 0) {
+        // banded mode (reading of the head.cu page's band parameters: a band must hold its halo rows
+        // wherever the global row exists)
+        if (d->stride != 1) return fail(X3_ERR_INVALID, "banded mode needs stride 1");
+        if (d->H_global < 1 || d->band_rows < 1 || d->band_lo < 0 || d->band_lo + d->band_rows > d->H_global)
+            return fail(X3_ERR_INVALID, "band [%d, %d) is not inside the %d-row image", d->band_lo,
+                        d->band_lo + d->band_rows, d->H_global);
+        const int lo = d->band_lo > 0 ? d->band_lo - 1 : 0;
+        const int hi = d->band_lo + d->band_rows + 1 < d->H_global ? d->band_lo + d->band_rows + 1 : d->H_global;
+        if (d->H != hi - lo)
+            return fail(X3_ERR_INVALID,
+                        "a band needs its halo rows wherever the global row exists: output rows [%d, %d) of %d "
+                        "read input rows [%d, %d), so H must be %d (got %d)",
+                        d->band_lo, d->band_lo + d->band_rows, d->H_global, lo, hi, hi - lo, d->H);
+        if (d->kernel == X3_KERNEL_HEAD_TWO_PASS || d->kernel == X3_KERNEL_HEAD_SPLIT)
+            return fail(X3_ERR_INVALID, "the two-pass head kernels have no banded mode");
+    } else if (d->band_lo != 0 || d->band_rows != 0) {
+        return fail(X3_ERR_INVALID, "band_lo and band_rows need H_global (0 = the whole plane)");
+    }
     // Every tensor must be indexable with 63-bit offsets and every per-image plane with 31 bits.
     const long long frames = (long long)d->N * (d->dims == 3 ? d->D + 2 : 1);
     const long long plane = (long long)d->H * d->W;
@@ -103,7 +122,8 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan) {
     if (!p) return fail(X3_ERR_OOM, "out of host memory");
     p->d = *desc;
     if (p->d.dims == 2) p->d.D = 1;
-    p->H_out = (p->d.H - 1) / p->d.stride + 1;
+    p->H_out = p->d.H_global ? p->d.band_rows : (p->d.H - 1) / p->d.stride + 1;
+    p->row_shift = (p->d.H_global && p->d.band_lo > 0) ? 1 : 0;
     p->W_out = (p->d.W - 1) / p->d.stride + 1;
     p->num_sms = device_sms();
     bool igemm_ok = false;
@@ -237,10 +257,11 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, \"frames\": %d, "
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, "
-                        "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d, \"tn\": %d}",
+                        "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d, \"tn\": %d, "
+                        "\"row_shift\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn, c.tn);
+                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn, c.tn, plan->row_shift);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",

@@ -17,6 +17,7 @@ namespace x3 {
 
 struct DirectArgs {
     int dims, N, C_in, C_out, D, H, W, H_out, W_out, stride, act, unpatch, channels_last, has_carry;
+    int row_shift;  // banded mode: the input's first row is the band's upper halo row
 };
 
 __device__ __forceinline__ float ld_val(const __half* p, size_t i) { return __half2float(p[i]); }
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(256) direct_conv_kernel(const T* __restrict__ 
                     src = x; F = 1; f = 0;
                 }
                 for (int kh = 0; kh < 3; ++kh) {
-                    const int ih = a.stride * oh + kh - 1;
+                    const int ih = a.stride * oh + kh - 1 + a.row_shift;
                     if (ih < 0 || ih >= a.H) continue;
                     for (int kw = 0; kw < 3; ++kw) {
                         const int iw = a.stride * ow + kw - 1;
@@ -110,6 +111,7 @@ x3_status launch_direct(const x3_conv_plan* p, const void* x, const void* carry,
     a.H_out = p->H_out; a.W_out = p->W_out; a.stride = d.stride; a.act = d.act; a.unpatch = d.unpatchify2x2;
     a.channels_last = (d.layout == X3_NHWC || d.layout == X3_NDHWC);
     a.has_carry = carry != nullptr;
+    a.row_shift = p->row_shift;
     const size_t total = out_elems(p);
     const int threads = 256;
     size_t blocks = (total + threads - 1) / threads;

@@ -55,6 +55,7 @@ struct IgemmArgs {
     int BN, n_tiles, CK, n_chunks, KT, NSUB, Rt, Wt, P, spr, halo_rows, plane_stride, a_bytes, a_tx_bytes;
     int raw_w, raw_bytes, raw_tx_bytes, b_bytes, n_a, n_b, n_raw, acc_bufs, tmem_cols;
     int stride, raw_rows, phase_stride;  // NCHW: input stride, raw tile rows, bytes between phase planes
+    int row_shift;  // banded mode: the input's first row is the band's upper halo row
     int col_tiles, row_tiles, frames;
     int scr_pitch;  // epilogue scratch row pitch in bytes (0 = direct stores)
     long long tiles;
@@ -286,14 +287,14 @@ __global__ void __launch_bounds__(MODE == STAGE_NCHW ? 320 : 192, 1)
                             }
                             for (int j = 0; j < kpl; ++j)
                                 ptx::tma_load_4d(sA + st * a.a_bytes + j * a.plane_stride, map, bar_a_full + 8 * st,
-                                                 cc * a.CK + 8 * j, tc.ow0 - 1, tc.oh0 - 1, fcoord);
+                                                 cc * a.CK + 8 * j, tc.ow0 - 1, tc.oh0 - 1 + a.row_shift, fcoord);
                             ++a_cnt;
                         } else {
                             const uint32_t st = r_cnt % a.n_raw;
                             if (!wait_bar(bar_r_empty + 8 * st, ((r_cnt / a.n_raw) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(bar_r_full + 8 * st, (uint32_t)a.raw_tx_bytes);
                             ptx::tma_load_4d(sRaw + st * a.raw_bytes, &tm_x, bar_r_full + 8 * st,
-                                             a.stride * tc.ow0 - 8, a.stride * tc.oh0 - 1, cc * a.CK, n);
+                                             a.stride * tc.ow0 - 8, a.stride * tc.oh0 - 1 + a.row_shift, cc * a.CK, n);
                             ++r_cnt;
                         }
                         const uint8_t* wblk = a.w + ((((size_t)tc.nt * a.KT + kt) * a.n_chunks + cc) * 9) * a.b_bytes;
@@ -771,6 +772,7 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
     a.a_bytes = g.a_bytes; a.a_tx_bytes = g.a_tx_bytes; a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes;
     a.raw_tx_bytes = g.CK * g.raw_rows * g.raw_w * 2; a.b_bytes = g.b_bytes; a.n_a = g.n_a; a.n_b = g.n_b;
     a.stride = g.stride; a.raw_rows = g.raw_rows; a.phase_stride = g.phase_stride;
+    a.row_shift = p->row_shift;
     a.n_raw = g.n_raw; a.acc_bufs = g.acc_bufs; a.tmem_cols = g.tmem_cols;
     a.col_tiles = g.col_tiles; a.row_tiles = g.row_tiles; a.frames = g.frames; a.tiles = g.tiles;
     a.scr_pitch = g.scr_pitch;

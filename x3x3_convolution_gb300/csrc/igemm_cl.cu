@@ -106,6 +106,7 @@ struct ClArgs {
     int tn_cp, tn_n; // TN: output channels padded to 16, MMA N (3 horizontal taps x tn_cp)
     int x_bytes;     // TN: bytes after the staging blocks (the epilogue warps' bias copies)
     int tn_tma;      // TN: each warp writes its raster row (64 channels) with one TMA store (tm_y)
+    int row_shift;   // banded mode: the input's first row is the band's upper halo row
     long long tiles;
     FastDiv fd_frames, fd_ntiles, fd_windows, fd_strips, fd_dout, fd_P, fd_chunks;
     uint32_t idesc;
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 const uint32_t sr = r_cnt % a.n_raw;
                                 if (!cl_wait(bar_r_empty + 8 * sr, ((r_cnt / a.n_raw) & 1u) ^ 1u, abort_flag, a.status)) { ok = false; break; }
                                 ptx::mbar_arrive_expect_tx(bar_r_full + 8 * sr, (uint32_t)a.raw_tx_bytes);
-                                ptx::tma_load_4d(sRaw + sr * a.raw_bytes, &tm_x, bar_r_full + 8 * sr, ow0 - 8, r0 - 1,
+                                ptx::tma_load_4d(sRaw + sr * a.raw_bytes, &tm_x, bar_r_full + 8 * sr, ow0 - 8, r0 - 1 + a.row_shift,
                                                  cc * kCK + 16 * sc, n);
                                 ++r_cnt;
                             }
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 // and one barrier for both
                                 if (STN)
                                     ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1,
-                                                     tc.win * (a.HR - 2) - 1, fcoord);
+                                                     tc.win * (a.HR - 2) - 1 + a.row_shift, fcoord);
                                 else
                                     ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
                                 ptx::bulk_load(sH + sh * a.h_bytes + (uint32_t)kCtrW,
@@ -423,7 +424,8 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK,
                                                  2 * (ow0 - 1) + (kt & 1), 2 * (r0 - 1) + (kt >> 1), fcoord);
                             else
-                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1, r0 - 1, fcoord);
+                                ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1,
+                                                 r0 - 1 + a.row_shift, fcoord);
                             ++h_cnt;
                             hr.next(a.n_h);
                         }
@@ -1505,7 +1507,7 @@ namespace {
 
 // One launch of the engine for descriptor d (its layout, C_in and stride as the kernel sees them)
 // with tiling g over an H_out x W_out raster; the stored plane is yH x yW.
-x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out, int yH, int yW, int out_nchw,
+x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out, int yH, int yW, int out_nchw, int row_shift,
                     const void* x, const void* carry, const void* w_packed, const void* bias, void* y, cudaStream_t s) {
     const bool bf16 = d.dtype == X3_BF16;
     ClArgs a;
@@ -1515,6 +1517,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.sub2 = g.sub2; a.out_nchw = out_nchw; a.yH = yH; a.yW = yW; a.w_smem = g.w_smem;
     a.stage_warp = g.stage_warp;
     a.tn_cp = g.tn_cp; a.tn_n = g.tn_n; a.x_bytes = g.x_bytes;
+    a.row_shift = row_shift;
     a.frame_inner = g.ctr;
     a.g_f32 = d.kernel == X3_KERNEL_HEAD_SPLIT ? 1 : 0;
     a.has_carry = carry != nullptr;
@@ -1607,7 +1610,7 @@ x3_status launch_igemm_cl(const x3_conv_plan* p, const void* x, const void* carr
                           const void* bias, void* y, cudaStream_t s) {
     // stride 2 as sub2: the raster covers the input plane, the stored plane is the output
     const int rh = p->cl.sub2 ? p->d.H : p->H_out, rw = p->cl.sub2 ? p->d.W : p->W_out;
-    return launch_cl(p->d, p->cl, rh, rw, p->H_out, p->W_out, 0, x, carry, w_packed, bias, y, s);
+    return launch_cl(p->d, p->cl, rh, rw, p->H_out, p->W_out, 0, p->row_shift, x, carry, w_packed, bias, y, s);
 }
 
 x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const void* w_packed, const void* bias,
@@ -1618,7 +1621,7 @@ x3_status launch_igemm_cl_shadow(const x3_conv_plan* p, const void* x, const voi
     d.C_in = (d.C_in + 7) / 8 * 8;
     // S2: the raster is the output plane; sub2: the stride-1 raster over the input plane
     const int rh = p->cl_shadow.s2 ? p->H_out : d.H, rw = p->cl_shadow.s2 ? p->W_out : d.W;
-    return launch_cl(d, p->cl_shadow, rh, rw, p->H_out, p->W_out, out_nchw, x, nullptr,
+    return launch_cl(d, p->cl_shadow, rh, rw, p->H_out, p->W_out, out_nchw, 0, x, nullptr,
                      (const uint8_t*)w_packed + p->shadow_w_off, bias, y, s);
 }
 

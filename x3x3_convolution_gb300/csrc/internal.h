@@ -93,6 +93,9 @@ struct x3_conv_plan {
     x3::ClGeom cl;
     size_t packed_bytes;
     int num_sms;
+    // Banded mode: 1 when the input's first row is the halo row above the band (band_lo > 0), so
+    // output row r reads input rows r + kh (instead of r + kh - 1, whose -1 is the zero padding)
+    int row_shift;
     // Channels-last form of a 2D NCHW layer, used by the stack driver for the layers between the
     // first input and the last output: input NHWC with C_in rounded up to 8, stride 1 (stride 2 as
     // sub2). Its packed weights start at shadow_w_off bytes into the layer's packed buffer.

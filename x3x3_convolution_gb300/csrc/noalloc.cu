@@ -8,6 +8,7 @@
 //
 // The scratch is one file-scope device array of X3_NOALLOC_SCRATCH_BYTES. Every GPU that loads the
 // library holds it until the process exits, and every call on a device shares it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,21 +22,45 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[X3_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_ptr[kMaxDevices];
+static void* g_noalloc_ctx[kMaxDevices];  // the context the address was resolved in
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current context (NULL if the driver entry point is unavailable).
+static void* current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        fn = (CtxGetCurrentFn)f;
+    }
+    CUcontext c = nullptr;
+    return fn(&c) == CUDA_SUCCESS ? (void*)c : nullptr;
+}
 
 // Device address of the scratch array on the current device. The array's name is only a host-side
-// stand-in in host code, so its address is looked up once per device, with that device current.
+// stand-in in host code, so its address is looked up with that device current: once per device and
+// context (again after a cudaDeviceReset or under another context, whose module instance is a
+// different allocation).
 static x3_status noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(X3_ERR_CUDA, "conv_stack_forward_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(X3_ERR_UNSUPPORTED, "conv_stack_forward_noalloc: device %d out of range", dev);
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || !ctx || g_noalloc_ctx[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return fail(X3_ERR_CUDA, "conv_stack_forward_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = current_context();  // the runtime has made the device's context current by now
     }
     *out = g_noalloc_ptr[dev];
     return X3_OK;
