@@ -153,12 +153,19 @@ def _check_tn_plan(g, C_in, C_out):
     weights; two TMEM buffers of N columns at a 256-column stride."""
     P, HR, Wt = g["P"], g["HR"], g["Wt"]
     assert g["tn"] == 1 and g["m64"] == 0 and g["win_adv"] == 128
-    assert (P, Wt, HR) == (32, 30, 6)
+    assert g["tk"] == (C_in == 8)
+    assert (P, Wt, HR) == (32, 30, 7 if g["tk"] else 6)
     for win in range(min(g["windows"], 4 * P)):
         pos_off = (128 * win) % P
         assert pos_off == 0
-        need = pos_off + 127 + 2 * P + 1
-        assert need <= HR * P and need * 128 <= g["h_bytes"]
+        if g["tk"]:
+            # taps in K: the ninth tap's rows (offset 2P + 2) and its zero partner one position on,
+            # 16 bytes per position
+            need = pos_off + 127 + 2 * P + 2 + 1 + 1
+            assert need <= HR * P and need * 16 <= g["h_bytes"]
+        else:
+            need = pos_off + 127 + 2 * P + 1
+            assert need <= HR * P and need * 128 <= g["h_bytes"]
     cp = (C_out + 15) // 16 * 16
     assert 3 * cp <= 256 and g["h_bytes"] % 1024 == 0 and g["smem_bytes"] <= 232448
     assert 2 <= g["n_h"] <= 4
@@ -309,7 +316,8 @@ def test_nchw_layers_have_channels_last_forms(lib, name):
         elif cfg["C_out"] <= 80:
             # stride 1 with at most 80 output channels: positions as M, horizontal taps in N
             Ho, Wo = cfg["H"], cfg["W"]
-            assert s["tn"] == 1 and s["m64"] == 0 and (P, Wt, HR) == (32, 30, 6)
+            assert s["tn"] == 1 and s["m64"] == 0 and (P, Wt, HR) == (32, 30, 7 if s["tk"] else 6)
+            assert s["tk"] == ((cfg["C_in"] + 7) // 8 * 8 == 8)
             for win in range(min(s["windows"], 4 * P)):
                 assert (128 * win) % P + 127 + 2 * P + 1 <= HR * P
         else:
@@ -324,7 +332,7 @@ def test_nchw_layers_have_channels_last_forms(lib, name):
         assert s["smem_bytes"] <= 232448 and s["w_off"] % 256 == 0
         assert s["m64"] == (cfg["C_out"] <= 64 and not s["tn"])
         cp = (cfg["C_out"] + 15) // 16 * 16
-        shadow_bytes = (s["n_chunks"] * 3 * 3 * cp * 128 if s["tn"] else
+        shadow_bytes = (5 * cp * 32 if s.get("tk") else s["n_chunks"] * 3 * 3 * cp * 128 if s["tn"] else
                         s["n_tiles"] * s["n_chunks"] * 9 * (64 if s["m64"] else 128) * 64 * 2)
         assert x3.conv_packed_weight_bytes(p) == s["w_off"] + shadow_bytes or \
             (s["w_off"] == 0 and x3.conv_packed_weight_bytes(p) == shadow_bytes)

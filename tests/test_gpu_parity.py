@@ -87,7 +87,9 @@ NHWC_CASES = [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"), (
               (1, 64, 80, 19, 301, 1, "relu"), (2, 24, 24, 11, 40, 1, "none"), (1, 64, 8, 5, 260, 1, "relu"),
               (1, 136, 32, 7, 45, 1, "none"), (3, 16, 16, 6, 1, 1, "relu"),
               # 64 channels: each raster row leaves by one TMA store, clipped at a ragged right edge
-              (2, 32, 64, 7, 61, 1, "relu")]
+              (2, 32, 64, 7, 61, 1, "relu"),
+              # 8 input channels: two taps per K step (five MMAs), 64 and 24 output channels
+              (4, 8, 64, 37, 95, 1, "relu"), (1, 8, 24, 9, 31, 1, "none")]
 
 
 @pytest.mark.parametrize("variant", ["int", "random"])
@@ -109,7 +111,7 @@ def test_conv2d_nhwc(case, variant, dtype, form, monkeypatch):
     g = x3.conv_plan_describe(conv.plan)
     assert g["kernel"] == "igemm_tcgen05_sw128" and g["s2"] == (s == 2)
     if form == "auto" and s == 1 and Co <= 80 and not (Ci > 128 and Co > 32):
-        assert g["tn"] == 1
+        assert g["tn"] == 1 and g["tk"] == (Ci == 8)
     elif form == "m64":
         assert g["tn"] == 0 and g["m64"] == (Co <= 64 and Ci <= 64)
     ref = oracle2d(x, L, layout="NHWC")

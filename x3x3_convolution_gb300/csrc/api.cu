@@ -258,10 +258,10 @@ static int describe_main(const x3_conv_plan* plan, char* buf, size_t len) {
                         "\"h_bytes\": %d, \"n_h\": %d, \"n_w\": %d, \"kwm\": %d, \"nchw\": %d, \"win_adv\": %d, \"tiles\": %lld, "
                         "\"smem_bytes\": %d, \"grid\": %d, \"H_out\": %d, \"W_out\": %d, \"sms\": %d, "
                         "\"m64\": %d, \"sub2\": %d, \"s2\": %d, \"ctr\": %d, \"w2\": %d, \"stn\": %d, \"tn\": %d, "
-                        "\"row_shift\": %d}",
+                        "\"tk\": %d, \"row_shift\": %d}",
                         c.n_tiles, c.n_chunks, c.KT, c.Wt, c.P, c.HR, c.strips, c.windows, c.frames, c.h_bytes, c.n_h,
                         c.n_w, c.kwm, c.nchw, c.win_adv, c.tiles, c.smem_bytes, c.grid, plan->H_out, plan->W_out, plan->num_sms,
-                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn, c.tn, plan->row_shift);
+                        c.m64, c.sub2, c.s2, c.ctr, c.w2, c.stn, c.tn, c.tk, plan->row_shift);
     }
     if (plan->kind != K_IGEMM)
         return snprintf(buf, len, "{\"kernel\": \"direct_simt\", \"H_out\": %d, \"W_out\": %d, \"sms\": %d}",
@@ -288,9 +288,9 @@ int conv_plan_describe(const x3_conv_plan* plan, char* buf, size_t len) {
         const int m = snprintf(tmp + n - 1, sizeof tmp - (size_t)(n - 1),
                                ", \"shadow\": {\"Wt\": %d, \"P\": %d, \"HR\": %d, \"strips\": %d, \"windows\": %d, "
                                "\"n_chunks\": %d, \"n_tiles\": %d, \"n_w\": %d, \"n_h\": %d, \"sub2\": %d, \"s2\": %d, \"tiles\": %lld, "
-                               "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d, \"tn\": %d}}",
+                               "\"smem_bytes\": %d, \"grid\": %d, \"w_off\": %zu, \"m64\": %d, \"tn\": %d, \"tk\": %d}}",
                                c.Wt, c.P, c.HR, c.strips, c.windows, c.n_chunks, c.n_tiles, c.n_w, c.n_h, c.sub2, c.s2, c.tiles,
-                               c.smem_bytes, c.grid, plan->shadow_w_off, c.m64, c.tn);
+                               c.smem_bytes, c.grid, plan->shadow_w_off, c.m64, c.tn, c.tk);
         n = n - 1 + m;
     }
     return snprintf(buf, len, "%s", tmp);

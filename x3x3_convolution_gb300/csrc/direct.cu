@@ -182,8 +182,32 @@ __global__ void __launch_bounds__(256) pack_tn_kernel(const uint16_t* __restrict
     }
 }
 
+// Packed layout of the TK form (8 input channels, two taps per K step): five blocks (K steps), each the
+// K-major canonical B tile [2 halves][cp rows][8 channels], half h of block s carrying tap 2s + h (zero for
+// the tenth tap, for co >= C_out and for channels >= C_in).
+__global__ void __launch_bounds__(256) pack_tk_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                      int C_in, int C_out, int cp, size_t total) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        size_t r = i;
+        const int ci = (int)(r % 8); r /= 8;
+        const int co = (int)(r % cp); r /= cp;
+        const int h = (int)(r % 2); r /= 2;
+        const int tap = 2 * (int)r + h;
+        uint16_t v = 0;
+        if (tap < 9 && co < C_out && ci < C_in) v = w[((size_t)co * C_in + ci) * 9 + tap];
+        out[i] = v;
+    }
+}
+
 static x3_status launch_pack_tn(const x3_conv_plan* p, const ClGeom& g, const void* w, void* out, cudaStream_t s) {
     const size_t total = cl_packed_bytes(g) / 2;
+    if (g.tk) {
+        pack_tk_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>((const uint16_t*)w, (uint16_t*)out, p->d.C_in,
+                                                                       p->d.C_out, g.tn_cp, total);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(X3_ERR_CUDA, "pack kernel launch: %s", cudaGetErrorString(e));
+        return X3_OK;
+    }
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     pack_tn_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)w, (uint16_t*)out, p->d.C_in, p->d.C_out, g.KT,

@@ -261,8 +261,14 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // would reach into the next row are the junk columns. Every MMA row is an output position (or one of
 // the two junk columns), where the M = 64 form leaves half of the tensor core's rows empty; three MMAs
 // per 16 input channels instead of nine.
+// TK (with TN; 2D channels-last layers with 8 input channels, the first layer of an NCHW stack): the
+// taps go into K instead, two per 16-wide K step. The halo is staged unswizzled with 16 bytes (8
+// channels) per position, and the A descriptor of K step s starts at tap 2s's rows with its
+// leading-dimension byte offset (the K-half stride) set to the distance to tap 2s+1's rows, so one MMA
+// reads both taps' channels for 128 positions; five MMAs (the ninth tap paired with zero weights) of
+// N = C_out leave out[j] directly in TMEM, and the epilogue needs no shifts.
 template <bool BF16, bool KWM, bool NC, bool CTR = false, bool M64 = false, bool W2 = false,
-          bool STN = false, bool S2 = false, bool TN = false>
+          bool STN = false, bool S2 = false, bool TN = false, bool TK = false>
 __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     igemm_cl_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                     const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ ClArgs a) {
@@ -356,8 +362,8 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             RingPos hr, wr;  // halo and weight ring positions of h_cnt and w_cnt
             bool ok = true;
             if (M64 || TN) {  // every weight block of the layer, once, on the first weight barrier
-                const int nblk = a.KT * a.n_chunks * (TN ? 3 : 9);
-                const uint32_t bb = TN ? (uint32_t)a.tn_n * 128u : (uint32_t)kWBlock64;
+                const int nblk = TK ? 5 : a.KT * a.n_chunks * (TN ? 3 : 9);
+                const uint32_t bb = TK ? (uint32_t)a.tn_n * 32u : (TN ? (uint32_t)a.tn_n * 128u : (uint32_t)kWBlock64);
                 ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)nblk * bb);
                 for (int b = 0; b < nblk; ++b)
                     ptx::bulk_load(sW + (uint32_t)b * bb, a.w + (size_t)b * bb, bb, bar_w_full);
@@ -534,6 +540,28 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                         }
                         ptx::tc_fence_after();
                         const uint32_t hbase = sH + sh * (uint32_t)a.h_bytes;
+                        if constexpr (TK) {
+                            // K step s: taps 2s and 2s+1 (tap t = kh * 3 + kw at halo offset kh P + kw,
+                            // 16 bytes per position); no swizzle, SBO = 128 B (8 positions), LBO = the
+                            // second tap's offset; the ninth tap pairs with zero weights
+                            const uint32_t tk_hi = (128u >> 4) | (1u << 14);
+#pragma unroll
+                            for (int ks = 0; ks < 5; ++ks) {
+                                const int t0 = 2 * ks, t1 = 2 * ks + 1;
+                                const int o0 = (t0 / 3) * a.P + t0 % 3;
+                                const int o1 = t1 < 9 ? (t1 / 3) * a.P + t1 % 3 : o0 + 1;
+                                const uint32_t lo = (((hbase + (uint32_t)o0 * 16u) >> 4) & 0x3FFFu) |
+                                                    ((uint32_t)(o1 - o0) << 16);   // (o1 - o0) x 16 B / 16
+                                const uint64_t adesc = ((uint64_t)tk_hi << 32) | (uint64_t)lo;
+                                const uint64_t bdesc = tn_wdesc0 + (uint64_t)((uint32_t)ks * tn_kstep);
+                                ptx::mma_f16(d, adesc, bdesc, a.idesc, ks > 0 ? 1u : 0u);
+                            }
+                            acc = 1;
+                            ptx::mma_commit(bar_h_empty + 8 * sh);
+                            ++h_cnt;
+                            hr.next(a.n_h);
+                            continue;
+                        }
                         const uint64_t a0 = ((uint64_t)b_hi_fixed << 32) | (uint64_t)(((hbase >> 4) & 0x3FFFu) | (1u << 16));
                         const uint64_t w0 = tn_wdesc0 + (uint64_t)((uint32_t)((kt * a.n_chunks + cc) * 3) * tn_wstep);
                         const int rem = a.C_in - cc * kCK;
@@ -780,16 +808,22 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                 ptx::tc_fence_after();
                 auto load = [&](int c, uint32_t (&v0)[16], uint32_t (&v1)[16], uint32_t (&v2)[16]) {
                     ptx::tmem_ld16(tq + (uint32_t)(16 * c), v0);
-                    ptx::tmem_ld16(tq + (uint32_t)(cp + 16 * c), v1);
-                    ptx::tmem_ld16(tq + (uint32_t)(2 * cp + 16 * c), v2);
+                    if (!TK) {
+                        ptx::tmem_ld16(tq + (uint32_t)(cp + 16 * c), v1);
+                        ptx::tmem_ld16(tq + (uint32_t)(2 * cp + 16 * c), v2);
+                    }
                 };
                 auto sum = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16], const uint32_t (&v2)[16]) {
                     float o[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
-                        const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
-                        o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
+                        if (TK) {
+                            o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + sb[16 * c + k], act_lo), act_hi);
+                        } else {
+                            const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
+                            const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
+                            o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
+                        }
                     }
                     if (tma) {
                         uint4 w0, w1;
@@ -1197,8 +1231,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 // es = 2: every second position along W and H (the box spans 2 box_w x 2 box_h positions of the
 // tensor and lands box_w x box_h rows in shared memory); box_w and box_h are the landed counts.
+// inner8: a box of 8 channels (16 bytes per position), no swizzle (the TK form's halo).
 x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, uint64_t W, uint64_t H,
-                       uint64_t F, uint32_t box_w, uint32_t box_h, uint32_t es_wh = 1) {
+                       uint64_t F, uint32_t box_w, uint32_t box_h, uint32_t es_wh = 1, bool inner8 = false) {
     static EncodeTiledFn fn = nullptr;
     if (!fn) {
         void* f = nullptr;
@@ -1213,10 +1248,11 @@ x3_status encode_sw128(CUtensorMap* m, bool bf16, const void* ptr, uint64_t C, u
     }
     cuuint64_t gd[4] = {C, W, H, F};
     cuuint64_t gs[3] = {C * 2, C * 2 * W, C * 2 * W * H};
-    cuuint32_t bd[4] = {(cuuint32_t)kCK, box_w * es_wh, box_h * es_wh, 1};
+    cuuint32_t bd[4] = {inner8 ? 8u : (cuuint32_t)kCK, box_w * es_wh, box_h * es_wh, 1};
     cuuint32_t es[4] = {1, es_wh, es_wh, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-                    const_cast<void*>(ptr), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    const_cast<void*>(ptr), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    inner8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(X3_ERR_CUDA, "cuTensorMapEncodeTiled (128-byte swizzle) failed (%d)", (int)r);
     return X3_OK;
@@ -1260,6 +1296,7 @@ bool pdl_enabled() {
 }
 
 size_t cl_packed_bytes(const ClGeom& g) {
+    if (g.tk) return (size_t)5 * g.tn_n * 32;
     if (g.tn) return (size_t)g.KT * g.n_chunks * 3 * g.tn_n * 128;
     return (size_t)g.n_tiles * g.KT * g.n_chunks * (g.kwm ? 3 : 9) * ((g.m64 ? 64 : kBM) * kCK * 2);
 }
@@ -1332,27 +1369,31 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         const int cp = (d.C_out + 15) / 16 * 16;
         if (small_cout && d.dims == 2 && !g.s2 && !g.nchw && !g.kwm && !g.ctr && d.C_out <= 80 &&
             !(tn_env && !strcmp(tn_env, "0"))) {
-            const int tn_n = 3 * cp;
+            // eight input channels: the taps in K (TK), N = the output channels
+            const bool tk = d.C_in == 8 && !(getenv("X3CONV_TK") && !strcmp(getenv("X3CONV_TK"), "0"));
+            const int tn_n = tk ? cp : 3 * cp;
             // eight epilogue warps, each holding a copy of the bias; with 64 channels each also stages its
             // raster row (32 positions x 128 B, 1024-aligned) for a TMA store, other widths store straight
             // from registers
             const int x_bytes = 32 * cp;
-            const int wres = g.KT * g.n_chunks * 3 * tn_n * 128;
+            const int wres = tk ? 5 * tn_n * 32 : g.KT * g.n_chunks * 3 * tn_n * 128;
             int stage_warp = cp == 64 ? 4096 : 0;
-            if (stage_warp && 1024 + 8 * stage_warp + 512 + x_bytes + wres + 2 * HR_TN * 32 * 128 > kSmemLimit)
+            if (stage_warp && 1024 + 8 * stage_warp + 512 + x_bytes + wres + 2 * (HR_TN + 1) * 32 * 128 > kSmemLimit)
                 stage_warp = 0;  // no room for the row buffers next to two halo stages: direct stores
             const int tfixed = 1024 + 8 * stage_warp + 512 + x_bytes;
             // pitch 32: a tile (128 positions) is four whole raster rows of 30 output columns and two
             // junk columns, one row per TMEM lane quarter; the halo is those rows plus one above and
             // one below (six rows of 32 positions)
-            const int P = 32, Wt = 30, HR = HR_TN;
-            const int h_bytes = HR * P * 128;
+            // TK: 16 bytes per position, and one more row: the pairs' second taps read up to two
+            // positions past the 192 (junk outputs only)
+            const int P = 32, Wt = 30, HR = tk ? HR_TN + 1 : HR_TN;
+            const int h_bytes = tk ? (HR * P * 16 + 1023) / 1024 * 1024 : HR * P * 128;
             int n_h = (kSmemLimit - tfixed - wres) / h_bytes;
             if (n_h > 4) n_h = 4;
             long long best = -1;
             if (n_h >= 2) {
                 best = 0;
-                g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = kCK * 2 * P * HR;
+                g.Wt = Wt; g.P = P; g.HR = HR; g.h_bytes = h_bytes; g.h_tx_bytes = (tk ? 8 : kCK) * 2 * P * HR;
                 g.n_h = n_h; g.n_w = 1; g.strips = (W_out + Wt - 1) / Wt; g.windows = (H_out + 3) / 4;
                 g.tiles = (long long)g.strips * g.windows * g.frames;
                 g.w_smem = wres; g.n_raw = 0; g.raw_w = g.raw_bytes = g.raw_tx_bytes = 0;
@@ -1360,7 +1401,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
                 g.smem_bytes = tfixed + n_h * h_bytes + wres;
             }
             if (best >= 0) {
-                g.tn = 1; g.tn_cp = cp; g.tn_n = tn_n; g.m64 = 0; g.n_tiles = 1; g.win_adv = 128;
+                g.tn = 1; g.tk = tk ? 1 : 0; g.tn_cp = cp; g.tn_n = tn_n; g.m64 = 0; g.n_tiles = 1; g.win_adv = 128;
                 found = true;
             }
         }
@@ -1549,10 +1590,10 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         const bool flat = g.ctr && !g.stn;
         const uint64_t mw = flat ? (uint64_t)d.H * d.W : (uint64_t)d.W, mh = flat ? 1 : (uint64_t)d.H;
         const uint32_t bw = flat ? (uint32_t)kBNP : (uint32_t)g.P, bh = flat ? 1u : (uint32_t)g.HR;
-        st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh, g.s2 ? 2u : 1u);
+        st = encode_sw128(&mx, bf16, x, d.C_in, mw, mh, frames_x, bw, bh, g.s2 ? 2u : 1u, g.tk != 0);
         if (st != X3_OK) return st;
         if (carry) {
-            st = encode_sw128(&mc, bf16, carry, d.C_in, mw, mh, (uint64_t)d.N * 2, bw, bh);
+            st = encode_sw128(&mc, bf16, carry, d.C_in, mw, mh, (uint64_t)d.N * 2, bw, bh, 1u, g.tk != 0);
             if (st != X3_OK) return st;
         } else {
             mc = mx;
@@ -1569,7 +1610,9 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         a.tn_tma = 1;
     }
     void (*k)(CUtensorMap, CUtensorMap, CUtensorMap, ClArgs);
-    if (g.tn) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
+    if (g.tk) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true, true>
+                       : igemm_cl_kernel<false, false, false, false, false, false, false, false, true, true>;
+    else if (g.tn) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, false, false, false, true>
                        : igemm_cl_kernel<false, false, false, false, false, false, false, false, true>;
     else if (g.w2) k = bf16 ? igemm_cl_kernel<true, false, false, false, false, true>
                        : igemm_cl_kernel<false, false, false, false, false, true>;

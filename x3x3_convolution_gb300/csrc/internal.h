@@ -77,7 +77,8 @@ struct ClGeom {
     int stn;                     // 1: head with the spatial stencil in the epilogue (centre-tap MMAs)
     int stage_warp;              // epilogue staging bytes per warp
     int tn;                      // 1: positions as M (128 per tile), the three horizontal taps in N
-    int tn_cp, tn_n;             // tn: output channels padded to 16; MMA N = 3 * tn_cp
+    int tn_cp, tn_n;             // tn: output channels padded to 16; MMA N = 3 * tn_cp (tk: tn_cp)
+    int tk;                      // 1 (with tn): 8 input channels, two taps per 16-wide K step
     int x_bytes;                 // tn: shared memory for the kw-sum exchange and the bias copies
     long long tiles;
     int smem_bytes, grid;
