@@ -44,10 +44,12 @@ WORKLOAD = ("decoder pass: TAESD-like 2D chain (N=4, 3x256x256, 7 convs, NCHW f1
 FRAMES = 4
 STAGES = ["taesd", "stack", "l3", "head"]
 AB_STAGES = ["head_fused", "head_two_pass", "head_split"]
+SINGLE_STAGES = ["conv16", "conv256"]
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of each kernel at the benchmark's size,
-# from one ncu capture of that launch of the current code (each kernel's summary under profiles/);
-# None where there is no such capture
-DRAM_BYTES = {"conv16": None, "taesd": None, "conv256": None, "stack_128": None, "l3": None, "head": None}
+# from one ncu capture of that launch of the current code (each kernel's summary under profiles/; the
+# TAESD entry is its stage's eight launches; the 256->256 layer's was taken back to back, L2-warm)
+DRAM_BYTES = {"conv16": 337408.0, "taesd": 157760512.0, "conv256": 46845440.0, "stack_128": 875257600.0,
+              "l3": 264802048.0, "head": 695635968.0}
 
 
 def layer_descs():
@@ -526,6 +528,37 @@ def run_reference(args, rank):
 def run_stage(wl, args, stream, fl, nb):
     """Warm up, then time `steps` runs of one stage alone (CUDA events); one JSON line."""
     import torch
+    if args.stage in SINGLE_STAGES:
+        import x3x3_convolution_gb300 as x3
+        from x3x3_convolution_gb300 import synth
+        dd = layer_descs()[args.stage]
+        if args.stage == "conv16":
+            x, L = synth.conv2d_single(seed=1001)
+            carry = None
+            flop, nbytes = flop2d(1, 16, 16, 64, 64), 2.0 * (16 * 64 * 64 * 2 + 16 * 16 * 9 + 16)
+        else:
+            x, c, L = synth.conv3d_single(seed=1003)
+            carry = c.torch(stream.device)
+            flop = flop3d(256, 256, 4, 88, 156)
+            nbytes = 2.0 * (6 * 88 * 156 * 256 + 4 * 88 * 156 * 256 + 256 * 256 * 27 + 256)
+        conv = x3.Conv(x3.make_desc(**dd), L.w.torch(stream.device), L.b.torch(stream.device))
+        xd = x.torch(stream.device)
+        out = torch.empty(conv.out_shape(), dtype=xd.dtype, device=xd.device)
+        run = lambda: conv(xd, carry, out=out, stream=stream)
+        for _ in range(args.warmup):
+            run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        print(json.dumps({"stage": args.stage, "ms": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+                          "gbs": nbytes / (ms * 1e-3) / 1e9, "note": "back to back (L2-warm)",
+                          "plan": x3.conv_plan_describe(conv.plan)}), flush=True)
+        return
     fn = {"taesd": lambda: wl.taesd(wl.taesd_x, out=wl.taesd_y, stream=stream),
           "stack": lambda: wl.stack(wl.stack_x, carries=wl.stack_carries, carry_valid=True, out=wl.stack_y,
                                     stream=stream),
@@ -584,7 +617,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-memory", action="store_true", help="skip the pass-decoder peak-memory curve")
-    ap.add_argument("--stage", choices=STAGES + AB_STAGES, default=None,
+    ap.add_argument("--stage", choices=STAGES + AB_STAGES + SINGLE_STAGES, default=None,
                     help="run only this stage per step (for profiler captures); prints its per-launch time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
