@@ -47,6 +47,12 @@
  * conv_stack_forward call, X3CONV_PDL once per process). The results are the same under every
  * setting; only the kernels that compute them change:
  *   X3CONV_FORCE_KERNEL=direct|igemm  plans made with X3_KERNEL_AUTO use that engine
+ *   X3CONV_FORCE_KERNEL=igemm_nsub    plans made with X3_KERNEL_AUTO skip the swapped-operand engine and
+ *                                     use the positions-as-M tcgen05 engine ("igemm_tcgen05") where it
+ *                                     applies, else the direct kernel
+ *   X3CONV_TN=0                       2D channels-last layers with at most 64 output channels use the
+ *                                     M = 64 form instead of the positions-as-M / horizontal-taps-in-N
+ *                                     form (and X3CONV_TK=0 keeps 8-channel inputs off the taps-in-K form)
  *   X3CONV_STACK_LAYOUT=nchw          2D NCHW stacks run every layer in NCHW (no channels-last pass)
  *   X3CONV_S2=0                       stride 2 as the stride-1 raster with even positions kept,
  *                                     instead of the four input phases
