@@ -57,6 +57,9 @@
  *   X3CONV_S2=0                       stride 2 as the stride-1 raster with even positions kept,
  *                                     instead of the four input phases
  *   X3CONV_W2=1                       two-window tiles for causal channels-last layers
+ *   X3CONV_FRAME_PAIRS=0              causal channels-last layers compute their output frames one after
+ *                                     another instead of in adjacent pairs (the pairs read each shared
+ *                                     input frame from DRAM once)
  *   X3CONV_PDL=0                      launches fully serialised (no programmatic dependent launch)
  */
 #ifndef X3CONV_H

@@ -100,7 +100,7 @@ struct ClArgs {
     int out_nchw;    // 1: channels-last input, NCHW output (the NCHW epilogue)
     int yH, yW;      // stored output plane (H_out x W_out, or halved when sub2)
     int w_smem;      // bytes of shared memory for weight blocks (n_w stages, or all blocks when resident)
-    int frame_inner; // tile order with the output frame varying fastest
+    int frame_inner; // tile order: 1 = output frame fastest; 2 = frame pairs (frame within a pair fastest)
     int g_f32;       // centre-tap form: the tap planes of G in fp32 (else bf16)
     int stage_warp;  // epilogue staging bytes per warp
     int tn_cp, tn_n; // TN: output channels padded to 16, MMA N (3 horizontal taps x tn_cp)
@@ -126,6 +126,24 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
     ClTile c;
     uint32_t t = (uint32_t)tile;
     uint32_t q;
+    if (a.frame_inner == 2) {
+        // output frames in adjacent pairs (0,1), (2,3), ... of a pass: the two frames of a pair are
+        // computed together, so the two input frames they share are read from DRAM once and then
+        // hit in L2, while every tile that reads the carried frames (frames 0 and 1) still comes in
+        // the first pairs
+        const uint32_t fi = t & 1u;
+        t >>= 1;
+        q = fdiv(t, a.fd_ntiles);
+        c.nt = (int)(t - q * a.fd_ntiles.d);
+        t = q;
+        q = fdiv(t, a.fd_windows);
+        c.win = (int)(t - q * a.fd_windows.d);
+        t = q;
+        q = fdiv(t, a.fd_strips);
+        c.strip = (int)(t - q * a.fd_strips.d);
+        c.fr = (int)(2 * q + fi);
+        return c;
+    }
     if (a.frame_inner) {
         // frames fastest: the output frames of one window are in flight together, so the input frames
         // they share (three temporal taps each) are read from DRAM once and then hit in L2
@@ -1559,7 +1577,15 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.stage_warp = g.stage_warp;
     a.tn_cp = g.tn_cp; a.tn_n = g.tn_n; a.x_bytes = g.x_bytes;
     a.row_shift = row_shift;
-    a.frame_inner = g.ctr;
+    a.frame_inner = g.ctr ? 1 : 0;
+    // causal channels-last layers whose passes have an even number of frames: frame pairs, unless
+    // X3CONV_FRAME_PAIRS=0 (the tiles and their sums are the same; only the order changes)
+    {
+        const char* fp = getenv("X3CONV_FRAME_PAIRS");
+        if (!g.ctr && !g.tn && !g.nchw && !g.w2 && g.KT == 3 && d.dims == 3 && (d.D % 2) == 0 &&
+            !(fp && !strcmp(fp, "0")))
+            a.frame_inner = 2;
+    }
     a.g_f32 = d.kernel == X3_KERNEL_HEAD_SPLIT ? 1 : 0;
     a.has_carry = carry != nullptr;
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
