@@ -359,6 +359,17 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
     // waits in the same way before it touches this one's output. With a carry, the next kernel may
     // be the copy that overwrites it, so the MMA issuer signals only once every read of the carry
     // by this CTA has landed in shared memory (one signal per CTA counts; the first one).
+    // Resident weights (M = 64, TN and TK forms) are loaded before that wait: the packed weights are
+    // written by the packing kernel, never by the kernel this one may overlap (that kernel passed its
+    // own wait, so every kernel before it, the packing included, has completed), and the copy then
+    // overlaps the previous kernel's tail.
+    if ((M64 || TN) && warp == 0 && lane == 0) {
+        const int nblk = TK ? 5 : a.KT * a.n_chunks * (TN ? 3 : 9);
+        const uint32_t bb = TK ? (uint32_t)a.tn_n * 32u : (TN ? (uint32_t)a.tn_n * 128u : (uint32_t)kWBlock64);
+        ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)nblk * bb);
+        for (int b = 0; b < nblk; ++b)
+            ptx::bulk_load(sW + (uint32_t)b * bb, a.w + (size_t)b * bb, bb, bar_w_full);
+    }
     ptx::grid_dep_wait();
     if (!a.has_carry) ptx::grid_dep_launch();
     const uint32_t tmem_base = *tmem_slot;
@@ -379,12 +390,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             uint32_t h_cnt = 0, w_cnt = 0, r_cnt = 0;
             RingPos hr, wr;  // halo and weight ring positions of h_cnt and w_cnt
             bool ok = true;
-            if (M64 || TN) {  // every weight block of the layer, once, on the first weight barrier
-                const int nblk = TK ? 5 : a.KT * a.n_chunks * (TN ? 3 : 9);
-                const uint32_t bb = TK ? (uint32_t)a.tn_n * 32u : (TN ? (uint32_t)a.tn_n * 128u : (uint32_t)kWBlock64);
-                ptx::mbar_arrive_expect_tx(bar_w_full, (uint32_t)nblk * bb);
-                for (int b = 0; b < nblk; ++b)
-                    ptx::bulk_load(sW + (uint32_t)b * bb, a.w + (size_t)b * bb, bb, bar_w_full);
+            if (M64 || TN) {  // every weight block of the layer, loaded once before the grid dependency wait
                 w_cnt = 1;
                 wr.next(a.n_w);
             }
