@@ -62,7 +62,7 @@ constexpr int kStageGenericBytes = 32 * kStagePitch;  // per-warp staging block 
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
 constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
-constexpr int kStnPitch = 67;     // STN: fp32 staging row (the 66 TMEM columns a chunk reads + pad) per tap row
+constexpr int kStnPitch = 65;     // STN: fp32 staging row (a ring of four 16-position window rows + pad) per tap row
 constexpr int kStnStageBytes = 27 * kStnPitch * 4;  // 27 rows: 9 taps x 3 channels
 
 // Division by a run-time constant d without a division instruction: for 0 <= x < 2^31,
@@ -1064,36 +1064,57 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     drain(4);
                 } else if (STN) {
                     // Window position m = 16a + c holds G at plane row a, column c (row 0 and 15, column 0
-                    // and 15 are halo). Per chunk of 32 output positions, the warp stages TMEM columns
-                    // [32k - 17, 32k + 49) of its 27 rows (9 taps x 3 channels) as S[lane][0..65];
-                    // thread t then sums, for output m = 32k + t, bias + the nine taps in (i, j) order
-                    // at m + (i-1)*16 + (j-1), all inside the staged range since |offset| <= 17.
+                    // and 15 are halo). The warp stages its 27 rows (9 taps x 3 channels) one window row
+                    // at a time into a ring of four rows, S[lane][16 * (a & 3) + c]: chunk k (outputs in
+                    // window rows 2k and 2k + 1) adds rows 2k + 1 and 2k + 2 to the row 0 and rows up to
+                    // 2k staged before, so every TMEM column is read and staged once. Thread t then sums,
+                    // for output m = 32k + t, bias + the nine taps in (i, j) order at row a + i - 1,
+                    // column c + j - 1.
                     float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [27][kStnPitch]
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
                     const int oh_base = tc.win * (a.HR - 2) - 1, ow_base = ow0 - 1;
                     const size_t W2o = 2 * (size_t)a.W_out;
                     const size_t row0 = ((size_t)n * a.dout + t) * 2 * (size_t)a.H_out;
-                    for (int k = 0; k < kBNP / 32; ++k) {
+                    {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(tq, v);  // window row 0
+                        ptx::tmem_ld_wait();
+                        if (lane < 27) {
 #pragma unroll
-                        for (int part = 0; part < 3; ++part) {
-                            const int col = 32 * (k - 1 + part);
-                            if (col < 0 || col >= kBNP) continue;  // only invalid outputs would read it
+                            for (int x = 0; x < 16; ++x) S[lane * kStnPitch + x] = __uint_as_float(v[x]);
+                        }
+                    }
+                    for (int k = 0; k < kBNP / 32; ++k) {
+                        if (k < kBNP / 32 - 1) {
                             uint32_t v[32];
-                            ptx::tmem_ld32(tq + (uint32_t)col, v);
+                            ptx::tmem_ld32(tq + (uint32_t)(32 * k + 16), v);  // window rows 2k + 1, 2k + 2
                             ptx::tmem_ld_wait();
                             if (lane < 27) {
+                                float* s1 = S + lane * kStnPitch + 16 * ((2 * k + 1) & 3);
+                                float* s2 = S + lane * kStnPitch + 16 * ((2 * k + 2) & 3);
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    const int sc = part * 32 + j - 15;  // staged column of TMEM column col + j
-                                    if (sc >= 0 && sc < 66) S[lane * kStnPitch + sc] = __uint_as_float(v[j]);
+                                for (int x = 0; x < 16; ++x) {
+                                    s1[x] = __uint_as_float(v[x]);
+                                    s2[x] = __uint_as_float(v[16 + x]);
                                 }
+                            }
+                        } else {
+                            uint32_t v[16];
+                            ptx::tmem_ld16(tq + (uint32_t)(32 * k + 16), v);  // window row 15 (the last)
+                            ptx::tmem_ld_wait();
+                            if (lane < 27) {
+                                float* s1 = S + lane * kStnPitch + 16 * ((2 * k + 1) & 3);
+#pragma unroll
+                                for (int x = 0; x < 16; ++x) s1[x] = __uint_as_float(v[x]);
                             }
                         }
                         __syncwarp();
-                        const int m = 32 * k + lane;
-                        const int wa = m >> 4, wc = m & 15;
+                        const int wa = 2 * k + (lane >> 4), wc = lane & 15;
                         const int oh = oh_base + wa, ow = ow_base + wc;
                         if (wa >= 1 && wa <= 14 && wc >= 1 && wc <= 14 && oh < a.H_out && ow < a.W_out) {
+                            int ro[3];
+#pragma unroll
+                            for (int i = 0; i < 3; ++i) ro[i] = 16 * ((wa + i - 1) & 3) + wc - 1;
 #pragma unroll
                             for (int cl = 0; cl < 3; ++cl) {
                                 const int c = 3 * q + cl;
@@ -1102,7 +1123,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 for (int i = 0; i < 3; ++i)
 #pragma unroll
                                     for (int j = 0; j < 3; ++j)
-                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + 17 + lane + (i - 1) * 16 + (j - 1)];
+                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + ro[i] + j];
                                 const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
                                 y[((row0 + 2 * (size_t)oh + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
                                     cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, acc)));
