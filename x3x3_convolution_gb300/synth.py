@@ -168,7 +168,7 @@ def conv3d_stack(D=4, H=352, W=624, H3=176, W3=312, C=128, C3_in=256, variant="r
     return dict(x=x, carries=carries, layers=layers, x3=x3, carry3=carry3, L3=L3)
 
 
-def head(D=4, H=352, W=624, C_in=256, variant="random", seed=1005, dtype="bf16"):
+def head(D=4, H=352, W=624, C_in=256, variant="random", seed=1005, dtype="bf16", N=1):
     """conv_out head: causal 256->12 with clamp (bias U[-0.05,0.05])."""
-    return conv3d_single(C_in=C_in, C_out=12, D=D, H=H, W=W, variant=variant, seed=seed,
+    return conv3d_single(C_in=C_in, C_out=12, D=D, H=H, W=W, N=N, variant=variant, seed=seed,
                          act="clamp", dtype=dtype, bias_range=0.05)
