@@ -81,6 +81,36 @@ def test_noalloc_matches_workspace_stack_twice():
             assert torch.equal(a, b)
 
 
+def test_noalloc_matches_workspace_channels_last_2d_stack():
+    """A TAESD-like 2D NCHW stack (kept channels-last between its layers, stride 2 inside, NCHW out):
+    the built-in scratch holds the converted input and the ping-pong activations; twice in a row,
+    bit for bit the workspace version."""
+    N, H, W = 1, 96, 128
+    spec = [(3, 64, 1), (64, 64, 1), (64, 64, 2), (64, 64, 1)]
+    layers = [synth.make_layer([5200, i], 2, ci, co, "f16", stride=s, act="relu")
+              for i, (ci, co, s) in enumerate(spec)]
+    convs, h, w = [], H, W
+    for L in layers:
+        convs.append(x3.Conv(x3.make_desc(2, N, L.C_in, L.C_out, h, w, stride=L.stride, dtype="f16", act="relu"),
+                             dev(L.w), dev(L.b)))
+        h, w = convs[-1].H_out, convs[-1].W_out
+    stack = x3.ConvStack(convs)
+    assert 0 < stack.ws_bytes <= SCRATCH_BYTES
+    fn = _noalloc_fn()
+    plans, k1 = _arr([c.plan for c in convs])
+    wts, k2 = _arr([c._wp for c in convs])
+    bias, k3 = _arr([c.bias.data_ptr() for c in convs])
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        x = dev(synth.activation([5200, 10 + call], (N, 3, H, W), "f16", "random", ("uniform", -1.0, 1.0)))
+        y_ref = stack(x)
+        y_new = torch.empty_like(y_ref)
+        st = fn(plans, len(convs), x.data_ptr(), None, 0, wts, bias, y_new.data_ptr(), stream)
+        assert st == x3.X3_OK, x3.conv_last_error()
+        torch.cuda.synchronize()
+        assert torch.equal(y_new, y_ref)
+
+
 def test_noalloc_rejects_stacks_beyond_its_scratch():
     # two 128-channel 4-frame 352x624 intermediates need far more than the built-in scratch
     convs = [x3.Conv(x3.make_desc(3, 1, 128, 128, 352, 624, D=4, act="relu"),

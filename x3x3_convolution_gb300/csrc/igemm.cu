@@ -813,12 +813,10 @@ x3_status launch_igemm(const x3_conv_plan* p, const void* x, const void* carry, 
 // the status word records the timeout, exactly as in the convolution kernels.
 __global__ void selftest_wait_kernel(uint64_t limit_ns) {
     __shared__ __align__(8) uint64_t bar;
-    __shared__ int abort_flag;
     if (threadIdx.x != 0) return;
     const uint32_t b = ptx::smem_u32(&bar);
     ptx::mbar_init(b, 1);
     ptx::fence_mbar_init();
-    abort_flag = 0;
     const uint64_t t0 = ptx::globaltimer();
     while (!ptx::mbar_try_wait(b, 0)) {
         if (ptx::globaltimer() - t0 > limit_ns) {
