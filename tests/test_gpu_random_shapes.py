@@ -1,0 +1,106 @@
+"""A seeded sweep of random layer shapes through the C ABI, against the oracle.
+
+Each case draws its descriptor from a fixed generator: 2D layers (NCHW or NHWC, f16 or bf16, stride 1
+or 2) or causal 3D layers (NDHWC bf16, with or without a history), channel counts around and between
+the engines' tile sizes, heights and widths from one row or column to a few tiles with ragged tails,
+batches of 1 to 3 and every activation (TAESD conv page: pad-1 cross-correlation with stride, bias,
+ReLU; FastVideo head.cu page, header comment: causal 3x3x3 over [2 carried frames, current frames],
+all taps in one fp32 accumulator, clamp). Data are integers in {-2..2}, so every fp32 partial sum is an
+exact integer below 2^24 and the stored values must equal the oracle's, rounded once to the storage
+type, bit for bit, whatever engine or form the planner picks for the shape. The sweep must reach the
+tensor-core engines and the direct kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import x3x3_convolution_gb300 as x3
+from x3x3_convolution_gb300 import synth
+from tests.gpu_helpers import assert_exact, dev, host_values
+
+pytestmark = pytest.mark.gpu
+
+N_2D, N_3D = 28, 20
+MAX_FLOP = 1.5e10  # keeps the oracle at a few seconds per case
+
+
+def _draw(seed=7100):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < N_2D:
+        c = dict(dims=2, layout=str(rng.choice(["NCHW", "NHWC"])), dtype=str(rng.choice(["f16", "bf16"])),
+                 C_in=int(rng.choice([1, 3, 8, 16, 24, 40, 64, 72, 128])),
+                 C_out=int(rng.choice([8, 16, 32, 48, 64, 80, 96, 128, 136])),
+                 stride=int(rng.choice([1, 1, 2])), N=int(rng.integers(1, 4)), H=int(rng.integers(1, 70)),
+                 W=int(rng.integers(1, 150)), act=str(rng.choice(["none", "relu", "clamp"])))
+        if 2.0 * 9 * c["C_in"] * c["C_out"] * c["N"] * c["H"] * c["W"] <= MAX_FLOP:
+            cases.append(c)
+    while len(cases) < N_2D + N_3D:
+        c = dict(dims=3, layout="NDHWC", dtype="bf16", C_in=int(rng.choice([8, 16, 32, 40, 64, 128, 256])),
+                 C_out=int(rng.choice([8, 16, 64, 72, 96, 128, 256])), stride=1, N=int(rng.integers(1, 3)),
+                 D=int(rng.integers(1, 5)), H=int(rng.integers(1, 21)), W=int(rng.integers(1, 200)),
+                 act=str(rng.choice(["none", "relu", "clamp"])), carry=bool(rng.integers(0, 2)))
+        if 2.0 * 27 * c["C_in"] * c["C_out"] * c["N"] * c["D"] * c["H"] * c["W"] <= MAX_FLOP:
+            cases.append(c)
+    return cases
+
+
+CASES = _draw()
+SEEN = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    x3.load()
+    yield
+    assert x3.conv_device_status(1) == x3.X3_OK
+
+
+def _run(i, c):
+    seed = [7200, i]
+    if c["dims"] == 2:
+        shape = (c["N"], c["C_in"], c["H"], c["W"]) if c["layout"] == "NCHW" else (c["N"], c["H"], c["W"], c["C_in"])
+        x = synth.activation(seed + [0], shape, c["dtype"], "int")
+        L = synth.make_layer(seed, 2, c["C_in"], c["C_out"], c["dtype"], stride=c["stride"], act=c["act"], variant="int")
+        d = x3.make_desc(2, c["N"], c["C_in"], c["C_out"], c["H"], c["W"], stride=c["stride"], layout=c["layout"],
+                         dtype=c["dtype"], act=c["act"])
+        conv = x3.Conv(d, dev(L.w), dev(L.b))
+        got = host_values(conv(dev(x)), c["dtype"])
+        ref = oracle.conv2d(x.vals, L.w.vals, L.b.vals, stride=c["stride"], act=c["act"], layout=c["layout"])
+    else:
+        x = synth.activation(seed + [0], (c["N"], c["D"], c["H"], c["W"], c["C_in"]), "bf16", "int")
+        carry = synth.activation(seed + [1], (c["N"], 2, c["H"], c["W"], c["C_in"]), "bf16", "int") if c["carry"] else None
+        L = synth.make_layer(seed, 3, c["C_in"], c["C_out"], "bf16", act=c["act"], variant="int")
+        d = x3.make_desc(3, c["N"], c["C_in"], c["C_out"], c["H"], c["W"], D=c["D"], layout="NDHWC", dtype="bf16",
+                         act=c["act"])
+        conv = x3.Conv(d, dev(L.w), dev(L.b))
+        got = host_values(conv(dev(x), None if carry is None else dev(carry)), "bf16")
+        ref = oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=None if carry is None else carry.vals,
+                                   act=c["act"], layout="NDHWC")
+    torch.cuda.synchronize()
+    return got, ref, conv.kernel_name
+
+
+@pytest.mark.parametrize("i", range(len(CASES)))
+def test_random_shape_matches_oracle(i):
+    c = CASES[i]
+    got, ref, kname = _run(i, c)
+    SEEN[i] = kname
+    assert got.shape == ref.shape, (c, got.shape, ref.shape)
+    assert_exact(got, ref, c["dtype"])
+
+
+def test_sweep_reaches_every_engine():
+    """Runs after the cases (pytest keeps file order): the planner sent the sweep's shapes to the
+    swapped-operand tensor-core engine, to another tensor-core form or engine, and to the direct kernel."""
+    if len(SEEN) < len(CASES):
+        for i in range(len(CASES)):
+            if i not in SEEN:
+                SEEN[i] = _run(i, CASES[i])[2]
+    names = set(SEEN.values())
+    assert any(n.startswith("igemm_tcgen05_sw128") for n in names), names
+    assert any(n.startswith("igemm_tcgen05") for n in names), names
+    assert "direct_simt" in names, names
