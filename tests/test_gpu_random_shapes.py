@@ -1,4 +1,4 @@
-"""A seeded sweep of random layer shapes through the C ABI, against the oracle.
+"""Seeded sweeps of random layer shapes and 2D stacks through the C ABI, against the oracle.
 
 Each case draws its descriptor from a fixed generator: 2D layers (NCHW or NHWC, f16 or bf16, stride 1
 or 2) or causal 3D layers (NDHWC bf16, with or without a history), channel counts around and between
@@ -104,3 +104,43 @@ def test_sweep_reaches_every_engine():
     assert any(n.startswith("igemm_tcgen05_sw128") for n in names), names
     assert any(n.startswith("igemm_tcgen05") for n in names), names
     assert "direct_simt" in names, names
+
+
+def _draw_stacks(n=10, seed=7300):
+    """2D NCHW stacks of 2 to 5 layers: channel counts that are multiples of 8 after the first layer
+    (the channels-last stack path), stride 2 anywhere but the last layer."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        depth = int(rng.integers(2, 6))
+        chans = [int(rng.choice([1, 3, 8, 16]))] + [int(rng.choice([8, 16, 32, 48, 64, 72])) for _ in range(depth)]
+        strides = [int(rng.choice([1, 1, 2])) for _ in range(depth - 1)] + [1]
+        out.append(dict(N=int(rng.integers(1, 3)), H=int(rng.integers(8, 60)), W=int(rng.integers(8, 130)),
+                        dtype=str(rng.choice(["f16", "bf16"])), chans=chans, strides=strides))
+    return out
+
+
+STACKS = _draw_stacks()
+
+
+@pytest.mark.parametrize("i", range(len(STACKS)))
+def test_random_stack_matches_oracle(i):
+    """'fewtaps' data (integer inputs, three +-1 weights per output channel, integer bias) keep every
+    value of the chain an exact integer, so the stack's output equals the oracle's chain with the
+    intermediates rounded to the storage type bit for bit."""
+    c = STACKS[i]
+    x = synth.activation([7400, i, 0], (c["N"], c["chans"][0], c["H"], c["W"]), c["dtype"], "fewtaps")
+    layers = [synth.make_layer([7400, i, 1 + k], 2, ci, co, c["dtype"], stride=s, act="relu", variant="fewtaps")
+              for k, (ci, co, s) in enumerate(zip(c["chans"][:-1], c["chans"][1:], c["strides"]))]
+    convs, h, w = [], c["H"], c["W"]
+    for L in layers:
+        convs.append(x3.Conv(x3.make_desc(2, c["N"], L.C_in, L.C_out, h, w, stride=L.stride, dtype=c["dtype"],
+                                          act="relu"), dev(L.w), dev(L.b)))
+        h, w = convs[-1].H_out, convs[-1].W_out
+    got = host_values(x3.ConvStack(convs)(dev(x)), c["dtype"])
+    torch.cuda.synchronize()
+    y = x.vals
+    for L in layers:
+        y, _ = oracle.round_to(oracle.conv2d(y, L.w.vals, L.b.vals, stride=L.stride, act="relu"), c["dtype"])
+    assert got.shape == y.shape
+    assert np.array_equal(got, y)
