@@ -1,4 +1,5 @@
-"""Seeded sweeps of random layer shapes and 2D stacks through the C ABI, against the oracle.
+"""Seeded sweeps of random layer shapes and of random 2D and causal stacks through the C ABI, against the
+oracle.
 
 Each case draws its descriptor from a fixed generator: 2D layers (NCHW or NHWC, f16 or bf16, stride 1
 or 2) or causal 3D layers (NDHWC bf16, with or without a history), channel counts around and between
@@ -144,3 +145,55 @@ def test_random_stack_matches_oracle(i):
         y, _ = oracle.round_to(oracle.conv2d(y, L.w.vals, L.b.vals, stride=L.stride, act="relu"), c["dtype"])
     assert got.shape == y.shape
     assert np.array_equal(got, y)
+
+
+def _draw_stacks3d(n=6, seed=7500):
+    """Causal 3D stacks of 2 or 3 layers (channels-last bf16) run as two passes with their histories."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        depth = int(rng.integers(2, 4))
+        chans = [int(rng.choice([8, 16, 32, 64]))] + [int(rng.choice([16, 32, 64, 96, 128])) for _ in range(depth)]
+        out.append(dict(N=int(rng.integers(1, 3)), D=int(rng.integers(1, 5)), H=int(rng.integers(1, 13)),
+                        W=int(rng.integers(8, 150)), chans=chans,
+                        acts=[str(rng.choice(["relu", "none"])) for _ in range(depth)]))
+    return out
+
+
+STACKS3D = _draw_stacks3d()
+
+
+def _oracle_pass(x, carries, layers):
+    """Layer by layer, each output rounded to bf16 as the library stores it; the new histories are the
+    last two frames of each layer's input sequence [history, input]."""
+    y, new = x, []
+    for i, L in enumerate(layers):
+        seq = np.concatenate([carries[i], y], axis=1)
+        new.append(seq[:, -2:].copy())
+        y, _ = oracle.round_to(oracle.conv3d_causal(y, L.w.vals, L.b.vals, carry=carries[i], act=L.act,
+                                                    layout="NDHWC"), "bf16")
+    return y, new
+
+
+@pytest.mark.parametrize("i", range(len(STACKS3D)))
+def test_random_causal_stack_two_passes(i):
+    """Two passes of a random causal stack: the first with no history (zeros), the second reading the
+    histories the first wrote; outputs and the final histories bit for bit against the oracle on
+    'fewtaps' data (integer inputs, three +-1 weights per output channel: exact integer chains)."""
+    c = STACKS3D[i]
+    N, D, H, W, chans = c["N"], c["D"], c["H"], c["W"], c["chans"]
+    layers = [synth.make_layer([7600, i, k], 3, ci, co, "bf16", act=a, variant="fewtaps")
+              for k, (ci, co, a) in enumerate(zip(chans[:-1], chans[1:], c["acts"]))]
+    convs = [x3.Conv(x3.make_desc(3, N, L.C_in, L.C_out, H, W, D=D, act=L.act), dev(L.w), dev(L.b)) for L in layers]
+    stack = x3.ConvStack(convs)
+    cdev = [torch.zeros((N, 2, H, W, ci), dtype=torch.bfloat16, device="cuda") for ci in chans[:-1]]
+    chost = [np.zeros((N, 2, H, W, ci), np.float32) for ci in chans[:-1]]
+    for p in range(2):
+        x = synth.activation([7600, i, 10 + p], (N, D, H, W, chans[0]), "bf16", "fewtaps")
+        got = host_values(stack(dev(x), carries=cdev, carry_valid=p > 0), "bf16")
+        torch.cuda.synchronize()
+        want, chost = _oracle_pass(x.vals, chost, layers)
+        assert got.shape == want.shape
+        assert np.array_equal(got, want), (c, p)
+        for k in range(len(layers)):
+            assert np.array_equal(host_values(cdev[k], "bf16"), chost[k]), (c, p, k)
