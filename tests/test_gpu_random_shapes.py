@@ -1,5 +1,5 @@
-"""Seeded sweeps of random layer shapes and of random 2D and causal stacks through the C ABI, against the
-oracle.
+"""Seeded sweeps through the C ABI against the oracle: random layer shapes, random 2D and causal stacks,
+and random layers cut into random row bands.
 
 Each case draws its descriptor from a fixed generator: 2D layers (NCHW or NHWC, f16 or bf16, stride 1
 or 2) or causal 3D layers (NDHWC bf16, with or without a history), channel counts around and between
@@ -197,3 +197,71 @@ def test_random_causal_stack_two_passes(i):
         assert np.array_equal(got, want), (c, p)
         for k in range(len(layers)):
             assert np.array_equal(host_values(cdev[k], "bf16"), chost[k]), (c, p, k)
+
+
+def _draw_bands(n=8, seed=7700):
+    """Random stride-1 layers (2D NHWC, 2D NCHW, causal 3D) cut into 2 to 4 random row bands."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        dims = int(rng.choice([2, 2, 3]))
+        H = int(rng.integers(4, 60))
+        cuts = sorted(set(int(v) for v in rng.integers(1, H, size=int(rng.integers(1, 4)))))
+        bounds = [0] + cuts + [H]
+        c = dict(dims=dims, N=int(rng.integers(1, 3)), H=H, W=int(rng.integers(8, 140)),
+                 C_in=int(rng.choice([8, 16, 64, 128])), C_out=int(rng.choice([16, 64, 96, 128])),
+                 act=str(rng.choice(["none", "relu"])), bands=[(a, b - a) for a, b in zip(bounds[:-1], bounds[1:])])
+        if dims == 2:
+            c.update(layout=str(rng.choice(["NHWC", "NCHW"])), dtype=str(rng.choice(["f16", "bf16"])))
+            if c["layout"] == "NCHW":
+                c["W"] = (c["W"] + 7) // 8 * 8  # the NCHW tensor-core form stages 16-byte rows
+        else:
+            c.update(layout="NDHWC", dtype="bf16", D=int(rng.integers(1, 4)))
+        out.append(c)
+    return out
+
+
+BANDS = _draw_bands()
+
+
+@pytest.mark.parametrize("i", range(len(BANDS)))
+def test_random_bands_concatenate_to_the_plane(i):
+    """Banded mode (FastVideo head.cu page: head_stencil_kernel's band row offset and global height):
+    each band computed from its rows plus the halo rows that exist; the bands, concatenated, equal the
+    whole plane bit for bit, and the plane equals the oracle on integer data."""
+    c = BANDS[i]
+    dt, H, W, N = c["dtype"], c["H"], c["W"], c["N"]
+    if c["dims"] == 3:
+        x = synth.activation([7800, i, 0], (N, c["D"], H, W, c["C_in"]), dt, "int")
+        carry = synth.activation([7800, i, 1], (N, 2, H, W, c["C_in"]), dt, "int")
+        L = synth.make_layer([7800, i], 3, c["C_in"], c["C_out"], dt, act=c["act"], variant="int")
+        base = dict(dims=3, N=N, C_in=c["C_in"], C_out=c["C_out"], D=c["D"], W=W, layout="NDHWC", dtype=dt, act=c["act"])
+        ax = 2
+    else:
+        shape = (N, c["C_in"], H, W) if c["layout"] == "NCHW" else (N, H, W, c["C_in"])
+        x = synth.activation([7800, i, 0], shape, dt, "int")
+        carry = None
+        L = synth.make_layer([7800, i], 2, c["C_in"], c["C_out"], dt, act=c["act"], variant="int")
+        base = dict(dims=2, N=N, C_in=c["C_in"], C_out=c["C_out"], W=W, layout=c["layout"], dtype=dt, act=c["act"])
+        ax = 2 if c["layout"] == "NCHW" else 1
+    full = x3.Conv(x3.make_desc(H=H, **base), dev(L.w), dev(L.b))
+    xd, cd = dev(x), (dev(carry) if carry is not None else None)
+    y_full = full(xd, cd) if cd is not None else full(xd)
+    outs = []
+    for lo, rows in c["bands"]:
+        in_lo, in_hi = x3.band_input_rows(lo, rows, H)
+        conv = x3.Conv(x3.make_desc(H=in_hi - in_lo, band_lo=lo, band_rows=rows, H_global=H, **base), dev(L.w), dev(L.b))
+        assert conv.kernel_name == full.kernel_name
+        xb = xd.narrow(ax, in_lo, in_hi - in_lo).contiguous()
+        if cd is not None:
+            outs.append(conv(xb, cd.narrow(ax, in_lo, in_hi - in_lo).contiguous()))
+        else:
+            outs.append(conv(xb))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, dim=ax), y_full), c
+    got = host_values(y_full, dt)
+    if c["dims"] == 3:
+        ref = oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act=c["act"], layout="NDHWC")
+    else:
+        ref = oracle.conv2d(x.vals, L.w.vals, L.b.vals, act=c["act"], layout=c["layout"])
+    assert_exact(got, ref, dt)
