@@ -1,5 +1,5 @@
 """Seeded sweeps through the C ABI against the oracle: random layer shapes, random 2D and causal stacks,
-and random layers cut into random row bands.
+random layers cut into random row bands, and random conv_out head planes.
 
 Each case draws its descriptor from a fixed generator: 2D layers (NCHW or NHWC, f16 or bf16, stride 1
 or 2) or causal 3D layers (NDHWC bf16, with or without a history), channel counts around and between
@@ -265,3 +265,41 @@ def test_random_bands_concatenate_to_the_plane(i):
     else:
         ref = oracle.conv2d(x.vals, L.w.vals, L.b.vals, act=c["act"], layout=c["layout"])
     assert_exact(got, ref, dt)
+
+
+def _draw_heads(n=8, seed=7900):
+    rng = np.random.default_rng(seed)
+    return [dict(N=int(rng.integers(1, 3)), D=int(rng.integers(1, 5)), H=int(rng.integers(1, 60)),
+                 W=int(rng.integers(1, 120)), carry=bool(rng.integers(0, 2))) for _ in range(n)]
+
+
+HEADS = _draw_heads()
+
+
+@pytest.mark.parametrize("i", range(len(HEADS)))
+def test_random_head_shapes(i):
+    """The conv_out head (256 -> 12, clamp, 2x2 unpatchify; the stencil head, the default) on random
+    plane sizes, with and without history: exact on sparse {-1,0,1} weights (small sums, mostly
+    unclamped), and on random data bit for bit the split head with fp32 G (same fp32 sums, same order)."""
+    c = HEADS[i]
+    N, D, H, W = c["N"], c["D"], c["H"], c["W"]
+    for variant in ("sparse1", "random"):
+        x = synth.activation([8000, i, 0], (N, D, H, W, 256), "bf16", variant, ("normal", 1.0))
+        carry = synth.activation([8000, i, 1], (N, 2, H, W, 256), "bf16", variant, ("normal", 1.0)) if c["carry"] else None
+        L = synth.make_layer([8000, i], 3, 256, 12, "bf16", act="clamp", variant=variant, bias_range=0.05)
+        outs = {}
+        for kernel in ("auto", "head_split"):
+            d = x3.make_desc(3, N, 256, 12, H, W, D=D, layout="NDHWC", dtype="bf16", act="clamp", unpatchify2x2=True,
+                             kernel=kernel)
+            conv = x3.Conv(d, dev(L.w), dev(L.b))
+            if kernel == "auto":
+                assert conv.kernel_name == "igemm_tcgen05_sw128_head_stencil"
+            outs[kernel] = host_values(conv(dev(x), None if carry is None else dev(carry)), "bf16")
+        torch.cuda.synchronize()
+        y12 = oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=None if carry is None else carry.vals,
+                                   act="clamp", layout="NDHWC")
+        ref = oracle.unpatchify2x2(y12.transpose(0, 4, 1, 2, 3)).transpose(0, 2, 3, 4, 1)
+        assert outs["auto"].shape == ref.shape == (N, D, 2 * H, 2 * W, 3)
+        if variant == "sparse1":
+            assert_exact(outs["auto"], ref, "bf16")
+        assert np.array_equal(outs["auto"], outs["head_split"])
