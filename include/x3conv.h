@@ -159,9 +159,11 @@ x3_status conv_plan_create(const x3_conv_desc* desc, x3_conv_plan** plan);
 void conv_plan_destroy(x3_conv_plan* plan);
 
 /* Name of the kernel the plan runs, for logs and tests: "igemm_tcgen05_sw128" (swapped-operand
- * tcgen05 engine, channels-last), "igemm_tcgen05_sw128_head" (its conv_out head form),
- * "igemm_tcgen05_sw128_nchw" (its NCHW form), "igemm_tcgen05" (positions-as-M tcgen05 engine),
- * "direct_simt", "head_two_pass" / "head_split" (run with conv_head_two_pass). */
+ * tcgen05 engine, channels-last, including its positions-as-M forms for low-channel 2D layers),
+ * "igemm_tcgen05_sw128_head" (its single-pass conv_out head form), "igemm_tcgen05_sw128_head_stencil"
+ * (the one-kernel stencil head), "igemm_tcgen05_sw128_nchw" (its NCHW form), "igemm_tcgen05"
+ * (positions-as-M tcgen05 engine), "direct_simt", "head_two_pass" / "head_split" (run with
+ * conv_head_two_pass). */
 const char* conv_plan_kernel_name(const x3_conv_plan* plan);
 
 /*
