@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import x3x3_convolution_gb300 as x3
@@ -198,18 +199,122 @@ def _check_sw128_plan(g):
     assert g["tiles"] == g["strips"] * g["windows"] * g["frames"] * g["n_tiles"]
 
 
+def stn_runs(H, strips, n, ctas, s=0):
+    """Greedy runs of n windows over strips s.. for at most `ctas` runs: per run its pieces
+    (strip, first output row, windows), and whether they reach the last strip."""
+    o = 0
+    runs = []
+    for _ in range(ctas):
+        if s >= strips:
+            break
+        pieces, rem = [], n
+        while rem > 0 and s < strips:
+            need = (H - o + 17) // 16
+            if need <= rem:
+                pieces.append((s, o, need))
+                rem -= need
+                s, o = s + 1, 0
+            else:
+                pieces.append((s, o, rem))
+                o += 16 * rem - 2
+                rem = 0
+        runs.append(pieces)
+    return runs, s >= strips
+
+
+def stn_plan(H, strips, runs_max):
+    """The stencil head's assignment: with at least as many strips as runs, whole strips in rounds (run
+    r takes r, r + R, ...), then the greedy over the strips left; else the greedy over all strips.
+    Returns per run its pieces and the windows per run (the plan's `windows`)."""
+    full = (H + 17) // 16
+    k = strips // runs_max if strips >= runs_max else 0
+    R = runs_max if k else 0
+    left0 = k * R
+    runs = [[(r + j * R, 0, full) for j in range(k)] for r in range(R)]
+    nb = 0
+    if left0 < strips:
+        nb = 1
+        while not stn_runs(H, strips, nb, runs_max, left0)[1]:
+            nb += 1
+        tail, _ = stn_runs(H, strips, nb, runs_max, left0)
+        for r, pieces in enumerate(tail):
+            if r < len(runs):
+                runs[r] += pieces
+            else:
+                runs.append(pieces)
+    return runs, k * full + nb
+
+
+def _check_stn_runs(g):
+    """The runs the plan implies cover every output row of every strip exactly once (a piece of nb
+    windows from row o0 yields rows o0 .. o0 + 16 nb - 3, clipped at the plane), each run by one CTA
+    per frame group (the fewest frames per group that divide the frames and leave no more groups than
+    CTAs), with no more CTAs than SMs; whole strips go in rounds over neighbouring strips when there
+    are at least as many strips as runs."""
+    H, strips, n, F = g["H_out"], g["strips"], g["windows"], g["frames"]
+    ctas = min(g["sms"], 256)
+    fpc = 1
+    while F % fpc or F // fpc > ctas:
+        fpc += 1
+    groups = F // fpc
+    runs_max = ctas // groups
+    runs, n_model = stn_plan(H, strips, runs_max)
+    assert n == n_model
+    assert len(runs) * groups == g["grid"] <= ctas
+    assert g["tiles"] == sum(nb for r in runs for (_, _, nb) in r) * g["frames"]
+    assert all(sum(nb for (_, _, nb) in r) <= n for r in runs)
+    cover = np.zeros((strips, H), np.int32)
+    for r in runs:
+        for s, o0, nb in r:
+            cover[s, o0:min(o0 + 16 * nb - 2, H)] += 1
+    assert np.all(cover == 1)
+
+
+@pytest.mark.parametrize("H,W,D,N", [(352, 624, 4, 1), (17, 33, 1, 1), (100, 300, 2, 2), (5, 2000, 3, 1),
+                                     (1000, 14, 2, 1), (64, 64, 8, 1), (40, 60, 7, 1), (20, 30, 100, 2)])
+def test_stencil_head_runs(lib, H, W, D, N):
+    d = x3.make_desc(3, N, 256, 12, H, W, D=D, act="clamp", unpatchify2x2=True, kernel="head_stencil")
+    p = x3.conv_plan_create(d)
+    try:
+        g = x3.conv_plan_describe(p)
+    finally:
+        x3.conv_plan_destroy(p)
+    assert g["stn"] == 1 and g["frames"] == N * D
+    _check_stn_runs(g)
+
+
+def test_stencil_head_run_model_rejects_bad_runs():
+    """The coverage check above fails for runs that overlap or leave gaps (a run yielding 16 nb - 1
+    or 16 nb - 3 rows per piece), so it constrains the piece arithmetic."""
+    def cover(step):
+        c = np.zeros((3, 100), np.int32)
+        s = o = 0
+        while s < 3:
+            need = (100 - o + 17) // 16
+            nb = min(need, 2)
+            c[s, o:min(o + 16 * nb + step, 100)] += 1
+            if nb == need:
+                s, o = s + 1, 0
+            else:
+                o += 16 * nb - 2
+        return c
+    assert np.all(cover(-2) == 1)
+    assert not np.all(cover(-1) == 1) and not np.all(cover(-3) == 1)
+
+
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_igemm_plans_cover_their_reads(lib, name):
     p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
     try:
         g = x3.conv_plan_describe(p)
         if g.get("stn"):
-            # stencil head: 16 x 16 raster windows, 14 x 14 outputs each, one stage per (kt, chunk)
-            # holding the window (32 KB) and its weight block (16 KB)
-            assert g["P"] == 16 and g["Wt"] == 14 and g["HR"] == 16 and g["win_adv"] == 14 * 16
-            assert g["strips"] * 14 >= g["W_out"] and g["windows"] * 14 >= g["H_out"]
+            # stencil head: 16 x 16 raster windows (14 output columns), one stage per (kt, chunk)
+            # holding the window (32 KB) and its weight block (16 KB); every CTA runs `windows`
+            # consecutive windows down the strips
+            assert g["P"] == 16 and g["Wt"] == 14 and g["HR"] == 16 and g["win_adv"] == 16 * 16
+            assert g["strips"] * 14 >= g["W_out"]
             assert g["h_bytes"] == 16 * 16 * 128 + 128 * 64 * 2 and g["smem_bytes"] <= 232448
-            assert g["tiles"] == g["strips"] * g["windows"] * g["frames"]
+            _check_stn_runs(g)
             return
         if WORKLOADS[name].get("kernel") == "head_two_pass":
             # the temporal pass stages no halo: windows of 256 consecutive positions of a frame, each

@@ -40,9 +40,9 @@ FORMS = {
     "direct": (dict(dims=3, N=1, C_in=8, C_out=8, D=2, H=11, W=13, kernel="direct"), {}, "direct_simt"),
     "head_stencil": (dict(dims=3, N=1, C_in=256, C_out=12, D=2, H=30, W=40, act="clamp", unpatchify2x2=True), {},
                      "igemm_tcgen05_sw128_head_stencil"),
-    # a larger plane: bands of 60 rows, many windows per band
-    "head_stencil_large": (dict(dims=3, N=1, C_in=256, C_out=12, D=2, H=180, W=560, act="clamp", unpatchify2x2=True),
-                           {}, "igemm_tcgen05_sw128_head_stencil"),
+    # large enough that every band's CTAs run several abutting windows (row sums carried across seams)
+    "head_stencil_runs": (dict(dims=3, N=1, C_in=256, C_out=12, D=2, H=180, W=560, act="clamp", unpatchify2x2=True),
+                          {}, "igemm_tcgen05_sw128_head_stencil"),
     "head_single_pass": (dict(dims=3, N=1, C_in=256, C_out=12, D=2, H=30, W=40, act="clamp", unpatchify2x2=True,
                               kernel="igemm"), {}, "igemm_tcgen05_sw128_head"),
 }

@@ -177,20 +177,23 @@ def test_stencil_head(variant, shape):
         assert np.array_equal(got, split)
 
 
-# (D, H, W, N): larger planes than SHAPES, many strips and windows per frame, and two batch items
-LARGE_SHAPES = [(2, 100, 300, 2), (4, 200, 600, 1), (3, 47, 1000, 1)]
+# (D, H, W, N): plans whose CTAs each run several abutting windows down the strips, with runs that
+# start mid-strip and runs that finish one strip and go on at the top of the next
+RUN_SHAPES = [(2, 100, 300, 2), (4, 200, 600, 1), (3, 47, 1000, 1)]
 
 
-@pytest.mark.parametrize("shape", LARGE_SHAPES, ids=str)
+@pytest.mark.parametrize("shape", RUN_SHAPES, ids=str)
 @pytest.mark.parametrize("variant", ["int", "sparse1", "random"])
-def test_stencil_head_large(variant, shape):
-    """The stencil head on planes with many strips and overlapping windows per frame and N = 2: exact on
-    integer and sparse data against the oracle; on random data within the tolerance and bit for bit the
-    split form."""
+def test_stencil_head_window_runs(variant, shape):
+    """The stencil head where each CTA runs consecutive windows of a strip that abut (no overlap): the
+    output rows centred on a seam are finished from row sums carried from the window above, for every
+    output frame. Exact on integer and sparse data against the oracle; on random data within the
+    tolerance and bit for bit the split form (the carried sums keep the (i, j) order)."""
     D, H, W, N = shape
     x, carry, L = synth.head(D=D, H=H, W=W, N=N, variant=variant, seed=3900 + H + W)
     got, conv = run_head(x, carry, L, "head_stencil")
-    assert conv.kernel_name == "igemm_tcgen05_sw128_head_stencil"
+    g = x3.conv_plan_describe(conv.plan)
+    assert conv.kernel_name == "igemm_tcgen05_sw128_head_stencil" and g["windows"] >= 2
     ref = to_rgb(oracle.conv3d_causal(x.vals, L.w.vals, L.b.vals, carry=carry.vals, act="clamp", layout="NDHWC"))
     assert got.shape == ref.shape
     if variant != "random":

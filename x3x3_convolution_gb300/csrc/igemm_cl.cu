@@ -64,6 +64,7 @@ constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accum
 constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
 constexpr int kStnPitch = 65;     // STN: fp32 staging row (a ring of four 16-position window rows + pad) per tap row
 constexpr int kStnStageBytes = 27 * kStnPitch * 4;  // 27 rows: 9 taps x 3 channels
+constexpr int kStnCarryBytes = 3 * 2 * 16 * 4;      // STN: per warp and output frame, two partial rows of 3 channels
 
 // Division by a run-time constant d without a division instruction: for 0 <= x < 2^31,
 // x / d == (x * m) >> s with l = ceil(log2 d), s = 31 + l and m = ceil(2^s / d) < 2^32 (Granlund and
@@ -107,17 +108,25 @@ struct ClArgs {
     int x_bytes;     // TN: bytes after the staging blocks (the epilogue warps' bias copies)
     int tn_tma;      // TN: each warp writes its raster row (64 channels) with one TMA store (tm_y)
     int row_shift;   // banded mode: the input's first row is the band's upper halo row
+    int stn_n;       // STN: windows per run (run blockIdx.x / stn_groups starts at stn_start[run])
+    int stn_fpc;     // STN: output frames per CTA (frame group blockIdx.x % stn_groups)
+    int stn_full;    // STN: whole strips per run before its share of the rest (run r: r, r + runs, ...)
+    int stn_runs;    // STN: runs (stn_full > 0: one per strip of each round of whole strips)
     long long tiles;
     FastDiv fd_frames, fd_ntiles, fd_windows, fd_strips, fd_dout, fd_P, fd_chunks;
+    FastDiv fd_fpc, fd_groups;  // STN
     uint32_t idesc;
     const uint8_t* w;
     const void* bias;
     void* y;
     unsigned int* status;  // the library's device status word
+    uint32_t stn_start[kStnMaxCtas];
 };
 
 struct ClTile {
     int nt, win, strip, fr;
+    int grow;   // STN: input row of the window's first row
+    int fslot;  // STN: the frame's place in this CTA's frame group
 };
 
 // The planner keeps tile counts below 2^31, so the decode runs in 32-bit unsigned arithmetic (a 64-bit
@@ -168,6 +177,57 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
     c.strip = (int)(t - q * a.fd_strips.d);
     c.fr = (int)q;
     return c;
+}
+
+// Stencil head: the k-th tile of this CTA, false past its last. The output frames are split into
+// groups of stn_fpc frames, and the CTAs c of one run (c / groups the same) take the groups c % groups
+// side by side, so that the frames reading the same input frames are computed at the same time and
+// share them through L2. A CTA runs its windows one after another, the frames of its group fastest,
+// first through stn_full whole strips (run r takes strips r, r + runs, ..., so that at any moment the
+// runs are on the same rows of neighbouring strips and the halo columns two strips share are read from
+// DRAM once), then from its start in the remaining strips (strip, first output row o0) down that strip
+// and on from row 0 of the following strips. The windows of one strip in one run do not overlap:
+// window b covers input rows o0 - 1 + 16 b to o0 + 14 + 16 b, and the two output rows centred on the
+// seam between windows b and b + 1 take their first kernel rows from sums the epilogue carries over
+// from window b. A run piece of nb windows so yields output rows o0 .. o0 + 16 nb - 3; the planner lets
+// the next run start at o0 + 16 nb - 2 (its first window re-reads the two rows above).
+__device__ __forceinline__ bool stn_decode(const ClArgs& a, long long k, ClTile& c) {
+    const uint32_t kk = (uint32_t)k;
+    const uint32_t w = fdiv(kk, a.fd_fpc);
+    if ((int)w >= a.stn_n) return false;
+    const uint32_t run = fdiv(blockIdx.x, a.fd_groups);
+    const uint32_t grp = blockIdx.x - run * a.fd_groups.d;
+    const int full = (a.H_out + 17) >> 4;  // windows of a whole strip
+    int s = 0, o = 0, b = (int)w;
+    bool whole = false;
+    for (int j = 0; j < a.stn_full; ++j) {
+        if (b < full) {
+            s = (int)run + j * a.stn_runs;
+            whole = true;
+            break;
+        }
+        b -= full;
+    }
+    if (!whole) {
+        const uint32_t st = a.stn_start[run];
+        s = (int)(st >> 16);
+        o = (int)(st & 0xFFFFu);
+    }
+    for (;;) {
+        if (s >= a.strips) return false;
+        const int need = (a.H_out - o + 17) >> 4;  // windows that finish the strip from row o
+        if (b < need) break;
+        b -= need;
+        ++s;
+        o = 0;
+    }
+    c.nt = 0;
+    c.fslot = (int)(kk - w * a.fd_fpc.d);
+    c.fr = (int)(grp * a.fd_fpc.d) + c.fslot;
+    c.strip = s;
+    c.win = b;
+    c.grow = o - 1 + 16 * b;
+    return true;
 }
 
 // Position in a ring of n stages: the stage index and the parity of its current phase, advanced
@@ -395,9 +455,14 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                 wr.next(a.n_w);
             }
             for (long long k = 0; ok; ++k) {
-                const long long tile = cl_tile_of(k);
-                if (tile >= a.tiles) break;
-                const ClTile tc = cl_decode(a, tile);
+                ClTile tc;
+                if (STN) {
+                    if (!stn_decode(a, k, tc)) break;
+                } else {
+                    const long long tile = cl_tile_of(k);
+                    if (tile >= a.tiles) break;
+                    tc = cl_decode(a, tile);
+                }
                 const int n = (int)fdiv((uint32_t)tc.fr, a.fd_dout), t = tc.fr - n * a.dout;
                 const int r0 = (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P);
                 const int ow0 = tc.strip * a.Wt;
@@ -444,7 +509,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                                 // and one barrier for both
                                 if (STN)
                                     ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1,
-                                                     tc.win * (a.HR - 2) - 1 + a.row_shift, fcoord);
+                                                     tc.grow + a.row_shift, fcoord);
                                 else
                                     ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, tc.win * kBNP, 0, fcoord);
                                 ptx::bulk_load(sH + sh * a.h_bytes + (uint32_t)kCtrW,
@@ -530,18 +595,29 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             long long last_carry_k = -1;
             if (a.has_carry) {
                 for (long long k = 0;; ++k) {
-                    const long long tile = cl_tile_of(k);
-                    if (tile >= a.tiles) break;
-                    if (a.KT == 3) {
-                        const int fr = cl_decode(a, tile).fr;
-                        if (fr - (int)fdiv((uint32_t)fr, a.fd_dout) * a.dout < 2) last_carry_k = k;
+                    int fr;
+                    if (STN) {
+                        ClTile tc;
+                        if (!stn_decode(a, k, tc)) break;
+                        fr = tc.fr;
+                    } else {
+                        const long long tile = cl_tile_of(k);
+                        if (tile >= a.tiles) break;
+                        fr = a.KT == 3 ? cl_decode(a, tile).fr : 2;
                     }
+                    if (a.KT == 3 && fr - (int)fdiv((uint32_t)fr, a.fd_dout) * a.dout < 2) last_carry_k = k;
                 }
                 if (last_carry_k < 0) ptx::grid_dep_launch();
             }
             for (long long k = 0; ok; ++k) {
-                const long long tile = cl_tile_of(k);
-                if (tile >= a.tiles) break;
+                long long tile = 0;
+                ClTile tcs;
+                if (STN) {
+                    if (!stn_decode(a, k, tcs)) break;
+                } else {
+                    tile = cl_tile_of(k);
+                    if (tile >= a.tiles) break;
+                }
                 if constexpr (TN) {
                     // positions as M: per (kt, chunk) halo and kernel row kh, A = the 128 positions from
                     // halo position kh P (swizzled K-major rows; windows start at a raster row), B = the
@@ -611,8 +687,8 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     ++it;
                     continue;
                 }
-                const ClTile tc = cl_decode(a, tile);
-                const int pos_off = tc.win * a.win_adv - (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P) * a.P;
+                const ClTile tc = STN ? tcs : cl_decode(a, tile);
+                const int pos_off = STN ? 0 : tc.win * a.win_adv - (int)fdiv((uint32_t)(tc.win * a.win_adv), a.fd_P) * a.P;
                 // two accumulator buffers used alternately, or (W2) one pair of them per tile
                 const uint32_t ab = W2 ? 0u : (it & 1u);
                 const uint32_t use = W2 ? it : (it >> 1);
@@ -788,8 +864,14 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             __syncwarp();
         }
         for (long long k = 0;; ++k, ++it) {
-            const long long tile = cl_tile_of(k);
-            if (tile >= a.tiles) break;
+            long long tile = 0;
+            ClTile tcs;
+            if (STN) {
+                if (!stn_decode(a, k, tcs)) break;
+            } else {
+                tile = cl_tile_of(k);
+                if (tile >= a.tiles) break;
+            }
             // TN: warps 2-5 drain the even tiles (TMEM buffer 0), warps 6-9 the odd ones (buffer 1)
             if (TN && (int)(it & 1u) != (ew >> 2)) continue;
             if constexpr (TN) {
@@ -905,7 +987,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
             const uint32_t ab = W2 ? 0u : (it & 1u);
             if (!cl_wait(bar_acc_full + 8 * ab, (W2 ? it : (it >> 1)) & 1u, abort_flag, a.status)) break;
             ptx::tc_fence_after();
-            const ClTile tc = cl_decode(a, tile);
+            const ClTile tc = STN ? tcs : cl_decode(a, tile);
             const int n = (int)fdiv((uint32_t)tc.fr, a.fd_dout), t = tc.fr - n * a.dout;
             constexpr int kCpw = M64 ? 16 : 32;  // accumulator rows per TMEM lane quarter
             const int co_lane = (M64 && lane >= 16) ? a.C_out : tc.nt * (M64 ? 64 : kBM) + q * kCpw + lane;
@@ -1069,10 +1151,16 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     // window rows 2k and 2k + 1) adds rows 2k + 1 and 2k + 2 to the row 0 and rows up to
                     // 2k staged before, so every TMEM column is read and staged once. Thread t then sums,
                     // for output m = 32k + t, bias + the nine taps in (i, j) order at row a + i - 1,
-                    // column c + j - 1.
+                    // column c + j - 1. Window row a is centred on output row grow + a; rows 1-14 are
+                    // complete here. At the seam with the next window of the run, chunk 7 leaves in
+                    // shared memory (per output frame) the partial sums, in the same order, of the
+                    // output rows centred on rows 15 (kernel rows i = 0, 1) and 16 (i = 0); chunk 0 of
+                    // that next window finishes them.
                     float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [27][kStnPitch]
+                    float* Cw = reinterpret_cast<float*>(sbase + (sBiasT - base)) +
+                                (size_t)(ew * a.stn_fpc + tc.fslot) * (kStnCarryBytes / 4);  // [3][2][16]
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
-                    const int oh_base = tc.win * (a.HR - 2) - 1, ow_base = ow0 - 1;
+                    const int oh_base = tc.grow, ow_base = ow0 - 1;
                     const size_t W2o = 2 * (size_t)a.W_out;
                     const size_t row0 = ((size_t)n * a.dout + t) * 2 * (size_t)a.H_out;
                     {
@@ -1111,22 +1199,43 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                         __syncwarp();
                         const int wa = 2 * k + (lane >> 4), wc = lane & 15;
                         const int oh = oh_base + wa, ow = ow_base + wc;
-                        if (wa >= 1 && wa <= 14 && wc >= 1 && wc <= 14 && oh < a.H_out && ow < a.W_out) {
-                            int ro[3];
-#pragma unroll
-                            for (int i = 0; i < 3; ++i) ro[i] = 16 * ((wa + i - 1) & 3) + wc - 1;
+                        const bool col_ok = wc >= 1 && wc <= 14 && ow < a.W_out;
+                        // acc plus the three taps (i, 0..2) of channel 3q + cl at window row r
+                        auto taps = [&](float acc, int cl, int i, int r) -> float {
+                            const float* sp = S + (cl * 9 + i * 3) * kStnPitch + 16 * (r & 3) + wc - 1;
+                            acc += sp[0];
+                            acc += sp[kStnPitch + 1];
+                            acc += sp[2 * kStnPitch + 2];
+                            return acc;
+                        };
+                        auto put = [&](int orow, int cl, float v) {
+                            const int c = 3 * q + cl;
+                            const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
+                            y[((row0 + 2 * (size_t)orow + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
+                                cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, v)));
+                        };
+                        if (col_ok && wa >= 1 && wa <= 14 && oh < a.H_out) {
 #pragma unroll
                             for (int cl = 0; cl < 3; ++cl) {
-                                const int c = 3 * q + cl;
                                 float acc = stn_bias[cl];
 #pragma unroll
-                                for (int i = 0; i < 3; ++i)
+                                for (int i = 0; i < 3; ++i) acc = taps(acc, cl, i, wa + i - 1);
+                                put(oh, cl, acc);
+                            }
+                        }
+                        if (k == 0 && col_ok && wa == 0 && tc.win > 0) {
+                            // the seam rows: centred on the previous window's row 15 (oh - 1) and on row 0
 #pragma unroll
-                                    for (int j = 0; j < 3; ++j)
-                                        acc += S[(cl * 9 + i * 3 + j) * kStnPitch + ro[i] + j];
-                                const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
-                                y[((row0 + 2 * (size_t)oh + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
-                                    cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, acc)));
+                            for (int cl = 0; cl < 3; ++cl) {
+                                if (oh - 1 < a.H_out) put(oh - 1, cl, taps(Cw[cl * 32 + wc], cl, 2, 0));
+                                if (oh < a.H_out) put(oh, cl, taps(taps(Cw[cl * 32 + 16 + wc], cl, 1, 0), cl, 2, 1));
+                            }
+                        }
+                        if (k == kBNP / 32 - 1 && col_ok && wa == 15) {
+#pragma unroll
+                            for (int cl = 0; cl < 3; ++cl) {
+                                Cw[cl * 32 + wc] = taps(taps(stn_bias[cl], cl, 0, 14), cl, 1, 15);
+                                Cw[cl * 32 + 16 + wc] = taps(stn_bias[cl], cl, 0, 15);
                             }
                         }
                         __syncwarp();
@@ -1451,20 +1560,81 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
             }
         }
     }
+    int stn_ctas = 0;
     if (g.stn) {
-        // stencil head: 16 x 16 raster windows (pitch 16, 14 output columns and rows inside one
-        // halo column and row on each side), consecutive windows of a strip two rows apart in overlap
+        // stencil head: 16 x 16 raster windows (pitch 16: one halo column on each side of 14 output
+        // columns). Each CTA runs a stretch of consecutive windows down the strips, every window for
+        // all output frames, the windows of one strip abutting (the seams are joined by row sums the
+        // epilogue carries, one set per output frame)
         g.Wt = 14; g.P = 16; g.HR = 16;
         g.strips = (W_out + 13) / 14;
-        g.windows = (H_out + 13) / 14;
-        g.win_adv = 14 * 16;
+        g.win_adv = 16 * 16;
         g.h_bytes = g.h_tx_bytes = kCtrW + kWBlock;
-        g.n_h = (kSmemLimit - fixed) / g.h_bytes < 4 ? (kSmemLimit - fixed) / g.h_bytes : 4;
+        // frame groups: the fewest frames per CTA (a divisor of the frame count) that leave no more
+        // groups than CTAs
+        const int ctas = num_sms < kStnMaxCtas ? num_sms : kStnMaxCtas;
+        int fpc = 1;
+        while (g.frames % fpc != 0 || g.frames / fpc > ctas) ++fpc;
+        g.stn_fpc = fpc;
+        g.stn_groups = g.frames / fpc;
+        g.x_bytes = 4 * fpc * kStnCarryBytes;
+        const int room = kSmemLimit - fixed - g.x_bytes;
+        g.n_h = room / g.h_bytes < 4 ? room / g.h_bytes : 4;
         g.n_w = 1;
         g.w_smem = 0;
-        g.smem_bytes = fixed + g.n_h * g.h_bytes;
-        if (g.n_h < 2) return false;
-        g.tiles = (long long)g.strips * g.windows * g.frames;
+        g.smem_bytes = fixed + g.x_bytes + g.n_h * g.h_bytes;
+        if (g.n_h < 2 || H_out > 0xFFFF || g.strips > 0xFFFF) return false;
+        // Runs: with at least as many strips as runs, round j of whole strips gives strip r + j R to
+        // run r (R runs side by side on neighbouring strips); the strips left after the whole rounds
+        // (or all of them, with fewer strips than runs) are cut greedily into the fewest windows per run
+        // with which the runs cover them: a run takes whole strip remainders while its windows last
+        // ((rows + 2) / 16 rounded up), else the 16 n - 2 rows its last n windows yield, and the next run
+        // starts below them
+        const int runs_max = ctas / g.stn_groups;
+        const int full = (H_out + 17) >> 4;
+        const bool rounds = g.strips >= runs_max;
+        const int R = rounds ? runs_max : 0;
+        g.stn_full = rounds ? g.strips / runs_max : 0;
+        const int left0 = g.stn_full * R;  // first strip of the greedy part
+        long long windows = (long long)g.stn_full * R * full;
+        int runs = R, nb = 0;
+        if (left0 < g.strips) {
+            for (int n = 1;; ++n) {
+                int st = left0, o = 0, used = 0;
+                long long wsum = 0;
+                for (int c = 0; c < runs_max && st < g.strips; ++c) {
+                    g.stn_start[c] = ((uint32_t)st << 16) | (uint32_t)o;
+                    ++used;
+                    for (int rem = n; rem > 0 && st < g.strips;) {
+                        const int need = (H_out - o + 17) >> 4;
+                        if (need <= rem) {
+                            rem -= need;
+                            wsum += need;
+                            ++st;
+                            o = 0;
+                        } else {
+                            o += 16 * rem - 2;
+                            wsum += rem;
+                            rem = 0;
+                        }
+                    }
+                }
+                if (st >= g.strips) {
+                    nb = n;
+                    windows += wsum;
+                    for (int c = used; c < runs_max; ++c) g.stn_start[c] = (uint32_t)g.strips << 16;
+                    if (!rounds) runs = used;
+                    break;
+                }
+            }
+        } else {
+            for (int c = 0; c < runs_max; ++c) g.stn_start[c] = (uint32_t)g.strips << 16;
+        }
+        g.stn_runs = R;
+        g.stn_n = g.stn_full * full + nb;
+        stn_ctas = runs * g.stn_groups;
+        g.windows = g.stn_n;
+        g.tiles = windows * g.frames;
         found = true;
     } else if (g.ctr) {
         // the centre tap needs no halo: a window is 256 consecutive positions of a frame's flattened
@@ -1580,7 +1750,7 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         }
     }
     if (g.tiles >= (1LL << 31)) return false;  // the kernel decodes tile indices in 32 bits
-    g.grid = (int)(g.tiles < num_sms ? g.tiles : num_sms);
+    g.grid = g.stn ? stn_ctas : (int)(g.tiles < num_sms ? g.tiles : num_sms);
     p->cl = g;
     // the packed weight blocks are the generic packer's layout with BN = 128, CK = 64 (the head form
     // has its own packer: 3 kh blocks per chunk with (kw, channel) rows)
@@ -1604,6 +1774,15 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.stage_warp = g.stage_warp;
     a.tn_cp = g.tn_cp; a.tn_n = g.tn_n; a.x_bytes = g.x_bytes;
     a.row_shift = row_shift;
+    if (g.stn) {
+        a.stn_n = g.stn_n;
+        a.stn_fpc = g.stn_fpc;
+        a.stn_full = g.stn_full;
+        a.stn_runs = g.stn_runs;
+        a.fd_fpc = make_fastdiv((uint32_t)g.stn_fpc);
+        a.fd_groups = make_fastdiv((uint32_t)g.stn_groups);
+        memcpy(a.stn_start, g.stn_start, sizeof a.stn_start);
+    }
     a.frame_inner = g.ctr ? 1 : 0;
     // causal channels-last layers whose passes have an even number of frames: frame pairs, unless
     // X3CONV_FRAME_PAIRS=0 (the tiles and their sums are the same; only the order changes)

@@ -57,6 +57,8 @@ struct IgemmGeom {
 // positions as N: vertical strips Wt columns wide walked as rasters of pitch P = Wt + 2, a tile being
 // a window of 256 consecutive raster positions of one frame; the halo of a window (HR rows of P
 // positions, 64 channels, 128-byte swizzle) is staged once per temporal tap and channel chunk.
+constexpr int kStnMaxCtas = 256;  // stencil head: most CTAs of one launch (one run of windows each)
+
 struct ClGeom {
     int KT, n_chunks, n_tiles;   // temporal taps, 64-channel chunks, 128-channel output tiles
     int Wt, P, HR;               // strip width, raster pitch, halo rows staged per window
@@ -79,9 +81,16 @@ struct ClGeom {
     int tn;                      // 1: positions as M (128 per tile), the three horizontal taps in N
     int tn_cp, tn_n;             // tn: output channels padded to 16; MMA N = 3 * tn_cp (tk: tn_cp)
     int tk;                      // 1 (with tn): 8 input channels, two taps per 16-wide K step
-    int x_bytes;                 // tn: shared memory for the kw-sum exchange and the bias copies
+    int x_bytes;                 // tn: the epilogue warps' bias copies; stn: their row carries
     long long tiles;
     int smem_bytes, grid;
+    // stn: the output frames are split into stn_groups groups of stn_fpc; CTA c runs group c % groups
+    // over run c / groups: stn_n consecutive windows (fewer at the very end), first stn_full whole
+    // strips (run, run + stn_runs, ...), then from strip stn_start[run] >> 16, output row
+    // stn_start[run] & 0xFFFF, down that strip and on from row 0 of the next ones
+    int stn_n, stn_fpc, stn_groups;
+    int stn_full, stn_runs;  // stn: rounds of whole strips per run, and the runs side by side in them
+    uint32_t stn_start[kStnMaxCtas];
 };
 
 }  // namespace x3
