@@ -199,58 +199,78 @@ def _check_sw128_plan(g):
     assert g["tiles"] == g["strips"] * g["windows"] * g["frames"] * g["n_tiles"]
 
 
-def stn_runs(H, strips, n, ctas, s=0):
-    """Greedy runs of n windows over strips s.. for at most `ctas` runs: per run its pieces
-    (strip, first output row, windows), and whether they reach the last strip."""
-    o = 0
-    runs = []
-    for _ in range(ctas):
-        if s >= strips:
-            break
-        pieces, rem = [], n
-        while rem > 0 and s < strips:
-            need = (H - o + 17) // 16
-            if need <= rem:
-                pieces.append((s, o, need))
-                rem -= need
-                s, o = s + 1, 0
-            else:
-                pieces.append((s, o, rem))
-                o += 16 * rem - 2
-                rem = 0
-        runs.append(pieces)
-    return runs, s >= strips
+def stn_segments(H, strips, runs_max):
+    """The stencil head's row segments: with fewer strips than runs each strip is cut into k segments
+    (at least 16 rows each) so that there are about as many segments as runs; part p of strip s is
+    segment p * strips + s. Returns (segment count, rows per segment)."""
+    k = -(-runs_max // strips) if strips < runs_max else 1
+    seg_rows = -(-H // k)
+    if seg_rows < 16:
+        seg_rows = min(H, 16)
+    k = -(-H // seg_rows)
+    return strips * k, seg_rows
 
 
 def stn_plan(H, strips, runs_max):
-    """The stencil head's assignment: with at least as many strips as runs, whole strips in rounds (run
-    r takes r, r + R, ...), then the greedy over the strips left; else the greedy over all strips.
-    Returns per run its pieces and the windows per run (the plan's `windows`)."""
-    full = (H + 17) // 16
-    k = strips // runs_max if strips >= runs_max else 0
-    R = runs_max if k else 0
-    left0 = k * R
-    runs = [[(r + j * R, 0, full) for j in range(k)] for r in range(R)]
-    nb = 0
-    if left0 < strips:
-        nb = 1
-        while not stn_runs(H, strips, nb, runs_max, left0)[1]:
-            nb += 1
-        tail, _ = stn_runs(H, strips, nb, runs_max, left0)
+    """The assignment of 8-row windows to runs: whole segments in rounds (run r takes r, r + R, ...)
+    when there are at least as many segments as runs, then the greedy over the segments left (a run
+    takes segment remainders while its windows last, else the 8 n - 2 rows its last n windows yield).
+    Returns per run its pieces (strip, first output row, windows, segment end) and the windows of the
+    longest run (the plan's `windows`)."""
+    nseg, seg_rows = stn_segments(H, strips, runs_max)
+
+    def bounds(sg):
+        lo = (sg // strips) * seg_rows
+        return sg % strips, lo, min(lo + seg_rows, H)
+
+    full = nseg // runs_max if nseg >= runs_max else 0
+    R = runs_max if full else 0
+    runs = []
+    for r in range(R):
+        pieces = []
+        for j in range(full):
+            st, lo, hi = bounds(r + j * R)
+            pieces.append((st, lo, (hi - lo + 9) // 8, hi))
+        runs.append(pieces)
+    left0 = full * R
+    if left0 < nseg:
+        n = 1
+        while True:
+            sg, o, tail = left0, bounds(left0)[1], []
+            for _ in range(runs_max):
+                if sg >= nseg:
+                    break
+                pieces, rem = [], n
+                while rem > 0 and sg < nseg:
+                    st, lo, hi = bounds(sg)
+                    need = (hi - o + 9) // 8
+                    if need <= rem:
+                        pieces.append((st, o, need, hi))
+                        rem -= need
+                        sg += 1
+                        if sg < nseg:
+                            o = bounds(sg)[1]
+                    else:
+                        pieces.append((st, o, rem, hi))
+                        o += 8 * rem - 2
+                        rem = 0
+                tail.append(pieces)
+            if sg >= nseg:
+                break
+            n += 1
         for r, pieces in enumerate(tail):
             if r < len(runs):
                 runs[r] += pieces
             else:
                 runs.append(pieces)
-    return runs, k * full + nb
+    return runs, max(sum(p[2] for p in r) for r in runs)
 
 
 def _check_stn_runs(g):
     """The runs the plan implies cover every output row of every strip exactly once (a piece of nb
-    windows from row o0 yields rows o0 .. o0 + 16 nb - 3, clipped at the plane), each run by one CTA
-    per frame group (the fewest frames per group that divide the frames and leave no more groups than
-    CTAs), with no more CTAs than SMs; whole strips go in rounds over neighbouring strips when there
-    are at least as many strips as runs."""
+    windows from row o0 stores rows o0 .. o0 + 8 nb - 3, clipped at its segment's end), each run by
+    one CTA per frame group (the fewest frames per group that divide the frames and leave no more groups
+    than CTAs), with no more CTAs than SMs."""
     H, strips, n, F = g["H_out"], g["strips"], g["windows"], g["frames"]
     ctas = min(g["sms"], 256)
     fpc = 1
@@ -261,12 +281,11 @@ def _check_stn_runs(g):
     runs, n_model = stn_plan(H, strips, runs_max)
     assert n == n_model
     assert len(runs) * groups == g["grid"] <= ctas
-    assert g["tiles"] == sum(nb for r in runs for (_, _, nb) in r) * g["frames"]
-    assert all(sum(nb for (_, _, nb) in r) <= n for r in runs)
+    assert g["tiles"] == sum(p[2] for r in runs for p in r) * g["frames"]
     cover = np.zeros((strips, H), np.int32)
     for r in runs:
-        for s, o0, nb in r:
-            cover[s, o0:min(o0 + 16 * nb - 2, H)] += 1
+        for s, o0, nb, hi in r:
+            cover[s, o0:min(o0 + 8 * nb - 2, hi)] += 1
     assert np.all(cover == 1)
 
 
@@ -308,11 +327,11 @@ def test_igemm_plans_cover_their_reads(lib, name):
     try:
         g = x3.conv_plan_describe(p)
         if g.get("stn"):
-            # stencil head: 16 x 16 raster windows (14 output columns), one stage per (kt, chunk)
-            # holding the window (32 KB) and its weight block (16 KB); every CTA runs `windows`
+            # stencil head: 32 x 8 raster windows (30 output columns), one stage per (kt, chunk)
+            # holding the window (32 KB) and its weight block (16 KB); every CTA runs at most `windows`
             # consecutive windows down the strips
-            assert g["P"] == 16 and g["Wt"] == 14 and g["HR"] == 16 and g["win_adv"] == 16 * 16
-            assert g["strips"] * 14 >= g["W_out"]
+            assert g["P"] == 32 and g["Wt"] == 30 and g["HR"] == 8 and g["win_adv"] == 256
+            assert g["strips"] * 30 >= g["W_out"]
             assert g["h_bytes"] == 16 * 16 * 128 + 128 * 64 * 2 and g["smem_bytes"] <= 232448
             _check_stn_runs(g)
             return

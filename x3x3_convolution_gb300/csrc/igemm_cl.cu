@@ -40,6 +40,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <vector>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -62,9 +64,10 @@ constexpr int kStageGenericBytes = 32 * kStagePitch;  // per-warp staging block 
 constexpr int kSPitch = 35;       // head form: fp32 staging row (34 columns + pad) per TMEM lane
 constexpr int kGPitch = 36;       // centre-tap form: fp32 staging row (32 accumulator rows + pad) per position
 constexpr int kStageWarpBytes = 32 * kGPitch * 4;  // per-warp staging block (every form but STN)
-constexpr int kStnPitch = 65;     // STN: fp32 staging row (a ring of four 16-position window rows + pad) per tap row
+constexpr int kStnRows = 8;       // STN: rows of a window (32 positions each: 30 output columns and 2 halo)
+constexpr int kStnPitch = 33;     // STN: fp32 staging row (one 32-position window row + pad) per tap row
 constexpr int kStnStageBytes = 27 * kStnPitch * 4;  // 27 rows: 9 taps x 3 channels
-constexpr int kStnCarryBytes = 3 * 2 * 16 * 4;      // STN: per warp and output frame, two partial rows of 3 channels
+constexpr int kStnCarryBytes = 2 * 3 * 32 * 4;      // STN: per warp and output frame, two pending rows of 3 channels
 
 // Division by a run-time constant d without a division instruction: for 0 <= x < 2^31,
 // x / d == (x * m) >> s with l = ceil(log2 d), s = 31 + l and m = ceil(2^s / d) < 2^32 (Granlund and
@@ -110,8 +113,9 @@ struct ClArgs {
     int row_shift;   // banded mode: the input's first row is the band's upper halo row
     int stn_n;       // STN: windows per run (run blockIdx.x / stn_groups starts at stn_start[run])
     int stn_fpc;     // STN: output frames per CTA (frame group blockIdx.x % stn_groups)
-    int stn_full;    // STN: whole strips per run before its share of the rest (run r: r, r + runs, ...)
-    int stn_runs;    // STN: runs (stn_full > 0: one per strip of each round of whole strips)
+    int stn_full;    // STN: whole segments per run before its share of the rest (run r: r, r + runs, ...)
+    int stn_runs;    // STN: runs side by side in the rounds of whole segments
+    int stn_nseg, stn_seg_rows;  // STN: segments (strip-fastest: part p of strip s is p * strips + s), rows each
     long long tiles;
     FastDiv fd_frames, fd_ntiles, fd_windows, fd_strips, fd_dout, fd_P, fd_chunks;
     FastDiv fd_fpc, fd_groups;  // STN
@@ -127,6 +131,7 @@ struct ClTile {
     int nt, win, strip, fr;
     int grow;   // STN: input row of the window's first row
     int fslot;  // STN: the frame's place in this CTA's frame group
+    int rend;   // STN: end of the window's row segment (its last window computes rows past it: not stored)
 };
 
 // The planner keeps tile counts below 2^31, so the decode runs in 32-bit unsigned arithmetic (a 64-bit
@@ -182,51 +187,61 @@ __device__ __forceinline__ ClTile cl_decode(const ClArgs& a, long long tile) {
 // Stencil head: the k-th tile of this CTA, false past its last. The output frames are split into
 // groups of stn_fpc frames, and the CTAs c of one run (c / groups the same) take the groups c % groups
 // side by side, so that the frames reading the same input frames are computed at the same time and
-// share them through L2. A CTA runs its windows one after another, the frames of its group fastest,
-// first through stn_full whole strips (run r takes strips r, r + runs, ..., so that at any moment the
-// runs are on the same rows of neighbouring strips and the halo columns two strips share are read from
-// DRAM once), then from its start in the remaining strips (strip, first output row o0) down that strip
-// and on from row 0 of the following strips. The windows of one strip in one run do not overlap:
-// window b covers input rows o0 - 1 + 16 b to o0 + 14 + 16 b, and the two output rows centred on the
-// seam between windows b and b + 1 take their first kernel rows from sums the epilogue carries over
-// from window b. A run piece of nb windows so yields output rows o0 .. o0 + 16 nb - 3; the planner lets
-// the next run start at o0 + 16 nb - 2 (its first window re-reads the two rows above).
+// share them through L2. Each strip is cut into row segments (part p of strip s is segment
+// p * strips + s, stn_seg_rows output rows). A CTA runs its windows one after another, the frames of
+// its group fastest, first through stn_full whole segments (run r takes segments r, r + runs, ..., so
+// that at any moment the runs are on the same rows of neighbouring strips and the halo columns two
+// strips share are read from DRAM once), then from its start in the remaining segments (segment,
+// first output row o0) down that segment and on through the following ones. The windows of one
+// segment in one run do not overlap: window b covers input rows o0 - 1 + 8 b to o0 + 6 + 8 b, and the
+// two output rows centred on the seam between windows b and b + 1 take their first kernel rows from
+// sums the epilogue carries over from window b. A piece of nb windows so yields output rows
+// o0 .. o0 + 8 nb - 3 (the next piece starts at o0 + 8 nb - 2 and re-reads the two rows above).
+__device__ __forceinline__ void stn_segment(const ClArgs& a, int sg, int& strip, int& lo, int& hi) {
+    const int part = (int)fdiv((uint32_t)sg, a.fd_strips);
+    strip = sg - part * a.strips;
+    lo = part * a.stn_seg_rows;
+    hi = lo + a.stn_seg_rows < a.H_out ? lo + a.stn_seg_rows : a.H_out;
+}
+
 __device__ __forceinline__ bool stn_decode(const ClArgs& a, long long k, ClTile& c) {
     const uint32_t kk = (uint32_t)k;
     const uint32_t w = fdiv(kk, a.fd_fpc);
     if ((int)w >= a.stn_n) return false;
     const uint32_t run = fdiv(blockIdx.x, a.fd_groups);
     const uint32_t grp = blockIdx.x - run * a.fd_groups.d;
-    const int full = (a.H_out + 17) >> 4;  // windows of a whole strip
-    int s = 0, o = 0, b = (int)w;
-    bool whole = false;
+    int s = 0, lo = 0, hi = 0, b = (int)w, o = -1;
     for (int j = 0; j < a.stn_full; ++j) {
-        if (b < full) {
-            s = (int)run + j * a.stn_runs;
-            whole = true;
+        stn_segment(a, (int)run + j * a.stn_runs, s, lo, hi);
+        const int nwin = (hi - lo + 9) >> 3;
+        if (b < nwin) {
+            o = lo;
             break;
         }
-        b -= full;
+        b -= nwin;
     }
-    if (!whole) {
+    if (o < 0) {
         const uint32_t st = a.stn_start[run];
-        s = (int)(st >> 16);
+        int sg = (int)(st >> 16);
         o = (int)(st & 0xFFFFu);
-    }
-    for (;;) {
-        if (s >= a.strips) return false;
-        const int need = (a.H_out - o + 17) >> 4;  // windows that finish the strip from row o
-        if (b < need) break;
-        b -= need;
-        ++s;
-        o = 0;
+        for (;;) {
+            if (sg >= a.stn_nseg) return false;
+            stn_segment(a, sg, s, lo, hi);
+            if (o < lo) o = lo;
+            const int need = (hi - o + 9) >> 3;  // windows that finish the segment from row o
+            if (b < need) break;
+            b -= need;
+            ++sg;
+            o = 0;
+        }
     }
     c.nt = 0;
     c.fslot = (int)(kk - w * a.fd_fpc.d);
     c.fr = (int)(grp * a.fd_fpc.d) + c.fslot;
     c.strip = s;
     c.win = b;
-    c.grow = o - 1 + 16 * b;
+    c.grow = o - 1 + kStnRows * b;
+    c.rend = hi;
     return true;
 }
 
@@ -1145,100 +1160,72 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     __syncwarp();
                     drain(4);
                 } else if (STN) {
-                    // Window position m = 16a + c holds G at plane row a, column c (row 0 and 15, column 0
-                    // and 15 are halo). The warp stages its 27 rows (9 taps x 3 channels) one window row
-                    // at a time into a ring of four rows, S[lane][16 * (a & 3) + c]: chunk k (outputs in
-                    // window rows 2k and 2k + 1) adds rows 2k + 1 and 2k + 2 to the row 0 and rows up to
-                    // 2k staged before, so every TMEM column is read and staged once. Thread t then sums,
-                    // for output m = 32k + t, bias + the nine taps in (i, j) order at row a + i - 1,
-                    // column c + j - 1. Window row a is centred on output row grow + a; rows 1-14 are
-                    // complete here. At the seam with the next window of the run, chunk 7 leaves in
-                    // shared memory (per output frame) the partial sums, in the same order, of the
-                    // output rows centred on rows 15 (kernel rows i = 0, 1) and 16 (i = 0); chunk 0 of
-                    // that next window finishes them.
+                    // Window position m = 32 r + c holds G at window row r (input row grow + r) and column
+                    // c (input column ow0 - 1 + c; columns 0 and 31 are halo). The warp takes the rows in
+                    // order: it stages row r's 27 TMEM rows (9 taps x 3 channels) in shared memory,
+                    // S[tap row][c], and thread c adds row r's taps of kernel row i at columns c - 1 ..
+                    // c + 1 (j = 0, 1, 2) to the sums of three output rows pending in registers: i = 2 to
+                    // output row grow + r - 1, which is then complete, i = 1 to grow + r, and i = 0, after
+                    // the bias, to grow + r + 1. Every output so sums bias and the nine taps in (i, j)
+                    // order. The two sums still pending after the last row stay in shared memory (per
+                    // output frame) for the next window of the run; the first window of a run piece
+                    // starts them afresh and stores from its third row on.
                     float* S = reinterpret_cast<float*>(stage_ptr + ew * a.stage_warp);  // [27][kStnPitch]
                     float* Cw = reinterpret_cast<float*>(sbase + (sBiasT - base)) +
-                                (size_t)(ew * a.stn_fpc + tc.fslot) * (kStnCarryBytes / 4);  // [3][2][16]
+                                (size_t)(ew * a.stn_fpc + tc.fslot) * (kStnCarryBytes / 4);  // [2][3][32]
                     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
-                    const int oh_base = tc.grow, ow_base = ow0 - 1;
+                    const int ow = ow0 - 1 + lane;
+                    const bool col_ok = lane >= 1 && lane <= 30 && ow < a.W_out;
                     const size_t W2o = 2 * (size_t)a.W_out;
                     const size_t row0 = ((size_t)n * a.dout + t) * 2 * (size_t)a.H_out;
-                    {
-                        uint32_t v[16];
-                        ptx::tmem_ld16(tq, v);  // window row 0
+                    const bool first = tc.win == 0;
+                    float pa[3], pb[3];  // pending sums of output rows grow + r - 1 and grow + r
+#pragma unroll
+                    for (int cl = 0; cl < 3; ++cl) {
+                        pa[cl] = (!first && col_ok) ? Cw[cl * 32 + lane] : 0.0f;
+                        pb[cl] = (!first && col_ok) ? Cw[(3 + cl) * 32 + lane] : 0.0f;
+                    }
+                    uint32_t vn[32];
+                    ptx::tmem_ld32(tq, vn);  // window row 0
+                    for (int r = 0; r < kStnRows; ++r) {
                         ptx::tmem_ld_wait();
                         if (lane < 27) {
 #pragma unroll
-                            for (int x = 0; x < 16; ++x) S[lane * kStnPitch + x] = __uint_as_float(v[x]);
+                            for (int x = 0; x < 32; ++x) S[lane * kStnPitch + x] = __uint_as_float(vn[x]);
                         }
-                    }
-                    for (int k = 0; k < kBNP / 32; ++k) {
-                        if (k < kBNP / 32 - 1) {
-                            uint32_t v[32];
-                            ptx::tmem_ld32(tq + (uint32_t)(32 * k + 16), v);  // window rows 2k + 1, 2k + 2
-                            ptx::tmem_ld_wait();
-                            if (lane < 27) {
-                                float* s1 = S + lane * kStnPitch + 16 * ((2 * k + 1) & 3);
-                                float* s2 = S + lane * kStnPitch + 16 * ((2 * k + 2) & 3);
+                        if (r + 1 < kStnRows) ptx::tmem_ld32(tq + (uint32_t)(32 * (r + 1)), vn);  // in flight meanwhile
+                        __syncwarp();
+                        if (col_ok) {
+                            const int orow = tc.grow + r - 1;  // the output row completed by window row r
+                            const bool store = !(first && r < 2) && orow < tc.rend;
 #pragma unroll
-                                for (int x = 0; x < 16; ++x) {
-                                    s1[x] = __uint_as_float(v[x]);
-                                    s2[x] = __uint_as_float(v[16 + x]);
+                            for (int cl = 0; cl < 3; ++cl) {
+                                const float* sp = S + (cl * 9) * kStnPitch + lane - 1;
+                                float sa = pa[cl], sb = pb[cl], sc = stn_bias[cl];
+#pragma unroll
+                                for (int j = 0; j < 3; ++j) sa += sp[(6 + j) * kStnPitch + j];
+#pragma unroll
+                                for (int j = 0; j < 3; ++j) sb += sp[(3 + j) * kStnPitch + j];
+#pragma unroll
+                                for (int j = 0; j < 3; ++j) sc += sp[j * kStnPitch + j];
+                                if (store) {
+                                    const int c = 3 * q + cl;
+                                    const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
+                                    y[((row0 + 2 * (size_t)orow + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
+                                        cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, sa)));
                                 }
-                            }
-                        } else {
-                            uint32_t v[16];
-                            ptx::tmem_ld16(tq + (uint32_t)(32 * k + 16), v);  // window row 15 (the last)
-                            ptx::tmem_ld_wait();
-                            if (lane < 27) {
-                                float* s1 = S + lane * kStnPitch + 16 * ((2 * k + 1) & 3);
-#pragma unroll
-                                for (int x = 0; x < 16; ++x) s1[x] = __uint_as_float(v[x]);
+                                pa[cl] = sb;
+                                pb[cl] = sc;
                             }
                         }
                         __syncwarp();
-                        const int wa = 2 * k + (lane >> 4), wc = lane & 15;
-                        const int oh = oh_base + wa, ow = ow_base + wc;
-                        const bool col_ok = wc >= 1 && wc <= 14 && ow < a.W_out;
-                        // acc plus the three taps (i, 0..2) of channel 3q + cl at window row r
-                        auto taps = [&](float acc, int cl, int i, int r) -> float {
-                            const float* sp = S + (cl * 9 + i * 3) * kStnPitch + 16 * (r & 3) + wc - 1;
-                            acc += sp[0];
-                            acc += sp[kStnPitch + 1];
-                            acc += sp[2 * kStnPitch + 2];
-                            return acc;
-                        };
-                        auto put = [&](int orow, int cl, float v) {
-                            const int c = 3 * q + cl;
-                            const int rgb = c >> 2, dy = (c >> 1) & 1, dx = c & 1;
-                            y[((row0 + 2 * (size_t)orow + dy) * W2o + 2 * (size_t)ow + dx) * 3 + rgb] =
-                                cl_round<BF16>(fminf(act_hi, fmaxf(act_lo, v)));
-                        };
-                        if (col_ok && wa >= 1 && wa <= 14 && oh < a.H_out) {
+                    }
+                    if (col_ok) {
 #pragma unroll
-                            for (int cl = 0; cl < 3; ++cl) {
-                                float acc = stn_bias[cl];
-#pragma unroll
-                                for (int i = 0; i < 3; ++i) acc = taps(acc, cl, i, wa + i - 1);
-                                put(oh, cl, acc);
-                            }
+                        for (int cl = 0; cl < 3; ++cl) {
+                            Cw[cl * 32 + lane] = pa[cl];
+                            Cw[(3 + cl) * 32 + lane] = pb[cl];
                         }
-                        if (k == 0 && col_ok && wa == 0 && tc.win > 0) {
-                            // the seam rows: centred on the previous window's row 15 (oh - 1) and on row 0
-#pragma unroll
-                            for (int cl = 0; cl < 3; ++cl) {
-                                if (oh - 1 < a.H_out) put(oh - 1, cl, taps(Cw[cl * 32 + wc], cl, 2, 0));
-                                if (oh < a.H_out) put(oh, cl, taps(taps(Cw[cl * 32 + 16 + wc], cl, 1, 0), cl, 2, 1));
-                            }
-                        }
-                        if (k == kBNP / 32 - 1 && col_ok && wa == 15) {
-#pragma unroll
-                            for (int cl = 0; cl < 3; ++cl) {
-                                Cw[cl * 32 + wc] = taps(taps(stn_bias[cl], cl, 0, 14), cl, 1, 15);
-                                Cw[cl * 32 + 16 + wc] = taps(stn_bias[cl], cl, 0, 15);
-                            }
-                        }
-                        __syncwarp();
                     }
                 } else if (CTR) {
                     // Temporal pass of the split head: accumulator row r = (i*3+j)*12 + c goes to plane
@@ -1562,13 +1549,13 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
     }
     int stn_ctas = 0;
     if (g.stn) {
-        // stencil head: 16 x 16 raster windows (pitch 16: one halo column on each side of 14 output
+        // stencil head: 32 x 8 raster windows (pitch 32: one halo column on each side of 30 output
         // columns). Each CTA runs a stretch of consecutive windows down the strips, every window for
-        // all output frames, the windows of one strip abutting (the seams are joined by row sums the
-        // epilogue carries, one set per output frame)
-        g.Wt = 14; g.P = 16; g.HR = 16;
-        g.strips = (W_out + 13) / 14;
-        g.win_adv = 16 * 16;
+        // the output frames of its group, the windows of one strip abutting (the seams are joined by
+        // row sums the epilogue carries, one set per output frame)
+        g.Wt = 30; g.P = 32; g.HR = kStnRows;
+        g.strips = (W_out + 29) / 30;
+        g.win_adv = kBNP;
         g.h_bytes = g.h_tx_bytes = kCtrW + kWBlock;
         // frame groups: the fewest frames per CTA (a divisor of the frame count) that leave no more
         // groups than CTAs
@@ -1584,54 +1571,88 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         g.w_smem = 0;
         g.smem_bytes = fixed + g.x_bytes + g.n_h * g.h_bytes;
         if (g.n_h < 2 || H_out > 0xFFFF || g.strips > 0xFFFF) return false;
-        // Runs: with at least as many strips as runs, round j of whole strips gives strip r + j R to
-        // run r (R runs side by side on neighbouring strips); the strips left after the whole rounds
-        // (or all of them, with fewer strips than runs) are cut greedily into the fewest windows per run
-        // with which the runs cover them: a run takes whole strip remainders while its windows last
-        // ((rows + 2) / 16 rounded up), else the 16 n - 2 rows its last n windows yield, and the next run
-        // starts below them
+        // Segments: with fewer strips than runs, each strip is cut into k row segments so that there
+        // are about as many segments as runs (segments at least 16 rows). Runs: with at least as many
+        // segments as runs, round j of whole segments gives segment r + j R to run r (R runs side by
+        // side: neighbouring strips, same rows); the segments left after the whole rounds (or all of
+        // them) are cut greedily into the fewest windows per run with which the runs cover them: a run
+        // takes whole segment remainders while its windows last ((rows + 2) / 8 rounded up), else the
+        // 8 n - 2 rows its last n windows yield, and the next run starts below them
         const int runs_max = ctas / g.stn_groups;
-        const int full = (H_out + 17) >> 4;
-        const bool rounds = g.strips >= runs_max;
+        int k = g.strips < runs_max ? (runs_max + g.strips - 1) / g.strips : 1;
+        int seg_rows = (H_out + k - 1) / k;
+        if (seg_rows < 16) seg_rows = H_out < 16 ? H_out : 16;
+        k = (H_out + seg_rows - 1) / seg_rows;
+        const int nseg = g.strips * k;
+        if (nseg > 0xFFFF) return false;
+        auto seg_bounds = [&](int sg, int& lo, int& hi) {
+            lo = (sg / g.strips) * seg_rows;
+            hi = lo + seg_rows < H_out ? lo + seg_rows : H_out;
+        };
+        const bool rounds = nseg >= runs_max;
         const int R = rounds ? runs_max : 0;
-        g.stn_full = rounds ? g.strips / runs_max : 0;
-        const int left0 = g.stn_full * R;  // first strip of the greedy part
-        long long windows = (long long)g.stn_full * R * full;
-        int runs = R, nb = 0;
-        if (left0 < g.strips) {
+        g.stn_full = rounds ? nseg / runs_max : 0;
+        const int left0 = g.stn_full * R;  // first segment of the greedy part
+        long long windows = 0;
+        std::vector<int> per_run(runs_max, 0);
+        for (int r = 0; r < R; ++r)
+            for (int j = 0; j < g.stn_full; ++j) {
+                int lo, hi;
+                seg_bounds(r + j * R, lo, hi);
+                per_run[r] += (hi - lo + 9) >> 3;
+            }
+        for (int r = 0; r < R; ++r) windows += per_run[r];
+        int runs = R;
+        if (left0 < nseg) {
             for (int n = 1;; ++n) {
-                int st = left0, o = 0, used = 0;
+                int sg = left0, o = 0, used = 0;
                 long long wsum = 0;
-                for (int c = 0; c < runs_max && st < g.strips; ++c) {
-                    g.stn_start[c] = ((uint32_t)st << 16) | (uint32_t)o;
+                {
+                    int lo, hi;
+                    seg_bounds(sg, lo, hi);
+                    o = lo;
+                }
+                std::vector<int> add(runs_max, 0);
+                for (int c = 0; c < runs_max && sg < nseg; ++c) {
+                    g.stn_start[c] = ((uint32_t)sg << 16) | (uint32_t)o;
                     ++used;
-                    for (int rem = n; rem > 0 && st < g.strips;) {
-                        const int need = (H_out - o + 17) >> 4;
+                    for (int rem = n; rem > 0 && sg < nseg;) {
+                        int lo, hi;
+                        seg_bounds(sg, lo, hi);
+                        const int need = (hi - o + 9) >> 3;
                         if (need <= rem) {
                             rem -= need;
                             wsum += need;
-                            ++st;
-                            o = 0;
+                            add[c] += need;
+                            ++sg;
+                            if (sg < nseg) {
+                                seg_bounds(sg, lo, hi);
+                                o = lo;
+                            }
                         } else {
-                            o += 16 * rem - 2;
+                            o += kStnRows * rem - 2;
                             wsum += rem;
+                            add[c] += rem;
                             rem = 0;
                         }
                     }
                 }
-                if (st >= g.strips) {
-                    nb = n;
+                if (sg >= nseg) {
                     windows += wsum;
-                    for (int c = used; c < runs_max; ++c) g.stn_start[c] = (uint32_t)g.strips << 16;
+                    for (int c = 0; c < runs_max; ++c) per_run[c] += add[c];
+                    for (int c = used; c < runs_max; ++c) g.stn_start[c] = (uint32_t)nseg << 16;
                     if (!rounds) runs = used;
                     break;
                 }
             }
         } else {
-            for (int c = 0; c < runs_max; ++c) g.stn_start[c] = (uint32_t)g.strips << 16;
+            for (int c = 0; c < runs_max; ++c) g.stn_start[c] = (uint32_t)nseg << 16;
         }
         g.stn_runs = R;
-        g.stn_n = g.stn_full * full + nb;
+        g.stn_nseg = nseg;
+        g.stn_seg_rows = seg_rows;
+        g.stn_n = 0;
+        for (int r = 0; r < runs_max; ++r) g.stn_n = per_run[r] > g.stn_n ? per_run[r] : g.stn_n;
         stn_ctas = runs * g.stn_groups;
         g.windows = g.stn_n;
         g.tiles = windows * g.frames;
@@ -1779,6 +1800,8 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
         a.stn_fpc = g.stn_fpc;
         a.stn_full = g.stn_full;
         a.stn_runs = g.stn_runs;
+        a.stn_nseg = g.stn_nseg;
+        a.stn_seg_rows = g.stn_seg_rows;
         a.fd_fpc = make_fastdiv((uint32_t)g.stn_fpc);
         a.fd_groups = make_fastdiv((uint32_t)g.stn_groups);
         memcpy(a.stn_start, g.stn_start, sizeof a.stn_start);

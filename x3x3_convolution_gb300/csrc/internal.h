@@ -85,11 +85,12 @@ struct ClGeom {
     long long tiles;
     int smem_bytes, grid;
     // stn: the output frames are split into stn_groups groups of stn_fpc; CTA c runs group c % groups
-    // over run c / groups: stn_n consecutive windows (fewer at the very end), first stn_full whole
-    // strips (run, run + stn_runs, ...), then from strip stn_start[run] >> 16, output row
-    // stn_start[run] & 0xFFFF, down that strip and on from row 0 of the next ones
+    // over run c / groups: at most stn_n consecutive windows, first stn_full whole row segments (run,
+    // run + stn_runs, ...), then from segment stn_start[run] >> 16, output row stn_start[run] & 0xFFFF,
+    // down that segment and on through the next ones
     int stn_n, stn_fpc, stn_groups;
-    int stn_full, stn_runs;  // stn: rounds of whole strips per run, and the runs side by side in them
+    int stn_full, stn_runs;  // stn: rounds of whole segments per run, and the runs side by side in them
+    int stn_nseg, stn_seg_rows;  // stn: row segments (part p of strip s is p * strips + s) and rows each
     uint32_t stn_start[kStnMaxCtas];
 };
 
