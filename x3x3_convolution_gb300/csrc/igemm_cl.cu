@@ -333,11 +333,12 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
 // halo is staged by one box; each weight K slice feeds an MMA for the first window and then one for
 // the second, which re-uses the A operand it just fetched, the two accumulators filling all 512 TMEM
 // columns (so the epilogue no longer overlaps the MMAs).
-// STN (with CTR; the conv_out head in one pass): the centre-tap MMAs over a 16 x 16 raster window
-// (one halo column and row on each side of 14 x 14 outputs; windows overlap by two rows), M rows
+// STN (with CTR; the conv_out head in one pass): the centre-tap MMAs over 32 x 8 raster windows (one
+// halo column on each side of 30 output columns) that abut down a strip segment (stn_decode), M rows
 // 32q + 9cl + tap for channel 3q + cl, so each epilogue warp holds all nine taps of its three channels;
-// the epilogue adds, in fp32, the bias and the nine taps' values at the shifted window positions
-// (staged through shared memory), clamps, rounds once and writes the unpatchified RGB pixels.
+// the epilogue streams the window's rows through shared memory and adds, in fp32, the bias and the
+// nine taps' values at the shifted positions into the output rows pending in registers, then clamps,
+// rounds once and writes the unpatchified RGB pixels.
 // S2 (2D channels-last, stride 2): the raster is the output plane (pitch Wt + 1) and the input is
 // staged as its four phases, even or odd rows by even or odd columns, each box loaded by the TMA
 // unit with element strides of 2. A phase is one pipeline group that feeds only the taps reading it
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                             ptx::mbar_arrive_expect_tx(bar_h_full + 8 * sh, (uint32_t)a.h_tx_bytes);
                             if (CTR) {
                                 // 256 consecutive positions of the frame's flattened plane (STN: the
-                                // 16 x 16 raster window) and the (kt, chunk) weight block, one stage
+                                // 32 x 8 raster window) and the (kt, chunk) weight block, one stage
                                 // and one barrier for both
                                 if (STN)
                                     ptx::tma_load_4d(sH + sh * a.h_bytes, map, bar_h_full + 8 * sh, cc * kCK, ow0 - 1,
