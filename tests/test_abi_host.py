@@ -205,6 +205,8 @@ def stn_segments(H, strips, runs_max):
     segment p * strips + s. Returns (segment count, rows per segment)."""
     k = -(-runs_max // strips) if strips < runs_max else 1
     seg_rows = -(-H // k)
+    if k > 1:
+        seg_rows += (6 - seg_rows % 8) % 8  # rows + 2 a multiple of 8: the windows fill exactly
     if seg_rows < 16:
         seg_rows = min(H, 16)
     k = -(-H // seg_rows)
@@ -233,36 +235,38 @@ def stn_plan(H, strips, runs_max):
             pieces.append((st, lo, (hi - lo + 9) // 8, hi))
         runs.append(pieces)
     left0 = full * R
+    whole = [sum(p[2] for p in r) for r in runs] + [0] * (runs_max - len(runs))
     if left0 < nseg:
-        n = 1
+        T = max(whole)
         while True:
-            sg, o, tail = left0, bounds(left0)[1], []
-            for _ in range(runs_max):
-                if sg >= nseg:
-                    break
-                pieces, rem = [], n
+            sg, o, tail = left0, bounds(left0)[1], [[] for _ in range(runs_max)]
+            for c in range(runs_max):
+                cap = T - whole[c]
+                if sg >= nseg or cap <= 0:
+                    continue
+                rem = cap
                 while rem > 0 and sg < nseg:
                     st, lo, hi = bounds(sg)
                     need = (hi - o + 9) // 8
                     if need <= rem:
-                        pieces.append((st, o, need, hi))
+                        tail[c].append((st, o, need, hi))
                         rem -= need
                         sg += 1
                         if sg < nseg:
                             o = bounds(sg)[1]
                     else:
-                        pieces.append((st, o, rem, hi))
+                        tail[c].append((st, o, rem, hi))
                         o += 8 * rem - 2
                         rem = 0
-                tail.append(pieces)
             if sg >= nseg:
                 break
-            n += 1
-        for r, pieces in enumerate(tail):
-            if r < len(runs):
-                runs[r] += pieces
+            T += 1
+        used = max((c + 1 for c in range(runs_max) if tail[c]), default=0)
+        for c in range(max(used, len(runs))):
+            if c < len(runs):
+                runs[c] += tail[c]
             else:
-                runs.append(pieces)
+                runs.append(tail[c])
     return runs, max(sum(p[2] for p in r) for r in runs)
 
 

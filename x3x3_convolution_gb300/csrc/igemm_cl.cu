@@ -1582,6 +1582,8 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
         const int runs_max = ctas / g.stn_groups;
         int k = g.strips < runs_max ? (runs_max + g.strips - 1) / g.strips : 1;
         int seg_rows = (H_out + k - 1) / k;
+        // a segment of rows + 2 = 8 n input rows fills its windows exactly
+        if (k > 1) seg_rows += (6 - seg_rows % 8 + 8) % 8;
         if (seg_rows < 16) seg_rows = H_out < 16 ? H_out : 16;
         k = (H_out + seg_rows - 1) / seg_rows;
         const int nseg = g.strips * k;
@@ -1603,9 +1605,13 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
                 per_run[r] += (hi - lo + 9) >> 3;
             }
         for (int r = 0; r < R; ++r) windows += per_run[r];
+        // the segments left after the whole rounds: the smallest window count T per run with which
+        // the runs, each taking up to T minus its whole-segment windows, cover them greedily
         int runs = R;
+        int T = 0;
+        for (int r = 0; r < runs_max; ++r) T = per_run[r] > T ? per_run[r] : T;
         if (left0 < nseg) {
-            for (int n = 1;; ++n) {
+            for (;; ++T) {
                 int sg = left0, o = 0, used = 0;
                 long long wsum = 0;
                 {
@@ -1615,9 +1621,14 @@ bool igemm_cl_plan(x3_conv_plan* p, int num_sms, bool small_cout) {
                 }
                 std::vector<int> add(runs_max, 0);
                 for (int c = 0; c < runs_max && sg < nseg; ++c) {
+                    const int cap = T - per_run[c];
+                    if (cap <= 0) {
+                        g.stn_start[c] = (uint32_t)nseg << 16;
+                        continue;
+                    }
                     g.stn_start[c] = ((uint32_t)sg << 16) | (uint32_t)o;
-                    ++used;
-                    for (int rem = n; rem > 0 && sg < nseg;) {
+                    used = c + 1;
+                    for (int rem = cap; rem > 0 && sg < nseg;) {
                         int lo, hi;
                         seg_bounds(sg, lo, hi);
                         const int need = (hi - o + 9) >> 3;
