@@ -580,3 +580,20 @@ def test_band_plans_do_not_chain(lib):
     finally:
         x3.conv_plan_destroy(a)
         x3.conv_plan_destroy(b)
+
+
+def test_stencil_head_runs_random_planes(lib):
+    """60 seeded random head planes (1 to 2000 rows, 1 to 4000 columns, 1 to 8 frames, batch 1 to 3):
+    every plan's runs cover each output row of each strip exactly once and agree with the model."""
+    rng = np.random.default_rng(8100)
+    for _ in range(60):
+        H, W = int(rng.integers(1, 2001)), int(rng.integers(1, 4001))
+        D, N = int(rng.integers(1, 9)), int(rng.integers(1, 4))
+        d = x3.make_desc(3, N, 256, 12, H, W, D=D, act="clamp", unpatchify2x2=True, kernel="head_stencil")
+        p = x3.conv_plan_create(d)
+        try:
+            g = x3.conv_plan_describe(p)
+        finally:
+            x3.conv_plan_destroy(p)
+        assert g["stn"] == 1, (H, W, D, N)
+        _check_stn_runs(g)
