@@ -156,12 +156,14 @@ def run_head(x, carry, L, kernel):
     return host_values(y, "bf16"), conv
 
 
-@pytest.mark.parametrize("shape", SHAPES + [(2, 15, 29), (1, 28, 14)], ids=str)
+@pytest.mark.parametrize("shape", SHAPES + [(2, 15, 29), (1, 28, 14), (2, 7, 31), (1, 6, 30), (2, 23, 61),
+                                            (1, 14, 60)], ids=str)
 @pytest.mark.parametrize("variant", ["int", "sparse1", "random"])
 def test_stencil_head(variant, shape):
     """The head in one kernel with the spatial stencil in the epilogue: exact on integer data against
     the oracle's single-pass head, and bit for bit the split form's values (same fp32 sums in the same
-    order) on random data; shapes around the 14 x 14 window interiors."""
+    order) on random data; shapes around the 30-column strips and 8-row windows (a column past a
+    strip, exactly one or two strips, heights that fill their last window exactly or by one row)."""
     D, H, W = shape
     x, carry, L = synth.head(D=D, H=H, W=W, variant=variant, seed=3800 + H + W)
     got, conv = run_head(x, carry, L, "head_stencil")
