@@ -491,12 +491,11 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     } else {
                         kt = (int)fdiv((uint32_t)gi, a.fd_chunks);
                         cc = gi - kt * a.n_chunks;
-                        // centre-tap forms: the last output frame of a pass takes its temporal taps in
-                        // the order 1, 2, 0, so that its tiles, the only ones that read the pass's last
-                        // input frame, start on a frame that the other frames' tiles read at the same
-                        // time (measured: the stencil head 1.5 % faster). Both the stencil head and the
-                        // split head's temporal pass do it, so that their fp32 sums keep one order.
-                        if (CTR && a.KT == 3 && a.dout >= 3 && t == a.dout - 1) kt = kt == 2 ? 0 : kt + 1;
+                        // centre-tap forms: the temporal taps in the order 1, 2, 0 (measured on the
+                        // stencil head at 4 + 2 frames: 0.1476 ms against 0.1511 in the order 0, 1, 2, the
+                        // order 2, 0, 1 as fast; same box). The stencil head and the split head's temporal
+                        // pass take the same order, so that their fp32 sums stay bit for bit equal.
+                        if (CTR && a.KT == 3) kt = kt == 2 ? 0 : kt + 1;
                     }
                     const void* map = &tm_x;
                     int fcoord;
