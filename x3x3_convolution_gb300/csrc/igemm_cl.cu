@@ -99,7 +99,6 @@ struct ClArgs {
     int win_adv;     // raster positions between consecutive windows (256, or 254 when kw is folded into M)
     int raw_w, raw_bytes, raw_tx_bytes, n_raw;  // NCHW: raw tile columns, stage bytes, TMA bytes, stages
     int ngroups;     // kw folded into M: channel groups (10 channels x 3 kw per TMEM lane quarter)
-    int ctr;         // 1: centre spatial tap only (the temporal pass of the two-pass head)
     int sub2;        // 1: stride 2 as the stride-1 raster with only even (oh, ow) stored at (oh/2, ow/2)
     int out_nchw;    // 1: channels-last input, NCHW output (the NCHW epilogue)
     int yH, yW;      // stored output plane (H_out x W_out, or halved when sub2)
@@ -1837,7 +1836,7 @@ x3_status launch_cl(const x3_conv_desc& d, const ClGeom& g, int H_out, int W_out
     a.KT = g.KT; a.n_chunks = g.n_chunks; a.n_tiles = g.n_tiles; a.Wt = g.Wt; a.P = g.P; a.HR = g.HR;
     a.strips = g.strips; a.windows = g.windows; a.frames = g.frames; a.h_bytes = g.h_bytes;
     a.h_tx_bytes = g.h_tx_bytes; a.n_h = g.n_h; a.n_w = g.n_w; a.tiles = g.tiles;
-    a.win_adv = g.win_adv; a.ngroups = g.ngroups; a.ctr = g.ctr;
+    a.win_adv = g.win_adv; a.ngroups = g.ngroups;
     a.raw_w = g.raw_w; a.raw_bytes = g.raw_bytes; a.raw_tx_bytes = g.raw_tx_bytes; a.n_raw = g.n_raw;
     a.idesc = g.tn ? ptx::idesc_f16(kBM, g.tn_n, bf16) : ptx::idesc_f16(g.m64 ? 64 : kBM, kBNP, bf16);
     a.fd_frames = make_fastdiv((uint32_t)g.frames);
