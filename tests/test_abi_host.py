@@ -85,6 +85,46 @@ def test_invalid_descriptors_rejected(lib, name):
     assert x3.conv_last_error() != ""
 
 
+LIMITS = [  # (descriptor changes, accepted) around the boundary's size limits
+    (dict(H=32768, W=32768), True),                  # a plane of 2^30 positions
+    (dict(H=32768, W=32769), False),
+    (dict(C_in=65536), True),
+    (dict(C_in=65537), False),
+    (dict(C_out=65536), True),
+    (dict(C_out=65537), False),
+    (dict(N=1 << 30, H=1, W=1), True),               # 2^30 frames
+    (dict(N=(1 << 30) + 1, H=1, W=1), False),
+    (dict(dims=3, layout="NDHWC", dtype="bf16", D=(1 << 30) - 2, H=1, W=1), True),  # N (D + 2) = 2^30
+    (dict(dims=3, layout="NDHWC", dtype="bf16", D=(1 << 30) - 1, H=1, W=1), False),
+]
+
+
+@pytest.mark.parametrize("i", range(len(LIMITS)))
+def test_size_limits(lib, i):
+    """Tensors up to the limits plan; one step past a limit is X3_ERR_INVALID ("tensor too large")."""
+    kw = dict(dims=2, N=1, C_in=16, C_out=16, H=8, W=8, layout="NCHW", dtype="f16")
+    change, ok = LIMITS[i]
+    kw.update(change)
+    st = _status(x3.make_desc(**kw))
+    if ok:
+        assert st == x3.X3_OK, x3.conv_last_error()
+    else:
+        assert st == x3.X3_ERR_INVALID and "too large" in x3.conv_last_error()
+
+
+@pytest.mark.parametrize("H,kernel", [(65535, "igemm_tcgen05_sw128_head_stencil"),
+                                      (65536, "igemm_tcgen05_sw128_head")])
+def test_head_rows_past_the_stencil_limit(lib, H, kernel):
+    """The stencil head keeps output rows in 16 bits: 65535 rows plan it, one more goes to the
+    single-pass head."""
+    p = x3.conv_plan_create(x3.make_desc(3, 1, 256, 12, H, 64, D=3, layout="NDHWC", dtype="bf16", act="clamp",
+                                         unpatchify2x2=True))
+    try:
+        assert x3.conv_plan_kernel_name(p) == kernel
+    finally:
+        x3.conv_plan_destroy(p)
+
+
 def test_forced_igemm_unsupported_is_reported(lib):
     d = x3.make_desc(2, 1, 16, 16, 9, 9, layout="NCHW", dtype="f16", kernel="igemm")  # W % 8 != 0
     assert _status(d) == x3.X3_ERR_UNSUPPORTED
