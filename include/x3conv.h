@@ -246,8 +246,8 @@ size_t conv_stack_workspace_bytes(const x3_conv_plan* const* plans, int n_layers
  *   carry_valid: 0 on the first pass of a sequence, 1 afterwards.
  *   w_packed[i], bias[i]: as for conv_forward with plans[i].
  *   workspace:   >= conv_stack_workspace_bytes(plans, n_layers) bytes, 256-byte aligned.
- * Errors: X3_ERR_INVALID (mismatched layers, NULL pointers), X3_ERR_OOM (workspace too small),
- * X3_ERR_CUDA.
+ * Errors: X3_ERR_INVALID (n_layers < 1, mismatched layers, NULL pointers), X3_ERR_OOM (workspace
+ * too small), X3_ERR_CUDA.
  */
 x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, const void* x,
                              void* const* carries, int carry_valid, const void* const* w_packed,

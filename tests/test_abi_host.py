@@ -147,6 +147,14 @@ def test_forward_null_pointers_rejected_without_launch(lib):
         x3.conv_plan_destroy(p)
 
 
+def test_empty_stack_rejected(lib):
+    for fn in (lib.conv_stack_forward, lib.conv_stack_forward_noalloc):
+        assert fn(None, 0, 16, None, 0, None, None, 256, *((None, 0) if fn is lib.conv_stack_forward else ()),
+                  None) == x3.X3_ERR_INVALID
+        assert "layers" in x3.conv_last_error()
+    assert lib.conv_stack_workspace_bytes(None, 0) == 0
+
+
 def test_stack_validation(lib):
     a = x3.conv_plan_create(x3.make_desc(3, 1, 16, 32, 8, 8, D=2))
     b = x3.conv_plan_create(x3.make_desc(3, 1, 16, 8, 8, 8, D=2))   # C_in 16 != 32

@@ -489,7 +489,8 @@ x3_status conv_stack_forward(const x3_conv_plan* const* plans, int n_layers, con
                              int carry_valid, const void* const* w_packed, const void* const* bias, void* y,
                              void* workspace, size_t workspace_bytes, x3_stream_t stream) {
     clear_err();
-    if (!plans || n_layers < 1 || !x || !y || !w_packed || (!bias && n_layers > 0 && plans[0] && plans[0]->d.has_bias))
+    if (n_layers < 1) return fail(X3_ERR_INVALID, "conv_stack_forward: n_layers must be at least 1 (got %d)", n_layers);
+    if (!plans || !x || !y || !w_packed || (!bias && plans[0] && plans[0]->d.has_bias))
         return fail(X3_ERR_INVALID, "conv_stack_forward: NULL argument");
     for (int i = 0; i < n_layers; ++i) {
         if (!plans[i] || !w_packed[i]) return fail(X3_ERR_INVALID, "conv_stack_forward: layer %d plan or weights NULL", i);
