@@ -125,6 +125,42 @@ def test_head_rows_past_the_stencil_limit(lib, H, kernel):
         x3.conv_plan_destroy(p)
 
 
+def test_plan_creation_from_threads(lib):
+    """Eight threads create and destroy plans at once (ctypes releases the GIL during each call), half of
+    them from descriptors that fail with a message naming the thread's own numbers: every status is
+    right, every thread reads back its own last error (thread-local), and a success clears it."""
+    import ctypes
+    import threading
+
+    failures = []
+
+    def worker(i):
+        try:
+            for k in range(200):
+                plan = ctypes.c_void_p()
+                if (i + k) % 2:
+                    d = x3.make_desc(2, 1, 16, 16, 8, 8 + i, layout="NCHW", dtype="f16")
+                    assert lib.conv_plan_create(ctypes.byref(d), ctypes.byref(plan)) == x3.X3_OK
+                    assert plan.value and x3.conv_last_error() == ""
+                    x3.conv_plan_destroy(plan.value)
+                else:
+                    d = x3.make_desc(2, 1, 16, 16, 8, 8, layout="NCHW", dtype="f16",
+                                     band_lo=0, band_rows=200 + i, H_global=100 + i)
+                    assert lib.conv_plan_create(ctypes.byref(d), ctypes.byref(plan)) == x3.X3_ERR_INVALID
+                    assert not plan.value
+                    want = f"band [0, {200 + i}) is not inside the {100 + i}-row image"
+                    assert want in x3.conv_last_error(), (i, x3.conv_last_error())
+        except Exception as e:  # reported by the main thread
+            failures.append((i, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not failures, failures[:3]
+
+
 def test_forced_igemm_unsupported_is_reported(lib):
     d = x3.make_desc(2, 1, 16, 16, 9, 9, layout="NCHW", dtype="f16", kernel="igemm")  # W % 8 != 0
     assert _status(d) == x3.X3_ERR_UNSUPPORTED
