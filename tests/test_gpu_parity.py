@@ -87,7 +87,7 @@ NHWC_CASES = [(2, 16, 32, 20, 150, 1, "relu"), (1, 64, 64, 9, 300, 1, "none"), (
               (1, 64, 80, 19, 301, 1, "relu"), (2, 24, 24, 11, 40, 1, "none"), (1, 64, 8, 5, 260, 1, "relu"),
               (1, 136, 32, 7, 45, 1, "none"), (3, 16, 16, 6, 1, 1, "relu"),
               # 64 channels: each raster row leaves by one TMA store, clipped at a ragged right edge
-              (2, 32, 64, 7, 61, 1, "relu"),
+              (2, 32, 64, 7, 61, 1, "relu"), (1, 32, 48, 9, 70, 1, "clamp"),
               # 8 input channels: two taps per K step (five MMAs), 64 and 24 output channels
               (4, 8, 64, 37, 95, 1, "relu"), (1, 8, 24, 9, 31, 1, "none")]
 

@@ -316,6 +316,23 @@ __device__ __forceinline__ uint32_t cl_pack2(float lo, float hi) {
     }
 }
 
+// A packed pair of storage-type values clamped to [lo, hi] (packed bounds). Applied after rounding it
+// gives what the clamp before rounding gives: the rounding is monotonic and the bounds in use (0, -1,
+// 1, -inf, inf) are representable.
+template <bool BF16>
+__device__ __forceinline__ uint32_t cl_clamp2(uint32_t v, uint32_t lo, uint32_t hi) {
+    if (BF16) {
+        const __nv_bfloat162 r = __hmin2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v),
+                                                 *reinterpret_cast<const __nv_bfloat162*>(&lo)),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&hi));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+        const __half2 r = __hmin2(__hmax2(*reinterpret_cast<const __half2*>(&v), *reinterpret_cast<const __half2*>(&lo)),
+                                  *reinterpret_cast<const __half2*>(&hi));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
 // KWM (the conv_out head form): the MMA's M rows are (kw, output channel) triples, quarter g of the
 // 128 TMEM lanes holding kw*10 + r for channel 10g + r, so one MMA covers the three horizontal taps
 // of a row of the window and the K loop runs over (kt, kh, channel) only; the epilogue adds the three
@@ -870,6 +887,7 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
         }
         const float act_lo = a.act == X3_ACT_RELU ? 0.0f : (a.act == X3_ACT_CLAMP1 ? -1.0f : -INFINITY);
         const float act_hi = a.act == X3_ACT_CLAMP1 ? 1.0f : INFINITY;
+        const uint32_t act2_lo = cl_pack2<BF16>(act_lo, act_lo), act2_hi = cl_pack2<BF16>(act_hi, act_hi);  // TN
         const float inv_p = 1.0f / (float)a.P;
         if (TN) {  // this warp's copy of the bias (zero past C_out)
             float* sb = reinterpret_cast<float*>(sbase + (sBiasT - base)) + ew * a.tn_cp;
@@ -940,23 +958,30 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     }
                 };
                 auto sum = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16], const uint32_t (&v2)[16]) {
-                    float o[16];
+                    // two channels at a time: ((D0 + D1 shifted) + D2 shifted) + bias with packed fp32
+                    // adds (each half is the scalar add, in the same order), one rounding of the pair,
+                    // then the activation's clamp on the rounded pair (measured on the TAESD-like chain:
+                    // 0.114 ms with scalar adds and the clamp before rounding, 0.106 with the packed
+                    // pairs, 0.119 when the clamp branches on the activation kind)
+                    uint32_t h[8];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        if (TK) {
-                            o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + sb[16 * c + k], act_lo), act_hi);
-                        } else {
-                            const float s1 = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
-                            const float s2 = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
-                            o[k] = fminf(fmaxf(__uint_as_float(v0[k]) + s1 + s2 + sb[16 * c + k], act_lo), act_hi);
+                    for (int k = 0; k < 16; k += 2) {
+                        uint64_t s = ptx::f32x2(__uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
+                        if (!TK) {
+                            const float s1a = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k]), 1);
+                            const float s1b = __shfl_down_sync(0xffffffffu, __uint_as_float(v1[k + 1]), 1);
+                            const float s2a = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k]), 2);
+                            const float s2b = __shfl_down_sync(0xffffffffu, __uint_as_float(v2[k + 1]), 2);
+                            s = ptx::add_f32x2(s, ptx::f32x2(s1a, s1b));
+                            s = ptx::add_f32x2(s, ptx::f32x2(s2a, s2b));
                         }
+                        s = ptx::add_f32x2(s, *reinterpret_cast<const uint64_t*>(sb + 16 * c + k));
+                        float lo, hi;
+                        ptx::f32x2_split(s, lo, hi);
+                        h[k >> 1] = cl_clamp2<BF16>(cl_pack2<BF16>(lo, hi), act2_lo, act2_hi);
                     }
                     if (tma) {
-                        uint4 w0, w1;
-                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
-                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
-                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
-                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
+                        const uint4 w0 = make_uint4(h[0], h[1], h[2], h[3]), w1 = make_uint4(h[4], h[5], h[6], h[7]);
                         uint8_t* rowp = sbase + (ob - base) + lane * 128;
                         *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (lane & 7)) << 4)) = w0;
                         *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (lane & 7)) << 4)) = w1;
@@ -966,13 +991,9 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     if (a.out_nchw) {
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
-                            if (16 * c + k < a.C_out) yp[(size_t)(16 * c + k) * plane] = cl_round<BF16>(o[k]);
+                            if (16 * c + k < a.C_out) yp[(size_t)(16 * c + k) * plane] = (uint16_t)(h[k >> 1] >> (16 * (k & 1)));
                     } else {
-                        uint4 w0, w1;
-                        w0.x = cl_pack2<BF16>(o[0], o[1]);   w0.y = cl_pack2<BF16>(o[2], o[3]);
-                        w0.z = cl_pack2<BF16>(o[4], o[5]);   w0.w = cl_pack2<BF16>(o[6], o[7]);
-                        w1.x = cl_pack2<BF16>(o[8], o[9]);   w1.y = cl_pack2<BF16>(o[10], o[11]);
-                        w1.z = cl_pack2<BF16>(o[12], o[13]); w1.w = cl_pack2<BF16>(o[14], o[15]);
+                        const uint4 w0 = make_uint4(h[0], h[1], h[2], h[3]), w1 = make_uint4(h[4], h[5], h[6], h[7]);
                         *reinterpret_cast<uint4*>(yp + 16 * c) = w0;
                         if (16 * c + 8 < a.C_out) *reinterpret_cast<uint4*>(yp + 16 * c + 8) = w1;
                     }
