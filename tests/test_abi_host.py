@@ -411,9 +411,45 @@ def test_stencil_head_run_model_rejects_bad_runs():
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_igemm_plans_cover_their_reads(lib, name):
-    p = x3.conv_plan_create(x3.make_desc(**WORKLOADS[name]))
+    _check_plan_of(WORKLOADS[name])
+
+
+def _random_descs(n, seed):
+    """Seeded random stride-1 channels-last layers: causal 3D (NDHWC bf16) and 2D (NHWC, f16 or bf16),
+    channel counts around the engines' thresholds and tile sizes, ragged planes."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        if i % 3:
+            out.append(dict(dims=3, N=int(rng.integers(1, 4)), C_in=int(rng.choice([8, 16, 24, 40, 64, 96, 128, 136, 256, 320])),
+                            C_out=int(rng.choice([8, 16, 32, 64, 72, 96, 128, 136, 200, 256])), D=int(rng.integers(1, 7)),
+                            H=int(rng.integers(1, 400)), W=int(rng.integers(1, 700)),
+                            act=str(rng.choice(["none", "relu", "clamp"]))))
+        else:
+            out.append(dict(dims=2, N=int(rng.integers(1, 5)), C_in=int(rng.choice([8, 16, 24, 64, 136])),
+                            C_out=int(rng.choice([8, 16, 24, 48, 64, 80, 96, 128, 256])), H=int(rng.integers(1, 300)),
+                            W=int(rng.integers(1, 600)), layout="NHWC", dtype=str(rng.choice(["f16", "bf16"])),
+                            act=str(rng.choice(["none", "relu"]))))
+    return out
+
+
+def test_random_plans_cover_their_reads(lib):
+    """300 seeded random layers plan without error, and every tensor-core plan among them passes the
+    same geometry checks as the workloads above (staged halo covers every read, tiles cover the
+    output, shared memory and TMEM within their limits)."""
+    kinds = set()
+    for wl in _random_descs(300, seed=7500):
+        kinds.add(_check_plan_of(wl))
+    assert {"igemm_tcgen05_sw128", "tn"} <= kinds, kinds
+
+
+def _check_plan_of(wl):
+    """Plan the layer and check its geometry; returns the form checked."""
+    p = x3.conv_plan_create(x3.make_desc(**wl))
     try:
         g = x3.conv_plan_describe(p)
+        if g["kernel"] == "direct_simt":
+            return "direct_simt"
         if g.get("stn"):
             # stencil head: 32 x 8 raster windows (30 output columns), one stage per (kt, chunk)
             # holding the window (32 KB) and its weight block (16 KB); every CTA runs at most `windows`
@@ -422,19 +458,19 @@ def test_igemm_plans_cover_their_reads(lib, name):
             assert g["strips"] * 30 >= g["W_out"]
             assert g["h_bytes"] == 16 * 16 * 128 + 128 * 64 * 2 and g["smem_bytes"] <= 232448
             _check_stn_runs(g)
-            return
-        if WORKLOADS[name].get("kernel") == "head_two_pass":
+            return "stn"
+        if wl.get("kernel") == "head_two_pass":
             # the temporal pass stages no halo: windows of 256 consecutive positions of a frame, each
             # stage holding the window (32 KB) and its (kt, chunk) weight block (16 KB)
             assert g["P"] == g["Wt"] == g["W_out"] and g["strips"] == 1
             assert g["windows"] * 256 >= g["H_out"] * g["W_out"] and g["h_bytes"] == 256 * 128 + 128 * 64 * 2
             assert g["tiles"] == g["windows"] * g["frames"] and g["smem_bytes"] <= 232448
-            return
+            return "two_pass"
         if g["kernel"] in ("igemm_tcgen05_sw128", "igemm_tcgen05_sw128_head"):
             if g.get("tn"):
-                _check_tn_plan(g, WORKLOADS[name]["C_in"], WORKLOADS[name]["C_out"])
+                _check_tn_plan(g, wl["C_in"], wl["C_out"])
             _check_sw128_plan(g)
-            return
+            return "tn" if g.get("tn") else g["kernel"]
         assert g["kernel"] == "igemm_tcgen05"
         P, Rt, Wt, NSUB, spr = g["P"], g["Rt"], g["Wt"], g["NSUB"], g["spr"]
         assert P == Wt + 2 and P <= 256
@@ -454,6 +490,7 @@ def test_igemm_plans_cover_their_reads(lib, name):
         assert g["smem_bytes"] <= 232448
         assert g["tiles"] == g["col_tiles"] * g["row_tiles"] * g["frames"] * g["n_tiles"]
         assert g["col_tiles"] * Wt >= g["W_out"] and g["row_tiles"] * Rt >= g["H_out"]
+        return "igemm_tcgen05"
     finally:
         x3.conv_plan_destroy(p)
 
