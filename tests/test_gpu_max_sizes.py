@@ -146,6 +146,40 @@ def test_largest_plane_nchw_f16():
     assert_exact(got, ref, "f16")
 
 
+def fill_nhwc(x, rows=64):
+    """x [1, H, W, C] on the device <- hashed(c, 0, h, w)."""
+    _, H, W, C = x.shape
+    wi = torch.arange(W, device=x.device, dtype=torch.int64)[None, :, None]
+    ci = torch.arange(C, device=x.device, dtype=torch.int64)[None, None, :]
+    for h0 in range(0, H, rows):
+        hi = torch.arange(h0, min(h0 + rows, H), device=x.device, dtype=torch.int64)[:, None, None]
+        x[0, h0:h0 + rows] = hashed(ci, 0, hi, wi).to(x.dtype)
+
+
+def test_large_plane_nhwc_taps_in_n():
+    """A 64 -> 64 NHWC f16 layer over a 16384 x 16384 plane (2^28 positions, 34 GB in and 34 GB out) in
+    the positions-as-M form with the horizontal taps in N and row stores by TMA, past 2^32 bytes in both
+    tensors."""
+    H = W = 16384
+    C = 64
+    L = synth.make_layer([9140], 2, C, C, "f16", act="relu", variant="int")
+    conv = x3.Conv(x3.make_desc(2, 1, C, C, H, W, layout="NHWC", dtype="f16", act="relu"), dev(L.w), dev(L.b))
+    g = x3.conv_plan_describe(conv.plan)
+    assert conv.kernel_name == "igemm_tcgen05_sw128" and g["tn"] == 1 and g["tk"] == 0
+    x = torch.empty((1, H, W, C), dtype=torch.float16, device="cuda")
+    fill_nhwc(x)
+    y = conv(x)
+    del x
+    pos = positions_2d(H, W, 400, seed=9141)
+    hs = torch.tensor([p[0] for p in pos], device="cuda")
+    ws = torch.tensor([p[1] for p in pos], device="cuda")
+    got = host_values(y[0][hs, ws].contiguous(), "f16")
+    del y
+    ref = oracle.conv2d(windows_2d(pos, C, H, W), L.w.vals, L.b.vals, act="relu")[:, :, 1, 1]
+    assert got.shape == ref.shape == (len(pos), C)
+    assert_exact(got, ref, "f16")
+
+
 @pytest.mark.parametrize("C_in,C_out", [(65536, 16), (16, 65536)], ids=["cin65536", "cout65536"])
 def test_most_channels_nchw_f16(C_in, C_out):
     """The most input channels (1024 staged 64-channel chunks per tile) and the most output channels
