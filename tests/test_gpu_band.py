@@ -5,7 +5,6 @@ the plane skipped). Bands of one plane, concatenated, must equal the whole plane
 and on integer data the whole plane equals the oracle. Each engine and form is covered: the channels-
 last tensor-core engine (128-row, positions-as-M, M = 64, NCHW, stencil head, single-pass head), the
 positions-as-M engine of 3D layers with fewer than 96 output channels, and the direct kernel."""
-import numpy as np
 import pytest
 import torch
 

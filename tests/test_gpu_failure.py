@@ -1,6 +1,5 @@
 """Failure detection on the GPU without faulting it: a bounded device wait that runs out reports
 X3_ERR_TIMEOUT through the device status word and leaves the context usable."""
-import numpy as np
 import pytest
 import torch
 

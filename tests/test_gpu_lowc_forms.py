@@ -9,7 +9,6 @@ integer data and within the tolerances on random data:
 * both in banded mode at a band's top, middle and bottom.
 The definition is the TAESD conv page's taesd_conv3x3_impl (pad-1 3x3 cross-correlation, bias-
 initialised fp32 accumulator, ReLU, one rounding at the store)."""
-import numpy as np
 import pytest
 import torch
 

@@ -56,9 +56,6 @@ def hashed(c, f, h, w):
     return ((k * 40503) >> 11) % 3 - 1
 
 
-TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
-
-
 def fill_nchw(x, rows=1024):
     """x [1, C, H, W] on the device <- hashed(c, 0, h, w)."""
     _, C, H, W = x.shape

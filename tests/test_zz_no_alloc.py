@@ -8,7 +8,6 @@ that contents the shared buffer keeps from the first call cannot leak into the s
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
