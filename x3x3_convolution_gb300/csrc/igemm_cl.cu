@@ -1000,6 +1000,24 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                 };
                 {
                     uint32_t a0[16], a1[16], a2[16], b0[16], b1[16], b2[16];
+                    if constexpr (TK) {
+                        // one TMEM value per output: every chunk's load (at most five: 80 channels) goes
+                        // out before a single wait, and the buffer goes back before any sum
+                        ptx::tmem_ld16(tq, a0);
+                        if (nck > 1) ptx::tmem_ld16(tq + 16u, b0);
+                        if (nck > 2) ptx::tmem_ld16(tq + 32u, a1);
+                        if (nck > 3) ptx::tmem_ld16(tq + 48u, b1);
+                        if (nck > 4) ptx::tmem_ld16(tq + 64u, a2);
+                        ptx::tmem_ld_wait();
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar_acc_empty + 8 * ab);
+                        sum(0, a0, a1, a2);
+                        if (nck > 1) sum(1, b0, b1, b2);
+                        if (nck > 2) sum(2, a1, a1, a2);
+                        if (nck > 3) sum(3, b1, b1, b2);
+                        if (nck > 4) sum(4, a2, a1, a2);
+                    } else
                     for (int c = 0; c < nck; c += 2) {
                         load(c, a0, a1, a2);
                         if (c + 1 < nck) load(c + 1, b0, b1, b2);
