@@ -1308,16 +1308,21 @@ __global__ void __launch_bounds__((NC || TN) ? 320 : 192, 1)
                     // Each warp transposes its own 32 channels x 32 positions through a private staging
                     // block (no barrier across warps), then writes 64 contiguous bytes per position row.
                     uint8_t* wst = stage_ptr + ew * a.stage_warp;
-                    // W2: the two windows of the tile, accumulators in TMEM columns 0-255 and 256-511
-                    for (int chunk = 0; chunk < (W2 ? 2 : 1) * (kBNP / 32); ++chunk) {
-                        uint32_t v[32];
-                        ptx::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP + (uint32_t)(chunk * 32), v);
+                    // W2: the two windows of the tile, accumulators in TMEM columns 0-255 and 256-511.
+                    // A chunk's TMEM load goes out as soon as the previous chunk is staged, so it lands
+                    // while that chunk's rows are written out.
+                    constexpr int n_ck = (W2 ? 2 : 1) * (kBNP / 32);
+                    const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBNP;
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tq, v);
+                    for (int chunk = 0; chunk < n_ck; ++chunk) {
                         ptx::tmem_ld_wait();
                         __syncwarp();
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             *reinterpret_cast<uint16_t*>(wst + j * kStagePitch + lane * 2) =
                                 cl_round<BF16>(cl_act(__uint_as_float(v[j]) + bias_r, a.act));
+                        if (chunk + 1 < n_ck) ptx::tmem_ld32(tq + (uint32_t)((chunk + 1) * 32), v);
                         __syncwarp();
 #pragma unroll
                         for (int k = 0; k < (M64 ? 2 : 4); ++k) {
